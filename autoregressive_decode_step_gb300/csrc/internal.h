@@ -1,0 +1,173 @@
+// Internal interfaces between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "../../include/decode_step.h"
+
+namespace ds {
+
+// Every workspace starts with this header; the error word is at byte 0.
+constexpr size_t kWsHeader = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// SM count of the current device (cached per device).
+int sm_count();
+
+// Launch `kernel` with cudaLaunchKernelEx; `pdl` adds the programmatic
+// stream-serialisation attribute so the kernel may begin while its
+// predecessor on the stream finishes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, bool pdl, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ------------------------------------------------------------------ GEMV
+enum Pro { PRO_PLAIN = 0, PRO_RMSNORM = 1 };
+enum Epi { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU = 2, EPI_QKV = 3 };
+
+// Bytes of one band's row segment in shared memory, rows per pipeline stage
+// and stages of the transposed GEMV's ring.
+constexpr int kGtBandBytes = 512;
+constexpr int kGtRows = 32;
+constexpr int kGtStages = 6;
+constexpr int kGtConsumerWarps = 8;
+
+struct GemvTArgs {
+    const char *a0;       // element (k, c) of sub-tile 0 at a0 + k*row_stride + c*es
+    const char *a1;       // sub-tile 1 (the up columns for EPI_SILU) or nullptr
+    long long row_stride; // bytes between consecutive rows
+    int K;                // reduced dimension (rows)
+    int sub_cols;         // columns of each sub-tile source
+    int n_bands;
+    const float *x;       // PRO_PLAIN: x[K]; PRO_RMSNORM: the residual [K]
+    const float *norm_w;  // PRO_RMSNORM weight [K] (fp32)
+    float eps;
+    float *partials;      // (grid + n_bands) * band_cols floats
+    int *counters;        // n_bands ints, zero between launches
+    int *err;
+    float *y;             // STORE/ADD: y[sub_cols]; SILU: f[sub_cols]; QKV: q out
+    // EPI_QKV: RoPE on the q and k columns, K/V written at position pos[0]
+    // of sequence 0.
+    void *k_cache;
+    void *v_cache;
+    int kv_dtype;
+    const int *pos;
+    int nq_cols, nkv_cols, head_dim, rope_layout;
+    const float *rope_cos, *rope_sin;  // [rope_rows][head_dim / 2]
+    int rope_rows;
+    const int *block_table;
+    int block_tokens, max_blocks;
+};
+
+// Columns of one band (partial sums per band) for an element size.
+inline int gemv_t_band_cols(int es) { return kGtBandBytes / es; }
+int gemv_t_grid(int K, int n_bands);
+size_t gemv_t_partial_floats(int grid, int n_bands, int es);
+// Can the bulk-copy kernel stream this matrix?
+bool gemv_t_streamable(const void *a0, const void *a1, long long row_stride, int sub_cols, int es);
+cudaError_t launch_gemv_t(const GemvTArgs &a, int dtype, int pro, int epi, int grid,
+                          cudaStream_t stream, bool pdl);
+
+struct GemvNArgs {
+    const char *W;        // [rows][cols]
+    int rows, cols;
+    const float *x;       // PRO_PLAIN: x[cols]; PRO_RMSNORM: the residual [cols]
+    const float *norm_w;
+    float eps;
+    float *y;             // [rows]
+    // fused greedy argmax over the rows (do_argmax != 0)
+    int do_argmax;
+    float *part_val;      // [grid]
+    int *part_idx;        // [grid]
+    int *counter;         // 1 int, zero between launches
+    int *ids_out;         // 1 int
+    float *max_out;       // 1 float or nullptr
+    int *tokens_adv;      // DS_STEP_ADVANCE targets or nullptr
+    int *pos_adv;
+    int *err;
+};
+int gemv_n_grid(int rows, int cols, int es);
+bool gemv_n_streamable(const void *W, int cols, int es);
+cudaError_t launch_gemv_n(const GemvNArgs &a, int dtype, int pro, int grid, cudaStream_t stream,
+                          bool pdl);
+
+// ------------------------------------------------------------------ attention
+struct AttnArgs {
+    const float *q;       // [n_seqs][n_qh * hd]
+    const void *k_cache;
+    const void *v_cache;
+    int kv_dtype;
+    long long cache_rows;
+    const int *block_table;
+    int max_blocks, block_tokens;
+    const int *seq_lens;  // [n_seqs] or nullptr (then n_ctx = pos[s] + 1)
+    const int *pos;
+    int n_qh, n_kvh, hd;
+    float scale;
+    float *out;           // [n_seqs][n_qh * hd]
+    float *partials;
+    int *counters;        // n_seqs * n_kvh ints, zero between launches
+    int *err;
+    int n_splits;
+};
+int attention_splits(int n_seqs, int n_kvh, long long max_ctx);
+size_t attention_partial_floats(int n_seqs, int n_qh, int n_kvh, int hd, int n_splits);
+cudaError_t launch_attention(const AttnArgs &a, int n_seqs, cudaStream_t stream, bool pdl);
+
+// ------------------------------------------------------------------ small ops
+cudaError_t launch_embed(const void *emb, int w_dtype, int vocab, int d, const int *tokens,
+                         float *x, int *err, int n_seqs, cudaStream_t stream, bool pdl);
+cudaError_t launch_rope_table(float *cos_t, float *sin_t, int rows, int head_dim, double base,
+                              cudaStream_t stream);
+
+// ------------------------------------------------------------------ picking
+struct ArgmaxArgs {
+    const float *logits;
+    int n_rows;
+    long long n;
+    int *ids;
+    float *max_logit;
+    float *part_val;
+    int *part_idx;
+    int *counters;        // n_rows ints
+    int *tokens_adv, *pos_adv;
+    int *err;
+    int blocks_per_row;
+};
+int argmax_blocks_per_row(long long n);
+cudaError_t launch_argmax(const ArgmaxArgs &a, cudaStream_t stream, bool pdl);
+
+struct SampleArgs {
+    const float *logits;
+    int n_rows;
+    long long n;
+    float temperature;
+    int top_k;
+    float top_p;
+    const float *u;
+    int *ids;
+    int *tokens_adv, *pos_adv;
+    int *err;
+};
+cudaError_t launch_sample(const SampleArgs &a, cudaStream_t stream, bool pdl);
+
+}  // namespace ds

@@ -1,0 +1,520 @@
+// The decode step: model object, workspace layout, the per-step launch
+// sequence, CUDA-graph capture and per-kernel timing.
+//
+// Per layer the step launches five kernels ("The forward pass end to end",
+// "What a forward step does"; "Inside the engine", section 1):
+//   1. fused q|k|v projection with RMSNorm in its prologue and RoPE + the K/V
+//      cache write in its epilogue (qkPrep);
+//   2. split-context grouped-query attention with its cross-split reduce;
+//   3. output projection with the residual add in its epilogue;
+//   4. fused gate|up projection with RMSNorm in its prologue and SiLU-gate in
+//      its epilogue;
+//   5. down projection with the residual add in its epilogue;
+// then the output head with the final RMSNorm in its prologue and the greedy
+// argmax fused in (or the sampler after it).  Every kernel is launched with
+// programmatic dependent launch, so each one's weight stream starts while its
+// predecessor drains.
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ds {
+cudaError_t prepare_kernels();
+}
+
+struct ds_model {
+    ds_model_config cfg;
+    const void *emb, *out;
+    const float *final_norm;
+    std::vector<const float *> n1, n2;
+    std::vector<const void *> wqkv, wo, wgu, wd;
+    char *ws;
+    size_t ws_bytes;
+    int *err;
+    float *x, *q, *att, *f, *logits, *rope_cos, *rope_sin;
+    int *g_counters;
+    float *g_partials;
+    int *a_counters;
+    float *a_partials;
+    float *am_val;
+    int *am_idx;
+    int *am_counter;
+    int grid_qkv, grid_o, grid_gu, grid_d, grid_head;
+    int nb_qkv, nb_o, nb_gu, nb_d;
+    int attn_splits;
+    int es;
+};
+
+struct ds_step_graph {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+namespace {
+
+using namespace ds;
+
+struct Layout {
+    size_t x, q, att, f, logits, rope_cos, rope_sin, g_counters, g_partials, a_counters, a_partials, am_val,
+        am_idx, am_counter, total;
+    int grid_qkv, grid_o, grid_gu, grid_d, grid_head, nb_qkv, nb_o, nb_gu, nb_d, attn_splits;
+};
+
+int validate(const ds_model_config *c) {
+    if (!c) return DS_BAD_ARGUMENT;
+    if (c->vocab < 1 || c->d < 1 || c->n_layer < 0 || c->n_qh < 1 || c->n_kvh < 1 || c->head_dim < 2 || c->ff < 1 ||
+        c->max_seqs < 1 || c->max_ctx < 1)
+        return DS_EMPTY_DIMENSION;
+    if (c->vocab > DS_MAX_DIM || c->d > DS_MAX_DIM || c->ff > DS_MAX_DIM || c->max_ctx > DS_MAX_DIM ||
+        (int64_t)c->n_qh * c->head_dim > DS_MAX_DIM)
+        return DS_DIMENSION_TOO_LARGE;
+    if ((c->w_dtype != DS_F32 && c->w_dtype != DS_BF16) || (c->kv_dtype != DS_F32 && c->kv_dtype != DS_BF16) ||
+        (c->rope_layout != DS_ROPE_HALF_SPLIT && c->rope_layout != DS_ROPE_INTERLEAVED))
+        return DS_BAD_DTYPE;
+    const int gq = c->n_qh / c->n_kvh;
+    if (c->n_qh % c->n_kvh || (gq != 1 && gq != 2 && gq != 4 && gq != 8)) return DS_BAD_ARGUMENT;
+    if (c->head_dim % 4 || c->head_dim > 256 || (c->head_dim > 128 && c->head_dim % 8)) return DS_BAD_ARGUMENT;
+    const int es = c->w_dtype == DS_BF16 ? 2 : 4;
+    // every projection streams whole 16-byte chunks; a band holds whole heads
+    if (((int64_t)c->d * es) % 16 || ((int64_t)c->ff * es) % 16 || ((int64_t)c->n_qh * c->head_dim * es) % 16 ||
+        ((int64_t)c->n_kvh * c->head_dim * es) % 16)
+        return DS_BAD_ARGUMENT;
+    if (gemv_t_band_cols(es) % c->head_dim) return DS_BAD_ARGUMENT;
+    if (!gemv_n_streamable(nullptr, c->d, es)) return DS_BAD_ARGUMENT;
+    if (!(c->eps >= 0.0f) || !(c->rope_base > 0.0)) return DS_BAD_ARGUMENT;
+    if (c->max_seqs != 1) return DS_BAD_ARGUMENT;  // batch-1 path
+    return DS_OK;
+}
+
+size_t carve(size_t &off, size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+}
+
+Layout make_layout(const ds_model_config *c) {
+    Layout L = {};
+    const int es = c->w_dtype == DS_BF16 ? 2 : 4;
+    const int bc = gemv_t_band_cols(es);
+    const int nq = c->n_qh * c->head_dim, nkv = c->n_kvh * c->head_dim;
+    const int S = c->max_seqs;
+    L.nb_qkv = (nq + 2 * nkv + bc - 1) / bc;
+    L.nb_o = (c->d + bc - 1) / bc;
+    L.nb_gu = (c->ff + bc / 2 - 1) / (bc / 2);
+    L.nb_d = (c->d + bc - 1) / bc;
+    L.grid_qkv = gemv_t_grid(c->d, L.nb_qkv);
+    L.grid_o = gemv_t_grid(nq, L.nb_o);
+    L.grid_gu = gemv_t_grid(c->d, L.nb_gu);
+    L.grid_d = gemv_t_grid(c->ff, L.nb_d);
+    L.grid_head = gemv_n_grid(c->vocab, c->d, es);
+    L.attn_splits = attention_splits(S, c->n_kvh, c->max_ctx);
+    size_t partial = 0;
+    partial = std::max(partial, gemv_t_partial_floats(L.grid_qkv, L.nb_qkv, es));
+    partial = std::max(partial, gemv_t_partial_floats(L.grid_o, L.nb_o, es));
+    partial = std::max(partial, gemv_t_partial_floats(L.grid_gu, L.nb_gu, es));
+    partial = std::max(partial, gemv_t_partial_floats(L.grid_d, L.nb_d, es));
+    const int max_bands = std::max(std::max(L.nb_qkv, L.nb_o), std::max(L.nb_gu, L.nb_d));
+    size_t off = kWsHeader;
+    L.x = carve(off, (size_t)S * c->d * 4);
+    L.q = carve(off, (size_t)S * nq * 4);
+    L.att = carve(off, (size_t)S * nq * 4);
+    L.f = carve(off, (size_t)S * c->ff * 4);
+    L.logits = carve(off, (size_t)S * c->vocab * 4);
+    L.rope_cos = carve(off, (size_t)c->max_ctx * (c->head_dim / 2) * 4);
+    L.rope_sin = carve(off, (size_t)c->max_ctx * (c->head_dim / 2) * 4);
+    L.g_counters = carve(off, (size_t)max_bands * 4);
+    L.g_partials = carve(off, partial * 4);
+    L.a_counters = carve(off, (size_t)S * c->n_kvh * 4);
+    L.a_partials = carve(off, attention_partial_floats(S, c->n_qh, c->n_kvh, c->head_dim, L.attn_splits) * 4);
+    L.am_val = carve(off, (size_t)L.grid_head * 4);
+    L.am_idx = carve(off, (size_t)L.grid_head * 4);
+    L.am_counter = carve(off, 4);
+    L.total = off;
+    return L;
+}
+
+int check_kv(const ds_model *m, const ds_kv_cache *kv) {
+    if (!kv || !kv->k || !kv->v) return DS_BAD_ARGUMENT;
+    if (kv->block_tokens < 1 || kv->max_blocks < 1 || kv->rows < 1) return DS_EMPTY_DIMENSION;
+    const int64_t cap = (int64_t)kv->block_tokens * kv->max_blocks;
+    if (cap > DS_MAX_DIM) return DS_DIMENSION_TOO_LARGE;
+    if (!kv->block_table && cap * m->cfg.max_seqs > kv->rows) return DS_CACHE_CAPACITY_EXCEEDED;
+    const int es = m->cfg.kv_dtype == DS_BF16 ? 2 : 4;
+    for (int l = 0; l < m->cfg.n_layer; ++l) {
+        if (!kv->k[l] || !kv->v[l]) return DS_BAD_ARGUMENT;
+        if (((uintptr_t)kv->k[l] | (uintptr_t)kv->v[l]) & 15) return DS_BAD_ARGUMENT;
+    }
+    (void)es;
+    return DS_OK;
+}
+
+// Optional per-launch event recorder used by the profiler.
+struct Recorder {
+    std::vector<cudaEvent_t> ev;
+    std::vector<int> kind;
+    size_t used = 0;
+    cudaStream_t stream;
+    bool record(int k) {
+        if (used >= ev.size()) {
+            cudaEvent_t e;
+            if (cudaEventCreate(&e) != cudaSuccess) return false;
+            ev.push_back(e);
+            kind.push_back(k);
+        }
+        kind[used] = k;
+        return cudaEventRecord(ev[used++], stream) == cudaSuccess;
+    }
+    ~Recorder() {
+        for (auto e : ev) cudaEventDestroy(e);
+    }
+};
+
+int run_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
+             const ds_sampling *sampling, const float *u, int32_t *next_ids, float *logits_out, unsigned flags,
+             cudaStream_t s, Recorder *rec) {
+    const ds_model_config &c = m->cfg;
+    const int es = m->es;
+    const int nq = c.n_qh * c.head_dim, nkv = c.n_kvh * c.head_dim;
+    const bool pdl = rec == nullptr;
+    const bool greedy = sampling == nullptr || !(sampling->temperature > 0.0f);
+    const bool advance = (flags & DS_STEP_ADVANCE) != 0;
+    float *logits = logits_out ? logits_out : m->logits;
+    cudaError_t e;
+#define DS_TRY(expr, kind)                              \
+    do {                                                \
+        e = (expr);                                     \
+        if (e != cudaSuccess) return DS_CUDA_ERROR;     \
+        if (rec && !rec->record(kind)) return DS_CUDA_ERROR; \
+    } while (0)
+
+    if (rec && !rec->record(-1)) return DS_CUDA_ERROR;
+    DS_TRY(launch_embed(m->emb, c.w_dtype, c.vocab, c.d, tokens, m->x, m->err, n_seqs, s, pdl), DS_KIND_EMBED);
+
+    GemvTArgs g = {};
+    g.err = m->err;
+    g.counters = m->g_counters;
+    g.partials = m->g_partials;
+    g.eps = c.eps;
+    for (int l = 0; l < c.n_layer; ++l) {
+        // 1. q|k|v = Wqkv^T RMSNorm(x, n1); RoPE; K/V written at pos
+        GemvTArgs a = g;
+        a.a0 = static_cast<const char *>(m->wqkv[l]);
+        a.row_stride = (long long)(nq + 2 * nkv) * es;
+        a.K = c.d;
+        a.sub_cols = nq + 2 * nkv;
+        a.n_bands = m->nb_qkv;
+        a.x = m->x;
+        a.norm_w = m->n1[l];
+        a.y = m->q;
+        a.k_cache = kv->k[l];
+        a.v_cache = kv->v[l];
+        a.kv_dtype = c.kv_dtype;
+        a.pos = pos;
+        a.nq_cols = nq;
+        a.nkv_cols = nkv;
+        a.head_dim = c.head_dim;
+        a.rope_layout = c.rope_layout;
+        a.rope_cos = m->rope_cos;
+        a.rope_sin = m->rope_sin;
+        a.rope_rows = c.max_ctx;
+        a.block_table = kv->block_table;
+        a.block_tokens = kv->block_tokens;
+        a.max_blocks = kv->max_blocks;
+        DS_TRY(launch_gemv_t(a, c.w_dtype, PRO_RMSNORM, EPI_QKV, m->grid_qkv, s, pdl), DS_KIND_QKV);
+
+        // 2. attention over positions 0..pos
+        AttnArgs at = {};
+        at.q = m->q;
+        at.k_cache = kv->k[l];
+        at.v_cache = kv->v[l];
+        at.kv_dtype = c.kv_dtype;
+        at.cache_rows = kv->rows;
+        at.block_table = kv->block_table;
+        at.max_blocks = kv->max_blocks;
+        at.block_tokens = kv->block_tokens;
+        at.seq_lens = nullptr;
+        at.pos = pos;
+        at.n_qh = c.n_qh;
+        at.n_kvh = c.n_kvh;
+        at.hd = c.head_dim;
+        at.scale = 1.0f / sqrtf((float)c.head_dim);
+        at.out = m->att;
+        at.partials = m->a_partials;
+        at.counters = m->a_counters;
+        at.err = m->err;
+        at.n_splits = m->attn_splits;
+        DS_TRY(launch_attention(at, n_seqs, s, pdl), DS_KIND_ATTENTION);
+
+        // 3. x += Wo^T att
+        a = g;
+        a.a0 = static_cast<const char *>(m->wo[l]);
+        a.row_stride = (long long)c.d * es;
+        a.K = nq;
+        a.sub_cols = c.d;
+        a.n_bands = m->nb_o;
+        a.x = m->att;
+        a.y = m->x;
+        DS_TRY(launch_gemv_t(a, c.w_dtype, PRO_PLAIN, EPI_ADD, m->grid_o, s, pdl), DS_KIND_O_PROJ);
+
+        // 4. f = silu(Wg^T h) * (Wu^T h), h = RMSNorm(x, n2)
+        a = g;
+        a.a0 = static_cast<const char *>(m->wgu[l]);
+        a.a1 = static_cast<const char *>(m->wgu[l]) + (size_t)c.ff * es;
+        a.row_stride = (long long)2 * c.ff * es;
+        a.K = c.d;
+        a.sub_cols = c.ff;
+        a.n_bands = m->nb_gu;
+        a.x = m->x;
+        a.norm_w = m->n2[l];
+        a.y = m->f;
+        DS_TRY(launch_gemv_t(a, c.w_dtype, PRO_RMSNORM, EPI_SILU, m->grid_gu, s, pdl), DS_KIND_GATE_UP);
+
+        // 5. x += Wd^T f
+        a = g;
+        a.a0 = static_cast<const char *>(m->wd[l]);
+        a.row_stride = (long long)c.d * es;
+        a.K = c.ff;
+        a.sub_cols = c.d;
+        a.n_bands = m->nb_d;
+        a.x = m->f;
+        a.y = m->x;
+        DS_TRY(launch_gemv_t(a, c.w_dtype, PRO_PLAIN, EPI_ADD, m->grid_d, s, pdl), DS_KIND_DOWN);
+    }
+
+    // logits = Out . RMSNorm(x, final); greedy argmax fused
+    GemvNArgs h = {};
+    h.W = static_cast<const char *>(c.tied ? m->emb : m->out);
+    h.rows = c.vocab;
+    h.cols = c.d;
+    h.x = m->x;
+    h.norm_w = m->final_norm;
+    h.eps = c.eps;
+    h.y = logits;
+    h.do_argmax = greedy ? 1 : 0;
+    h.part_val = m->am_val;
+    h.part_idx = m->am_idx;
+    h.counter = m->am_counter;
+    h.ids_out = next_ids;
+    h.max_out = nullptr;
+    h.tokens_adv = advance ? tokens : nullptr;
+    h.pos_adv = advance ? pos : nullptr;
+    h.err = m->err;
+    DS_TRY(launch_gemv_n(h, c.w_dtype, PRO_RMSNORM, m->grid_head, s, pdl), DS_KIND_HEAD);
+
+    if (!greedy) {
+        SampleArgs sa = {};
+        sa.logits = logits;
+        sa.n_rows = n_seqs;
+        sa.n = c.vocab;
+        sa.temperature = sampling->temperature;
+        sa.top_k = sampling->top_k;
+        sa.top_p = sampling->top_p;
+        sa.u = u;
+        sa.ids = next_ids;
+        sa.tokens_adv = advance ? tokens : nullptr;
+        sa.pos_adv = advance ? pos : nullptr;
+        sa.err = m->err;
+        DS_TRY(launch_sample(sa, s, pdl), DS_KIND_SAMPLE);
+    }
+#undef DS_TRY
+    return DS_OK;
+}
+
+int check_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
+               const ds_sampling *sampling, const float *u, int32_t *next_ids) {
+    if (!m) return DS_BAD_ARGUMENT;
+    if (n_seqs < 1) return DS_EMPTY_DIMENSION;
+    if (n_seqs > m->cfg.max_seqs) return DS_DIMENSION_TOO_LARGE;
+    if (!tokens || !pos || !next_ids) return DS_BAD_ARGUMENT;
+    int st = check_kv(m, kv);
+    if (st != DS_OK) return st;
+    if (sampling && sampling->temperature > 0.0f) {
+        const int64_t V = m->cfg.vocab;
+        const int64_t k_eff = (sampling->top_k <= 0 || sampling->top_k >= V) ? V : sampling->top_k;
+        if (k_eff > DS_SAMPLE_MAX_TOP_K || !(sampling->top_p > 0.0f) || sampling->top_p > 1.0f)
+            return DS_BAD_SAMPLING_PARAM;
+        if (!u) return DS_BAD_ARGUMENT;
+    } else if (sampling && sampling->temperature != sampling->temperature) {
+        return DS_BAD_SAMPLING_PARAM;
+    }
+    return DS_OK;
+}
+
+}  // namespace
+
+extern "C" DS_API size_t ds_model_workspace_bytes(const ds_model_config *cfg) {
+    if (validate(cfg) != DS_OK) return 0;
+    return make_layout(cfg).total;
+}
+
+extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model_weights *w, void *workspace,
+                                      size_t workspace_bytes, ds_model **out) {
+    if (!out) return DS_BAD_ARGUMENT;
+    *out = nullptr;
+    int st = validate(cfg);
+    if (st != DS_OK) return st;
+    if (!w || !w->emb || (!cfg->tied && !w->out) || !w->final_norm) return DS_BAD_ARGUMENT;
+    if (cfg->n_layer > 0 && (!w->n1 || !w->wqkv || !w->wo || !w->n2 || !w->wgu || !w->wd)) return DS_BAD_ARGUMENT;
+    const Layout L = make_layout(cfg);
+    if (!workspace || workspace_bytes < L.total) return DS_WORKSPACE_TOO_SMALL;
+    if ((uintptr_t)workspace & 255) return DS_BAD_ARGUMENT;
+    auto aligned = [](const void *p) { return p && ((uintptr_t)p & 15) == 0; };
+    if (!aligned(w->emb) || (!cfg->tied && !aligned(w->out))) return DS_BAD_ARGUMENT;
+    for (int l = 0; l < cfg->n_layer; ++l)
+        if (!aligned(w->wqkv[l]) || !aligned(w->wo[l]) || !aligned(w->wgu[l]) || !aligned(w->wd[l]) || !w->n1[l] ||
+            !w->n2[l])
+            return DS_BAD_ARGUMENT;
+
+    ds_model *m = new (std::nothrow) ds_model();
+    if (!m) return DS_BAD_ARGUMENT;
+    m->cfg = *cfg;
+    m->es = cfg->w_dtype == DS_BF16 ? 2 : 4;
+    m->emb = w->emb;
+    m->out = cfg->tied ? w->emb : w->out;
+    m->final_norm = w->final_norm;
+    for (int l = 0; l < cfg->n_layer; ++l) {
+        m->n1.push_back(w->n1[l]);
+        m->n2.push_back(w->n2[l]);
+        m->wqkv.push_back(w->wqkv[l]);
+        m->wo.push_back(w->wo[l]);
+        m->wgu.push_back(w->wgu[l]);
+        m->wd.push_back(w->wd[l]);
+    }
+    char *ws = static_cast<char *>(workspace);
+    m->ws = ws;
+    m->ws_bytes = workspace_bytes;
+    m->err = reinterpret_cast<int *>(ws);
+    m->x = reinterpret_cast<float *>(ws + L.x);
+    m->q = reinterpret_cast<float *>(ws + L.q);
+    m->att = reinterpret_cast<float *>(ws + L.att);
+    m->f = reinterpret_cast<float *>(ws + L.f);
+    m->logits = reinterpret_cast<float *>(ws + L.logits);
+    m->rope_cos = reinterpret_cast<float *>(ws + L.rope_cos);
+    m->rope_sin = reinterpret_cast<float *>(ws + L.rope_sin);
+    m->g_counters = reinterpret_cast<int *>(ws + L.g_counters);
+    m->g_partials = reinterpret_cast<float *>(ws + L.g_partials);
+    m->a_counters = reinterpret_cast<int *>(ws + L.a_counters);
+    m->a_partials = reinterpret_cast<float *>(ws + L.a_partials);
+    m->am_val = reinterpret_cast<float *>(ws + L.am_val);
+    m->am_idx = reinterpret_cast<int *>(ws + L.am_idx);
+    m->am_counter = reinterpret_cast<int *>(ws + L.am_counter);
+    m->grid_qkv = L.grid_qkv;
+    m->grid_o = L.grid_o;
+    m->grid_gu = L.grid_gu;
+    m->grid_d = L.grid_d;
+    m->grid_head = L.grid_head;
+    m->nb_qkv = L.nb_qkv;
+    m->nb_o = L.nb_o;
+    m->nb_gu = L.nb_gu;
+    m->nb_d = L.nb_d;
+    m->attn_splits = L.attn_splits;
+
+    if (prepare_kernels() != cudaSuccess || cudaMemset(workspace, 0, L.total) != cudaSuccess ||
+        launch_rope_table(m->rope_cos, m->rope_sin, cfg->max_ctx, cfg->head_dim, cfg->rope_base, nullptr) !=
+            cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        delete m;
+        return DS_CUDA_ERROR;
+    }
+    *out = m;
+    return DS_OK;
+}
+
+extern "C" DS_API void ds_model_destroy(ds_model *m) { delete m; }
+
+extern "C" DS_API void *ds_model_workspace(ds_model *m) { return m ? m->ws : nullptr; }
+
+extern "C" DS_API int ds_decode_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
+                                     const ds_sampling *sampling, const float *u, int32_t *next_ids,
+                                     float *logits_out, unsigned flags, ds_stream_t stream) {
+    int st = check_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids);
+    if (st != DS_OK) return st;
+    return run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags,
+                    reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" DS_API int ds_step_graph_create(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos,
+                                           int n_seqs, const ds_sampling *sampling, const float *u,
+                                           int32_t *next_ids, float *logits_out, unsigned flags, ds_stream_t stream,
+                                           ds_step_graph **out) {
+    if (!out) return DS_BAD_ARGUMENT;
+    *out = nullptr;
+    int st = check_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids);
+    if (st != DS_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!s) return DS_BAD_ARGUMENT;  // the legacy stream cannot be captured
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return DS_CUDA_ERROR;
+    st = run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s, nullptr);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s, &graph);
+    if (st != DS_OK || e != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        cudaGetLastError();
+        return st != DS_OK ? st : DS_CUDA_ERROR;
+    }
+    cudaGraphExec_t exec = nullptr;
+    if (cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        return DS_CUDA_ERROR;
+    }
+    ds_step_graph *g = new (std::nothrow) ds_step_graph();
+    if (!g) {
+        cudaGraphExecDestroy(exec);
+        cudaGraphDestroy(graph);
+        return DS_BAD_ARGUMENT;
+    }
+    g->graph = graph;
+    g->exec = exec;
+    *out = g;
+    return DS_OK;
+}
+
+extern "C" DS_API int ds_step_graph_launch(ds_step_graph *g, ds_stream_t stream) {
+    if (!g) return DS_BAD_ARGUMENT;
+    return cudaGraphLaunch(g->exec, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DS_OK : DS_CUDA_ERROR;
+}
+
+extern "C" DS_API void ds_step_graph_destroy(ds_step_graph *g) {
+    if (!g) return;
+    cudaGraphExecDestroy(g->exec);
+    cudaGraphDestroy(g->graph);
+    delete g;
+}
+
+extern "C" DS_API int ds_decode_step_profile(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos,
+                                             int n_seqs, const ds_sampling *sampling, const float *u,
+                                             int32_t *next_ids, float *logits_out, unsigned flags, int reps,
+                                             float *ms_out, int32_t *kinds_out, int cap, int *n_out,
+                                             ds_stream_t stream) {
+    if (reps < 1 || !ms_out || !kinds_out || !n_out || cap < 1) return DS_BAD_ARGUMENT;
+    int st = check_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids);
+    if (st != DS_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    Recorder rec;
+    rec.stream = s;
+    std::vector<double> sum;
+    int slots = 0;
+    for (int r = 0; r < reps; ++r) {
+        rec.used = 0;
+        st = run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s, &rec);
+        if (st != DS_OK) return st;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return DS_CUDA_ERROR;
+        slots = (int)rec.used - 1;
+        if (sum.empty()) sum.assign(slots, 0.0);
+        for (int i = 0; i < slots; ++i) {
+            float ms = 0.0f;
+            if (cudaEventElapsedTime(&ms, rec.ev[i], rec.ev[i + 1]) != cudaSuccess) return DS_CUDA_ERROR;
+            sum[i] += ms;
+        }
+    }
+    const int n = std::min(cap, slots);
+    for (int i = 0; i < n; ++i) {
+        ms_out[i] = (float)(sum[i] / reps);
+        kinds_out[i] = rec.kind[i + 1];
+    }
+    *n_out = n;
+    return DS_OK;
+}

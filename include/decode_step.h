@@ -1,0 +1,387 @@
+/*
+ * decode_step.h — C ABI of the GB300 (sm_103a) single-token decode step.
+ *
+ * Every call takes plain pointers and sizes.  Unless stated otherwise:
+ *  - Buffers are DEVICE pointers owned by the caller; the library allocates
+ *    no device memory in any call (a decode step "runs with zero heap
+ *    allocations", "Inside the engine", section 1, "CausalLM: the forward
+ *    path").  Scratch space is a caller-supplied workspace whose size a
+ *    *_workspace_bytes call reports; a workspace must be zero-filled before
+ *    its first use and is left ready for the next call by every call.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and return before the GPU work finishes.
+ *  - Every length argument is an element count.  Each buffer's real length
+ *    is passed next to it and checked against the length the operation
+ *    needs, as the "LLM inference kernels" page's contract checks do
+ *    ("Status vocabulary and the shape checks (contract)", "Guarantees").
+ *    On any refusal the call returns before launching anything and leaves
+ *    every output untouched.
+ *  - Only what the host can see is checked on the host.  Values that live in
+ *    device memory (token ids, positions, sequence lengths) are checked by the
+ *    kernels: an out-of-range value is clamped or skipped and a bit is set in
+ *    the workspace's error word (see ds_workspace_error).
+ *  - Identical inputs give bit-identical outputs run to run: no reduction
+ *    depends on the order in which thread blocks finish.
+ *  - fp32 activations; weights fp32 or bf16; KV cache fp32 or bf16; fp32
+ *    accumulation.
+ */
+#ifndef DECODE_STEP_H
+#define DECODE_STEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define DS_API
+#else
+#define DS_API __attribute__((visibility("default")))
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *ds_stream_t;
+
+/* ---------------------------------------------------------------------
+ * Status vocabulary.  560-571 keep the numbers and meanings of the
+ * "LLM inference kernels" page ("Status vocabulary and the shape checks
+ * (contract)"); 572-577 are this library's additions in the unused part of
+ * the same 560-579 range.
+ * ------------------------------------------------------------------- */
+enum {
+    DS_OK = 560,                      /* ran; every output element is defined */
+    DS_EMPTY_DIMENSION = 561,         /* a required dimension was < 1 */
+    DS_A_LENGTH_MISMATCH = 562,       /* first operand's length != n */
+    DS_B_LENGTH_MISMATCH = 563,       /* second operand's length != n */
+    DS_DIMENSION_TOO_LARGE = 564,     /* a dimension exceeds DS_MAX_DIM */
+    DS_CODE_OUT_OF_RANGE = 565,       /* ds_status_name's answer for an unknown code */
+    DS_CACHE_LENGTH_MISMATCH = 566,   /* cache length / position out of range */
+    DS_NEW_LENGTH_MISMATCH = 567,     /* appended values' length != n_new */
+    DS_LOGITS_LENGTH_MISMATCH = 568,  /* logits length != n_rows * n */
+    DS_GEMV_A_LENGTH_MISMATCH = 569,  /* matrix length != rows * cols */
+    DS_GEMV_X_LENGTH_MISMATCH = 570,  /* vector length != the reduced dimension */
+    DS_CACHE_CAPACITY_EXCEEDED = 571, /* an append would overrun the reserved cache */
+    DS_BAD_DTYPE = 572,               /* dtype or layout code not supported here */
+    DS_CUDA_ERROR = 573,              /* a CUDA runtime call failed */
+    DS_WORKSPACE_TOO_SMALL = 574,     /* workspace NULL or smaller than required */
+    DS_BAD_SAMPLING_PARAM = 575,      /* temperature/top_k/top_p outside their domain */
+    DS_TOKEN_OUT_OF_RANGE = 576,      /* a host-visible token id outside [0, vocab) */
+    DS_BAD_ARGUMENT = 577             /* NULL pointer, misaligned pointer or bad count */
+};
+
+/* Largest accepted dimension (per dimension), 1 << 24, as on the
+ * "LLM inference kernels" page ("Status vocabulary and the shape checks"). */
+#define DS_MAX_DIM (1LL << 24)
+
+/* Storage dtypes. */
+enum { DS_F32 = 0, DS_BF16 = 1 };
+
+/* RoPE layouts: pairs (p, p + head_dim/2) — the GPT-NeoX split-half
+ * convention ("LLM inference kernels", "Two gaps, not three") — or pairs
+ * (2p, 2p + 1) ("The forward pass end to end", "The code"). */
+enum { DS_ROPE_HALF_SPLIT = 0, DS_ROPE_INTERLEAVED = 1 };
+
+/* Bits of a workspace's error word (set by kernels, never by the host). */
+enum {
+    DS_ERR_TOKEN_RANGE = 1,   /* a device-side token id was outside [0, vocab); clamped */
+    DS_ERR_POSITION = 2,      /* a device-side position or length exceeded the cache */
+    DS_ERR_WAIT_TIMEOUT = 4,  /* a bounded wait inside a kernel gave up */
+    DS_ERR_SAMPLING = 8       /* a sampler row had no finite logits */
+};
+
+/* Name of a status code ("ds_ok", "ds_a_length_mismatch", ...);
+ * "ds_code_out_of_range" for anything else.  Static storage. */
+DS_API const char *ds_status_name(int code);
+
+/* The residual-add shape check of the "LLM inference kernels" contract:
+ * 561 if n < 1, 564 if n > DS_MAX_DIM, 562 if a_len != n, 563 if b_len != n,
+ * else 560.  Host only. */
+DS_API int ds_residual_dims_check(int64_t n, int64_t a_len, int64_t b_len);
+
+/* Copy a workspace's error word (int32 at byte 0 of every workspace) to
+ * *host_word and clear it.  Synchronises `stream`. */
+DS_API int ds_workspace_error(void *workspace, int32_t *host_word, ds_stream_t stream);
+
+/* Number of streaming multiprocessors the library sizes its grids for on the
+ * current device (0 when no device is usable). */
+DS_API int ds_device_sm_count(void);
+
+/* ---------------------------------------------------------------------
+ * Projections
+ * ------------------------------------------------------------------- */
+
+/* Workspace bytes ds_gemv_transposed needs for a rows x cols matrix. */
+DS_API size_t ds_gemv_workspace_bytes(int64_t rows, int64_t cols, int a_dtype);
+
+/* y = A^T x: y[j] = sum_i A[i * cols + j] * x[i] for j < cols.
+ * The transposed mat-vec of "LLM inference kernels" ("A parallel path for
+ * one frozen kernel's known-slow shape"): A is row-major with `rows` input
+ * rows and `cols` output columns, the layout of every decode-step projection.
+ *   A: rows*cols elements of a_dtype (a_len must equal rows*cols, else 569)
+ *   x: rows fp32 (x_len must equal rows, else 570); y: cols fp32 (y_len must
+ *   equal cols, else 562); 561 / 564 for an empty / oversized dimension.
+ *   workspace: ds_gemv_workspace_bytes(rows, cols, a_dtype) bytes, zeroed
+ *   before first use.
+ * Weight rows stream through shared memory with bulk asynchronous copies when
+ * A is 16-byte aligned and cols * element size is a multiple of 16 bytes;
+ * other shapes run a plain-load kernel with the same result definition. */
+DS_API int ds_gemv_transposed(const void *A, int64_t a_len, int a_dtype, const float *x,
+                              int64_t x_len, int64_t rows, int64_t cols, float *y,
+                              int64_t y_len, void *workspace, size_t workspace_bytes,
+                              ds_stream_t stream);
+
+/* y = W x: y[r] = sum_c W[r * cols + c] * x[c] for r < rows — the
+ * untransposed form the "LLM inference kernels" page uses for lm_head.
+ *   W: rows*cols of w_dtype (569), x: cols fp32 (570), y: rows fp32 (562). */
+DS_API int ds_gemv(const void *W, int64_t w_len, int w_dtype, const float *x, int64_t x_len,
+                   int64_t rows, int64_t cols, float *y, int64_t y_len, ds_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * Decode glue
+ * ------------------------------------------------------------------- */
+
+/* out[i] = a[i] + b[i] in fp32 for i < n ("LLM inference kernels",
+ * "Residual add").  a_len/b_len must equal n (562/563); out has n elements and
+ * may alias a or b. */
+DS_API int ds_residual_add(const float *a, int64_t a_len, const float *b, int64_t b_len,
+                           float *out, int64_t n, ds_stream_t stream);
+
+/* residual += x (fp32, in place), then h = residual * (mean(residual^2) + eps)^(-1/2) * w,
+ * the square sum accumulated in fp32 ("decode-ops", "Usage" and
+ * "API — Method"; "The forward pass end to end", "The code", rmsnorm).
+ * x may be NULL (plain RMSNorm; x_len ignored).  residual_len (562), x_len
+ * (563), w_len and h_len (562) must equal n; w is fp32 or bf16. */
+DS_API int ds_add_rmsnorm(float *residual, int64_t residual_len, const float *x, int64_t x_len,
+                          const void *w, int64_t w_len, int w_dtype, float eps, float *h,
+                          int64_t h_len, int64_t n, ds_stream_t stream);
+
+/* Rotate q (n_qh heads) and k (n_kh heads, may be NULL with n_kh = 0) of
+ * head_dim values each, in place, to position `pos`: pair p turns by
+ * pos * base^(-2p/head_dim), angles formed in fp64 for this call ("decode-ops",
+ * "API — Method"), the rotation applied in fp32.  layout: DS_ROPE_*.
+ * q_len must be n_qh*head_dim (562), k_len n_kh*head_dim (563); head_dim
+ * even and <= 1024 (577); pos >= 0 (566). */
+DS_API int ds_rope(float *q, int64_t q_len, float *k, int64_t k_len, int64_t pos, int n_qh,
+                   int n_kh, int head_dim, double base, int layout, ds_stream_t stream);
+
+/* Reserved-capacity KV append: write the n_new fp32 values into
+ * cache[cache_len, cache_len + n_new) in place, converted to cache_dtype
+ * (bf16: round to nearest even) ("LLM inference kernels", "The hot loop
+ * doesn't call kv_cache_append_flat").  `capacity` is the cache's reserved
+ * element count.  561 for n_new < 1, 567 if new_len != n_new, 566 if
+ * cache_len < 0, 571 if cache_len + n_new > capacity. */
+DS_API int ds_kv_cache_append(void *cache, int cache_dtype, int64_t capacity, int64_t cache_len,
+                              const float *new_vals, int64_t new_len, int64_t n_new,
+                              ds_stream_t stream);
+
+/* out[i] = silu(gate[i]) * up[i], silu(z) = z / (1 + e^-z), fp32
+ * ("decode-ops", "Usage": silu_mul).  gate_len (562), up_len (563) equal n. */
+DS_API int ds_silu_mul(const float *gate, int64_t gate_len, const float *up, int64_t up_len,
+                       float *out, int64_t n, ds_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * Attention
+ * ------------------------------------------------------------------- */
+
+/* Workspace bytes for ds_gqa_decode_attn. */
+DS_API size_t ds_attention_workspace_bytes(int n_seqs, int n_qh, int n_kvh, int head_dim,
+                                           int64_t max_ctx);
+
+/* Grouped-query attention of one new query token per sequence over its
+ * cached positions ("The forward pass end to end", "The code":
+ * forward_token's attention; split across the context and reduced, "Inside
+ * the engine", section 1).  For sequence s and query head h, the KV head is
+ * g = h / (n_qh / n_kvh); scores q_h . k_t * scale over t < seq_lens[s],
+ * softmax, and out[s][h][:] = sum_t w_t v_t.
+ *   q: [n_seqs][n_qh][head_dim] fp32.  out: same shape fp32.
+ *   k_cache / v_cache: rows of n_kvh*head_dim elements of kv_dtype,
+ *   `cache_rows` rows each; position t of sequence s is row
+ *   blk * block_tokens + t % block_tokens with blk = block_table[s *
+ *   max_blocks_per_seq + t / block_tokens], or, with block_table NULL,
+ *   blk = s * max_blocks_per_seq + t / block_tokens (a contiguous slot per
+ *   sequence, "Inside the engine", section 3).
+ *   seq_lens: device int32 [n_seqs]; a length outside
+ *   [1, max_blocks_per_seq*block_tokens] is clamped and flags DS_ERR_POSITION.
+ *   n_qh must be a multiple of n_kvh; head_dim a multiple of 4 up to 128, or of 8 up to 256.
+ *   workspace: ds_attention_workspace_bytes(...) with max_ctx >= every length. */
+DS_API int ds_gqa_decode_attn(const float *q, const void *k_cache, const void *v_cache,
+                              int kv_dtype, int64_t cache_rows, const int32_t *block_table,
+                              int max_blocks_per_seq, int block_tokens, const int32_t *seq_lens,
+                              int n_seqs, int n_qh, int n_kvh, int head_dim, float scale,
+                              float *out, void *workspace, size_t workspace_bytes,
+                              ds_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * Picking the next token
+ * ------------------------------------------------------------------- */
+
+DS_API size_t ds_argmax_workspace_bytes(int n_rows, int64_t n);
+
+/* ids[r] = first index of the maximum of row r of logits [n_rows][n]
+ * ("LLM inference kernels", "KV-cache growth and greedy argmax": ties go to
+ * the first id; "decode-ops", "Correctness": exact against torch.argmax, NaN
+ * ranking above every number).  max_logit (optional) gets the row maxima.
+ * logits_len must be n_rows*n (568). */
+DS_API int ds_greedy_argmax(const float *logits, int64_t logits_len, int n_rows, int64_t n,
+                            int32_t *ids, float *max_logit, void *workspace,
+                            size_t workspace_bytes, ds_stream_t stream);
+
+/* Largest top_k the sampler accepts (top_k <= 0 or >= n disables top-k). */
+#define DS_SAMPLE_MAX_TOP_K 1024
+
+DS_API size_t ds_sample_workspace_bytes(int n_rows, int64_t n);
+
+/* Per row r of logits [n_rows][n], with the explicit uniform draw u[r] in
+ * [0,1): temperature -> top-k -> softmax over the survivors -> top-p ->
+ * renormalise -> inverse CDF at u ("decode-ops", "API — Method", the
+ * HuggingFace warper order).  In fp32 and in this order: l' = l / T;
+ * survivors = the top_k largest l', ties to the lower index, in descending
+ * order; e_i = exp(l'_i - l'_max); S = sum e_i in survivor order; p_i = e_i/S;
+ * keep the prefix whose exclusive running sum of p is < top_p (at least one;
+ * top_p >= 1 keeps all); token = first kept survivor whose inclusive running
+ * sum exceeds u * (sum of kept p), else the last kept.
+ *   temperature <= 0: greedy (first index of the maximum).
+ *   top_k: 1..DS_SAMPLE_MAX_TOP_K, or <= 0 / >= n for no top-k cut.
+ *   top_p in (0, 1].  575 for a parameter outside its domain.
+ *   u: device fp32 [n_rows]; ids: device int32 [n_rows]. */
+DS_API int ds_sample(const float *logits, int64_t logits_len, int n_rows, int64_t n,
+                     float temperature, int top_k, float top_p, const float *u, int32_t *ids,
+                     void *workspace, size_t workspace_bytes, ds_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * The decode step
+ * ------------------------------------------------------------------- */
+
+/* Model shape ("The forward pass end to end", "The code": Config, with the
+ * head dimension explicit). */
+typedef struct {
+    int32_t vocab, d, n_layer, n_qh, n_kvh, head_dim, ff;
+    int32_t rope_layout; /* DS_ROPE_* */
+    double rope_base;
+    float eps;           /* RMSNorm epsilon */
+    int32_t tied;        /* 1: the output head is the embedding table */
+    int32_t w_dtype;     /* DS_F32 or DS_BF16, for emb, out and projections */
+    int32_t kv_dtype;    /* DS_F32 or DS_BF16 */
+    int32_t max_seqs;    /* largest n_seqs a step will be given */
+    int32_t max_ctx;     /* largest position + 1 a step will see */
+} ds_model_config;
+
+/* Device pointers to the weights, in this storage layout:
+ *   emb [vocab][d]; out [vocab][d] (ignored when tied); final_norm [d] fp32;
+ *   per layer (host arrays of n_layer device pointers):
+ *   n1, n2 [d] fp32;  wqkv [d][(n_qh + 2 n_kvh) head_dim] with the q columns,
+ *   then k, then v;  wo [n_qh head_dim][d];  wgu [d][2 ff] with the gate
+ *   columns, then up;  wd [ff][d].  Projections are [in][out] row-major and
+ *   applied as y = W^T x.  The library keeps the pointers, not copies: the
+ *   weights must outlive the model. */
+typedef struct {
+    const void *emb;
+    const void *out;
+    const float *final_norm;
+    const float *const *n1;
+    const void *const *wqkv;
+    const void *const *wo;
+    const float *const *n2;
+    const void *const *wgu;
+    const void *const *wd;
+} ds_model_weights;
+
+/* The KV cache: per layer one K and one V buffer of rows of n_kvh*head_dim
+ * elements (kv_dtype), addressed as in ds_gqa_decode_attn ("Inside the
+ * engine", section 3: KvPool holds one K and one V buffer per layer). */
+typedef struct {
+    void *const *k;             /* host array of n_layer device pointers */
+    void *const *v;             /* host array of n_layer device pointers */
+    int64_t rows;               /* rows each per-layer buffer holds */
+    int32_t block_tokens;       /* positions per block */
+    int32_t max_blocks;         /* blocks per sequence */
+    const int32_t *block_table; /* device int32 [max_seqs][max_blocks], or NULL */
+} ds_kv_cache;
+
+/* Sampling parameters for a whole step (see ds_sample); NULL means greedy. */
+typedef struct {
+    float temperature;
+    int32_t top_k;
+    float top_p;
+} ds_sampling;
+
+typedef struct ds_model ds_model;
+
+/* Bytes of the model workspace (activations, split reductions, RoPE table,
+ * error word) for a configuration. */
+DS_API size_t ds_model_workspace_bytes(const ds_model_config *cfg);
+
+/* Validate the configuration and weights, carve the caller's workspace
+ * (zeroed here) and build the RoPE table (angles in fp64 on the device).
+ * Synchronises the device.  The model object lives in host memory. */
+DS_API int ds_model_create(const ds_model_config *cfg, const ds_model_weights *weights,
+                           void *workspace, size_t workspace_bytes, ds_model **out);
+DS_API void ds_model_destroy(ds_model *model);
+
+/* Workspace pointer of a model (its error word is at byte 0). */
+DS_API void *ds_model_workspace(ds_model *model);
+
+/* Flags of ds_decode_step. */
+#define DS_STEP_ADVANCE 1u /* after picking: tokens[s] = next_ids[s], pos[s] += 1 (on device) */
+
+/* One decode step for n_seqs sequences: for each sequence s, token
+ * tokens[s] at position pos[s] ("The forward pass end to end", "What a
+ * forward step does"; "LLM inference kernels", "How this composes into a
+ * decode step"): embed; per layer RMSNorm -> fused q|k|v projection -> RoPE on
+ * q and k with the K/V write at pos ("Inside the engine", section 1: qkPrep)
+ * -> attention over positions 0..pos -> output projection + residual ->
+ * RMSNorm -> fused gate|up projection with SiLU-gate -> down projection +
+ * residual; final RMSNorm -> output head -> greedy argmax (sampling NULL) or
+ * the sampler with draws u[s].
+ *   tokens, pos: device int32 [n_seqs]; next_ids: device int32 [n_seqs];
+ *   u: device fp32 [n_seqs] (sampling only); logits_out: optional device fp32
+ *   [n_seqs][vocab].  n_seqs in [1, max_seqs].
+ * Bad device-side tokens/positions are clamped/skipped and flag the model's
+ * error word. */
+DS_API int ds_decode_step(ds_model *model, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos,
+                          int n_seqs, const ds_sampling *sampling, const float *u,
+                          int32_t *next_ids, float *logits_out, unsigned flags,
+                          ds_stream_t stream);
+
+/* A decode step captured once as a CUDA graph and replayed ("Inside the
+ * engine", section 4: the launch sequence of a step replayed as a captured
+ * graph).  Arguments as ds_decode_step; the pointed-to device buffers are
+ * read at every launch, so with DS_STEP_ADVANCE each launch decodes the next
+ * token.  Capture uses `stream`, which must not be capturing already. */
+typedef struct ds_step_graph ds_step_graph;
+DS_API int ds_step_graph_create(ds_model *model, const ds_kv_cache *kv, int32_t *tokens,
+                                int32_t *pos, int n_seqs, const ds_sampling *sampling,
+                                const float *u, int32_t *next_ids, float *logits_out,
+                                unsigned flags, ds_stream_t stream, ds_step_graph **out);
+DS_API int ds_step_graph_launch(ds_step_graph *graph, ds_stream_t stream);
+DS_API void ds_step_graph_destroy(ds_step_graph *graph);
+
+/* Per-kernel timing of one decode step: the step's kernels are launched one
+ * at a time on `stream` with CUDA events around each, `reps` times, and the
+ * mean duration of each launch slot is written to ms_out[i] with its kernel
+ * kind in kinds_out[i] (DS_KIND_*).  *n_out gets the number of slots (at most
+ * cap).  Runs the step `reps` times: with DS_STEP_ADVANCE the state advances. */
+enum {
+    DS_KIND_EMBED = 0,
+    DS_KIND_QKV = 1,
+    DS_KIND_ATTENTION = 2,
+    DS_KIND_O_PROJ = 3,
+    DS_KIND_GATE_UP = 4,
+    DS_KIND_DOWN = 5,
+    DS_KIND_HEAD = 6,
+    DS_KIND_SAMPLE = 7,
+    DS_KIND_COUNT = 8
+};
+DS_API int ds_decode_step_profile(ds_model *model, const ds_kv_cache *kv, int32_t *tokens,
+                                  int32_t *pos, int n_seqs, const ds_sampling *sampling,
+                                  const float *u, int32_t *next_ids, float *logits_out,
+                                  unsigned flags, int reps, float *ms_out, int32_t *kinds_out,
+                                  int cap, int *n_out, ds_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_STEP_H */
