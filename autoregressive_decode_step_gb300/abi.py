@@ -111,6 +111,8 @@ _sig("ds_step_graph_create", ctypes.c_int, P, ctypes.POINTER(KVCache), P, P, cty
      ctypes.POINTER(Sampling), P, P, P, ctypes.c_uint, P, ctypes.POINTER(P))
 _sig("ds_step_graph_launch", ctypes.c_int, P, P)
 _sig("ds_step_graph_destroy", None, P)
+_sig("ds_decode_kernel_time", ctypes.c_int, P, ctypes.POINTER(KVCache), P, P, ctypes.c_int, ctypes.c_int,
+     ctypes.POINTER(ctypes.c_float), P)
 _sig("ds_decode_step_profile", ctypes.c_int, P, ctypes.POINTER(KVCache), P, P, ctypes.c_int,
      ctypes.POINTER(Sampling), P, P, P, ctypes.c_uint, ctypes.c_int, P, P, ctypes.c_int,
      ctypes.POINTER(ctypes.c_int), P)

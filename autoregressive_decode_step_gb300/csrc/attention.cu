@@ -18,7 +18,9 @@
 
 namespace ds {
 
-constexpr int kAttnWarps = 4;
+constexpr int kAttnWarps = 8;
+constexpr int kAttnMaxSplits = 64;
+constexpr int kAttnMinPerSplit = 64;  // positions: one run of eight per warp
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kAttnRun = 8;  // positions a warp fetches together
 
@@ -80,7 +82,10 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const __grid_co
         if (threadIdx.x == 0 && split == 0 && g == 0) flag_error(p.err, DS_ERR_POSITION);
         n_ctx = min(max(n_ctx, 1), cap);
     }
-    const int per = (n_ctx + p.n_splits - 1) / p.n_splits;
+    // positions per split, never fewer than kAttnMinPerSplit; splits past the
+    // context (split >= n_eff) have no work and write no partial
+    const int per = max(kAttnMinPerSplit, (n_ctx + p.n_splits - 1) / p.n_splits);
+    const int n_eff = (n_ctx + per - 1) / per;
     const int t0 = min(n_ctx, split * per), t1 = min(n_ctx, t0 + per);
 
     const bool active = lane * DPL < hd;
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const __grid_co
     const int slot = (seq * p.n_kvh + g) * p.n_splits + split;
     const int rec = GQ * (hd + 2);  // per split: m[GQ], l[GQ], acc[GQ][hd]
     float *part = p.partials + (size_t)slot * rec;
-    for (int idx = threadIdx.x; idx < GQ * hd; idx += kAttnThreads) {
+    for (int idx = threadIdx.x; split < n_eff && idx < GQ * hd; idx += kAttnThreads) {
         const int j = idx / hd;
         float M = -INFINITY;
         for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][j]);
@@ -193,28 +198,62 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const __grid_co
     if (!s_last) return;
     __threadfence();
 
+    // merge the n_eff splits in split order.  All (m, l) are staged in shared
+    // memory by parallel loads, the weights exp(m_s - M) computed in
+    // parallel, then every output is one fixed-order sum over the splits
+    // (two outputs per thread, their loads interleaved).
     const float *base = p.partials + (size_t)(seq * p.n_kvh + g) * p.n_splits * rec;
-    for (int idx = threadIdx.x; idx < GQ * hd; idx += kAttnThreads) {
-        const int j = idx / hd;
+    float *sm = s_acc;                          // [n_eff][GQ] m, then weights
+    float *sl = s_acc + kAttnMaxSplits * GQ;    // [n_eff][GQ] l
+    float *sM = sl + kAttnMaxSplits * GQ;       // [GQ] max, then [GQ] total
+    for (int i = threadIdx.x; i < n_eff * GQ; i += kAttnThreads) {
+        const int sp = i / GQ, j = i % GQ;
+        sm[i] = __ldcg(base + (size_t)sp * rec + j);
+        sl[i] = __ldcg(base + (size_t)sp * rec + GQ + j);
+    }
+    __syncthreads();
+    if (threadIdx.x < GQ) {
         float M = -INFINITY;
-        for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, __ldcg(base + (size_t)s * rec + j));
-        float L = 0.0f, A = 0.0f;
-        for (int s = 0; s < p.n_splits; ++s) {
-            const float ms = __ldcg(base + (size_t)s * rec + j);
-            if (ms == -INFINITY) continue;
-            const float c = expf(ms - M);
-            L = fmaf(__ldcg(base + (size_t)s * rec + GQ + j), c, L);
-            A = fmaf(__ldcg(base + (size_t)s * rec + 2 * GQ + idx), c, A);
+        for (int sp = 0; sp < n_eff; ++sp) M = fmaxf(M, sm[sp * GQ + threadIdx.x]);
+        sM[threadIdx.x] = M;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_eff * GQ; i += kAttnThreads) {
+        const float ms = sm[i];
+        sm[i] = ms == -INFINITY ? 0.0f : expf(ms - sM[i % GQ]);
+    }
+    __syncthreads();
+    if (threadIdx.x < GQ) {
+        float L = 0.0f;
+        for (int sp = 0; sp < n_eff; ++sp) L = fmaf(sl[sp * GQ + threadIdx.x], sm[sp * GQ + threadIdx.x], L);
+        sM[GQ + threadIdx.x] = L;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < GQ * hd; idx += 2 * kAttnThreads) {
+        const int idx2 = idx + kAttnThreads;
+        const bool two = idx2 < GQ * hd;
+        const int j = idx / hd, j2 = two ? idx2 / hd : j;
+        float A = 0.0f, A2 = 0.0f;
+#pragma unroll 8
+        for (int sp = 0; sp < n_eff; ++sp) {
+            const float *rp = base + (size_t)sp * rec + 2 * GQ;
+            const float a = __ldcg(rp + idx);
+            const float a2 = two ? __ldcg(rp + idx2) : 0.0f;
+            A = fmaf(a, sm[sp * GQ + j], A);
+            A2 = fmaf(a2, sm[sp * GQ + j2], A2);
         }
-        p.out[((long long)seq * p.n_qh + g * GQ + j) * hd + idx % hd] = A / L;
+        p.out[((long long)seq * p.n_qh + g * GQ + j) * hd + idx % hd] = A / sM[GQ + j];
+        if (two) p.out[((long long)seq * p.n_qh + g * GQ + j2) * hd + idx2 % hd] = A2 / sM[GQ + j2];
     }
 }
 
 int attention_splits(int n_seqs, int n_kvh, long long max_ctx) {
+    // about two CTAs per SM in all, at least kAttnMinPerSplit positions per
+    // split at the largest context, at most kAttnMaxSplits splits
     const long long target = 2LL * sm_count();
     long long s = (target + (long long)n_seqs * n_kvh - 1) / ((long long)n_seqs * n_kvh);
-    const long long by_ctx = (max_ctx + 15) / 16;
-    s = std::min(s, by_ctx);
+    const long long by_ctx = (max_ctx + kAttnMinPerSplit - 1) / kAttnMinPerSplit;
+    s = std::min(std::min(s, by_ctx), (long long)kAttnMaxSplits);
     return (int)std::max(1LL, s);
 }
 
@@ -227,7 +266,7 @@ template <typename KT, int DPL>
 static cudaError_t launch_attn_g(const AttnArgs &a, int n_seqs, cudaStream_t stream, bool pdl) {
     const int gq = a.n_qh / a.n_kvh;
     const dim3 grid(a.n_splits, a.n_kvh, n_seqs);
-    const size_t smem = (size_t)kAttnWarps * gq * a.hd * sizeof(float);
+    const size_t smem = std::max((size_t)kAttnWarps * gq * a.hd, (size_t)(2 * kAttnMaxSplits + 2) * gq) * sizeof(float);
     switch (gq) {
         case 1: return launch_ex(attention_kernel<KT, DPL, 1>, grid, dim3(kAttnThreads), smem, stream, pdl, a);
         case 2: return launch_ex(attention_kernel<KT, DPL, 2>, grid, dim3(kAttnThreads), smem, stream, pdl, a);

@@ -24,6 +24,7 @@
 //
 // Both kernels fetch weights before waiting on the previous kernel
 // (programmatic dependent launch): weights never depend on it.
+#include <algorithm>
 #include <cstdio>
 
 #include "common.cuh"
@@ -34,8 +35,13 @@ namespace ds {
 constexpr int kGtThreads = (kGtConsumerWarps + 1) * 32;
 constexpr int kGtConsumers = kGtConsumerWarps * 32;
 constexpr int kGtStageBytes = kGtBandBytes * kGtRows;
+constexpr int kGtBoxesPerStage = kGtRows / kGtBoxRows;
 constexpr int kGtRedFloats = kGtConsumerWarps * 256;
-constexpr size_t kGtSmem = (size_t)kGtStages * kGtStageBytes + kGtRedFloats * 4 + 256 * 4 + 256;
+// ring | red | vals | barriers and flags | x slice (xs_cap floats)
+constexpr size_t kGtSmemBase = (size_t)kGtStages * kGtStageBytes + kGtRedFloats * 4 + 256 * 4 + 256;
+constexpr int kGtMaxXs = 16384;  // floats of x one CTA may stage (64 KB)
+constexpr size_t kGtSmemMax = std::min<size_t>(kGtSmemBase + (size_t)kGtMaxXs * 4, 227 * 1024);
+static_assert(kGtRows % kGtBoxRows == 0, "stage rows must be whole boxes");
 
 // CTA whose range holds unit u when W units are cut into G ranges
 // [W*c/G, W*(c+1)/G).
@@ -45,6 +51,16 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long W, int G) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
+// One 2-D tensor-map box (columns c0.., rows r0..) into shared memory.
+__device__ __forceinline__ void tma_box_g2s(void *dst, const CUtensorMap *map, int c0, int r0, uint64_t *bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 template <typename T, int PRO, int EPI>
 __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_constant__ GemvTArgs p) {
     constexpr int ES = sizeof(T);
@@ -52,8 +68,10 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_cons
     constexpr int BAND_COLS = kGtBandBytes / ES; // partial columns per band
     constexpr bool PAIRED = (EPI == EPI_SILU);
     constexpr int SUB_BAND_COLS = PAIRED ? BAND_COLS / 2 : BAND_COLS;
+    constexpr int SUB_ROW_BYTES = SUB_BAND_COLS * ES;          // bytes of one box row
+    constexpr uint32_t BOX_BYTES = kGtBoxRows * SUB_ROW_BYTES;  // bytes of one box
 
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *ring = smem;
     float *red = reinterpret_cast<float *>(smem + (size_t)kGtStages * kGtStageBytes);
     float *vals = red + kGtRedFloats;
@@ -62,10 +80,13 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_cons
     volatile int *s_flag = reinterpret_cast<volatile int *>(empty + kGtStages);
     volatile int *s_abort = s_flag + 1;
     float *s_scale = reinterpret_cast<float *>(const_cast<int *>(s_flag) + 2);
+    float *xs = reinterpret_cast<float *>(smem + kGtSmemBase);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
-    const long long W = (long long)p.n_bands * p.K;
+    // work units are boxes of kGtBoxRows rows of one band
+    const int UB = (p.K + kGtBoxRows - 1) / kGtBoxRows;  // boxes per band
+    const long long W = (long long)p.n_bands * UB;
     const long long u0 = W * blockIdx.x / G, u1 = W * (blockIdx.x + 1) / G;
 
     if (threadIdx.x == 0) {
@@ -81,48 +102,39 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_cons
     allow_dependent_launch();
 
     if (warp == kGtConsumerWarps) {
-        // ---------------- producer: stream this CTA's rows into the ring
-        const uint64_t pol = policy_evict_first();
-        uint32_t fill = 0;
-        bool ok = true;
-        for (long long u = u0; u < u1 && ok;) {
-            const int band = (int)(u / p.K);
-            const int k0 = (int)(u - (long long)band * p.K);
-            const int k1 = (int)min((long long)p.K, k0 + (u1 - u));
-            u += k1 - k0;
-            const int vc = min(SUB_BAND_COLS, p.sub_cols - band * SUB_BAND_COLS);
-            const uint32_t sub_bytes = (uint32_t)vc * ES;
-            const char *src0 = p.a0 + (long long)band * SUB_BAND_COLS * ES;
-            const char *src1 = PAIRED ? p.a1 + (long long)band * SUB_BAND_COLS * ES : nullptr;
-            for (int kc = k0; kc < k1; kc += kGtRows) {
-                const int nr = min(kGtRows, k1 - kc);
-                const int s = fill % kGtStages;
-                const uint32_t use = fill / kGtStages;
-                if (use > 0) {
-                    int w_ok = 1;
-                    if (lane == 0) w_ok = mbar_wait(&empty[s], (use - 1) & 1, p.err);
-                    ok = __shfl_sync(0xffffffffu, w_ok, 0) != 0;
-                    if (!ok) {
+        // ---------------- producer: stream this CTA's boxes into the ring
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            uint32_t fill = 0;
+            bool ok = true;
+            for (long long u = u0; u < u1 && ok;) {
+                const int band = (int)(u / UB);
+                const int j0 = (int)(u - (long long)band * UB);
+                const int j1 = (int)min((long long)UB, j0 + (u1 - u));
+                for (int j = j0; j < j1; j += kGtBoxesPerStage) {
+                    const int nb = min(kGtBoxesPerStage, j1 - j);
+                    const int s = fill % kGtStages;
+                    const uint32_t use = fill / kGtStages;
+                    if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, p.err)) {
                         *s_abort = 1;
+                        ok = false;
                         break;
                     }
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)nb * BOX_BYTES * (PAIRED ? 2 : 1));
+                    unsigned char *dst = ring + (size_t)s * kGtStageBytes;
+                    for (int b = 0; b < nb; ++b) {
+                        const int r = (j + b) * kGtBoxRows;
+                        tma_box_g2s(dst + b * BOX_BYTES, &p.tm0, band * SUB_BAND_COLS, r, &full[s], pol);
+                        if (PAIRED)
+                            tma_box_g2s(dst + kGtStageBytes / 2 + b * BOX_BYTES, &p.tm1, band * SUB_BAND_COLS, r,
+                                        &full[s], pol);
+                    }
+                    ++fill;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nr * sub_bytes * (PAIRED ? 2 : 1));
-                __syncwarp();
-                unsigned char *dst = ring + (size_t)s * kGtStageBytes;
-                for (int r = lane; r < nr; r += 32) {
-                    const long long off = (long long)(kc + r) * p.row_stride;
-                    bulk_g2s(dst + r * kGtBandBytes, src0 + off, sub_bytes, &full[s], pol);
-                    if (PAIRED)
-                        bulk_g2s(dst + r * kGtBandBytes + kGtBandBytes / 2, src1 + off, sub_bytes,
-                                 &full[s], pol);
-                }
-                ++fill;
+                u += j1 - j0;
             }
-        }
-        // Every copy this CTA issued must land before its shared memory is
-        // released (bounded wait; already complete on the normal path).
-        if (lane == 0) {
+            // every copy this CTA issued must land before its shared memory
+            // is released (bounded wait; already complete on the normal path)
             const uint32_t first = fill > (uint32_t)kGtStages ? fill - kGtStages : 0;
             for (uint32_t f = first; f < fill; ++f) mbar_wait(&full[f % kGtStages], (f / kGtStages) & 1, p.err);
         }
@@ -153,19 +165,43 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_cons
         named_sync(1, kGtConsumers);
         scale = *s_scale;
     }
+    // this CTA's slice of x (normalised; zero past K) into shared memory
+    {
+        int off = 0;
+        for (long long u = u0; u < u1;) {
+            const int band = (int)(u / UB);
+            const int j0 = (int)(u - (long long)band * UB);
+            const int j1 = (int)min((long long)UB, j0 + (u1 - u));
+            u += j1 - j0;
+            const int k0 = j0 * kGtBoxRows, k1 = j1 * kGtBoxRows;
+            for (int k = k0 + t; k < k1; k += kGtConsumers) {
+                float v = 0.0f;
+                if (k < p.K) {
+                    v = p.x[k];
+                    if (PRO == PRO_RMSNORM) v = v * scale * p.norm_w[k];
+                }
+                if (off + k - k0 < p.xs_cap) xs[off + k - k0] = v;
+            }
+            off += k1 - k0;
+        }
+        named_sync(1, kGtConsumers);
+    }
 
     uint32_t fill = 0;
+    int seg_off = 0;
     for (long long u = u0; u < u1;) {
-        const int band = (int)(u / p.K);
-        const int k0 = (int)(u - (long long)band * p.K);
-        const int k1 = (int)min((long long)p.K, k0 + (u1 - u));
-        u += k1 - k0;
+        const int band = (int)(u / UB);
+        const int j0 = (int)(u - (long long)band * UB);
+        const int j1 = (int)min((long long)UB, j0 + (u1 - u));
+        u += j1 - j0;
+        const float *xseg = xs + seg_off - j0 * kGtBoxRows;  // xseg[k] for rows of this segment
+        seg_off += (j1 - j0) * kGtBoxRows;
 
         float acc[LE];
 #pragma unroll
         for (int e = 0; e < LE; ++e) acc[e] = 0.0f;
-        for (int kc = k0; kc < k1; kc += kGtRows) {
-            const int nr = min(kGtRows, k1 - kc);
+        for (int j = j0; j < j1; j += kGtBoxesPerStage) {
+            const int nr = min(kGtBoxesPerStage, j1 - j) * kGtBoxRows;
             const int s = fill % kGtStages;
             const uint32_t use = fill / kGtStages;
             if (!*s_abort) {
@@ -173,12 +209,15 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_cons
             }
             if (!*s_abort) {
                 const unsigned char *st = ring + (size_t)s * kGtStageBytes;
+                // lane's 16 bytes of row r: one dense [rows][SUB_ROW_BYTES] array
+                // per sub-tile, sub-tile 1 (lanes 16-31 when paired) in the upper half
+                const unsigned char *lane_base =
+                    PAIRED ? st + (lane >> 4) * (kGtStageBytes / 2) + (lane & 15) * 16 : st + lane * 16;
+                const int kr = j * kGtBoxRows;
 #pragma unroll 4
                 for (int r = warp; r < nr; r += kGtConsumerWarps) {
-                    const int k = kc + r;
-                    float xk = __ldg(p.x + k);
-                    if (PRO == PRO_RMSNORM) xk = xk * scale * __ldg(p.norm_w + k);
-                    const uint4 w = *reinterpret_cast<const uint4 *>(st + r * kGtBandBytes + lane * 16);
+                    const float xk = xseg[kr + r];
+                    const uint4 w = *reinterpret_cast<const uint4 *>(lane_base + r * SUB_ROW_BYTES);
                     float f[LE];
                     widen16(w, f);
 #pragma unroll
@@ -198,10 +237,10 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_cons
         if (t < BAND_COLS)
             for (int w = 0; w < kGtConsumerWarps; ++w) v += red[w * BAND_COLS + t];
 
-        const bool sole = (k0 == 0 && k1 == p.K);
+        const bool sole = (j0 == 0 && j1 == UB);
         if (!sole) {
-            const int first = cta_of_unit((long long)band * p.K, W, G);
-            const int last = cta_of_unit((long long)(band + 1) * p.K - 1, W, G);
+            const int first = cta_of_unit((long long)band * UB, W, G);
+            const int last = cta_of_unit((long long)(band + 1) * UB - 1, W, G);
             const int n_contrib = last - first + 1;
             if (t < BAND_COLS) p.partials[(size_t)(blockIdx.x + band) * BAND_COLS + t] = v;
             __threadfence();
@@ -212,8 +251,8 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_cons
             __threadfence();
             v = 0.0f;
             if (t < BAND_COLS)
-                for (int j = 0; j < n_contrib; ++j)
-                    v += __ldcg(&p.partials[(size_t)(first + j + band) * BAND_COLS + t]);
+                for (int c = 0; c < n_contrib; ++c)
+                    v += __ldcg(&p.partials[(size_t)(first + c + band) * BAND_COLS + t]);
             if (t == 0) p.counters[band] = 0;
         }
 
@@ -283,7 +322,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_cons
     }
 }
 
-// Plain-load fallback for shapes the bulk-copy path cannot stream (rows not a
+// Plain-load fallback for shapes the tensor-map path cannot stream (rows not a
 // multiple of 16 bytes or a misaligned base): one thread per output column,
 // rows summed in order.
 template <typename T>
@@ -297,9 +336,20 @@ __global__ void gemv_t_plain_kernel(const T *A, const float *x, int K, int N, fl
 }
 
 int gemv_t_grid(int K, int n_bands) {
-    const long long W = (long long)K * n_bands;
-    long long g = (W + 63) / 64;
-    return (int)std::max(1LL, std::min<long long>(g, sm_count()));
+    const long long UB = (K + kGtBoxRows - 1) / kGtBoxRows;
+    const long long W = UB * n_bands;
+    long long g = (W + 7) / 8;  // at least 8 boxes per CTA
+    g = std::min<long long>(g, sm_count());
+    // enough CTAs that each one's slice of x fits in shared memory
+    const long long per = kGtMaxXs / kGtBoxRows - 1;
+    g = std::max(g, (W + per - 1) / per);
+    return (int)std::max(1LL, g);
+}
+
+static int gemv_t_xs_cap(int K, int n_bands, int grid) {
+    const long long UB = (K + kGtBoxRows - 1) / kGtBoxRows;
+    const long long W = UB * n_bands;
+    return (int)(((W + grid - 1) / grid + 1) * kGtBoxRows);
 }
 
 size_t gemv_t_partial_floats(int grid, int n_bands, int es) {
@@ -308,8 +358,52 @@ size_t gemv_t_partial_floats(int grid, int n_bands, int es) {
 
 bool gemv_t_streamable(const void *a0, const void *a1, long long row_stride, int sub_cols, int es) {
     if (((uintptr_t)a0 & 15) || (a1 && ((uintptr_t)a1 & 15))) return false;
-    if (row_stride % 16) return false;
+    if (row_stride % 16 || row_stride >= (1LL << 40)) return false;
     if (((long long)sub_cols * es) % 16) return false;
+    return true;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+static bool encode_band_map(CUtensorMap *m, const void *base, int dtype, long long cols, long long rows,
+                            long long row_stride, int box_cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_stride};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kGtBoxRows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt = dtype == DS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool gemv_t_make_maps(GemvTArgs &a, int dtype) {
+    const int es = dtype == DS_BF16 ? 2 : 4;
+    const int band_cols = gemv_t_band_cols(es);
+    const int box_cols = a.a1 ? band_cols / 2 : band_cols;
+    if (!encode_band_map(&a.tm0, a.a0, dtype, a.sub_cols, a.K, a.row_stride, box_cols)) return false;
+    if (a.a1 && !encode_band_map(&a.tm1, a.a1, dtype, a.sub_cols, a.K, a.row_stride, box_cols)) return false;
     return true;
 }
 
@@ -320,7 +414,7 @@ static cudaError_t ensure_gt(bool force = false) {
     static bool done = false;
     if (done && !force) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(gemv_t_kernel<T, PRO, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kGtSmem);
+                                         (int)kGtSmemMax);
     if (e == cudaSuccess) done = true;
     return e;
 }
@@ -329,7 +423,11 @@ template <typename T, int PRO, int EPI>
 static cudaError_t launch_gt(const GemvTArgs &a, int grid, cudaStream_t stream, bool pdl) {
     cudaError_t e = ensure_gt<T, PRO, EPI>();
     if (e != cudaSuccess) return e;
-    return launch_ex(gemv_t_kernel<T, PRO, EPI>, dim3(grid), dim3(kGtThreads), kGtSmem, stream, pdl, a);
+    GemvTArgs b = a;
+    b.xs_cap = gemv_t_xs_cap(a.K, a.n_bands, grid);
+    if (b.xs_cap > kGtMaxXs) return cudaErrorInvalidValue;
+    const size_t smem = kGtSmemBase + align_up((size_t)b.xs_cap * 4, 16);
+    return launch_ex(gemv_t_kernel<T, PRO, EPI>, dim3(grid), dim3(kGtThreads), smem, stream, pdl, b);
 }
 
 template <typename T>
@@ -352,15 +450,28 @@ cudaError_t launch_gemv_t(const GemvTArgs &a, int dtype, int pro, int epi, int g
 // =====================================================================
 // gemv_n: whole rows per CTA, fused greedy argmax
 // =====================================================================
-constexpr int kGnStageBytes = 16384;
-constexpr int kGnStages = 5;
+#ifndef DS_GN_STAGE_BYTES
+#define DS_GN_STAGE_BYTES 65536
+#endif
+#ifndef DS_GN_STAGES
+#define DS_GN_STAGES 3
+#endif
+constexpr int kGnStageBytes = DS_GN_STAGE_BYTES;
+constexpr int kGnStages = DS_GN_STAGES;
 constexpr int kGnConsumerWarps = 8;
 constexpr int kGnThreads = (kGnConsumerWarps + 1) * 32;
 constexpr int kGnConsumers = kGnConsumerWarps * 32;
 constexpr int kGnMaxCols = 8192;
 constexpr int kGnMaxRowsPerStage = 256;
-constexpr size_t kGnSmem = (size_t)kGnStages * kGnStageBytes + kGnMaxCols * 4 + kGnMaxRowsPerStage * 8 * 4 +
-                           kGnConsumers * 8 + 256;
+// ring | barriers and flags | best value/index per consumer | x | row partials
+constexpr size_t kGnSmemBase = (size_t)kGnStages * kGnStageBytes + 256 + (size_t)kGnConsumers * 8;
+constexpr size_t kGnSmemMax = 227 * 1024;
+
+__host__ __device__ inline int gn_rows_per_stage(long long row_bytes) {
+    long long r = kGnStageBytes / row_bytes;
+    return (int)(r < 1 ? 1 : (r > kGnMaxRowsPerStage ? kGnMaxRowsPerStage : r));
+}
+__host__ __device__ inline int gn_parts(int rps) { return rps >= kGnConsumerWarps ? 1 : kGnConsumerWarps / rps; }
 
 template <typename T, int PRO>
 __global__ void __launch_bounds__(kGnThreads, 1) gemv_n_kernel(const __grid_constant__ GemvNArgs p) {
@@ -368,20 +479,21 @@ __global__ void __launch_bounds__(kGnThreads, 1) gemv_n_kernel(const __grid_cons
     constexpr int LE = 16 / ES;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *ring = smem;
-    float *xs = reinterpret_cast<float *>(smem + (size_t)kGnStages * kGnStageBytes);
-    float *rowpart = xs + kGnMaxCols;                               // [rps][parts]
-    float *bestv = rowpart + kGnMaxRowsPerStage * 8;                // [consumers]
-    int *besti = reinterpret_cast<int *>(bestv + kGnConsumers);     // [consumers]
-    uint64_t *full = reinterpret_cast<uint64_t *>(besti + kGnConsumers);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kGnStages * kGnStageBytes);
     uint64_t *empty = full + kGnStages;
     volatile int *s_flag = reinterpret_cast<volatile int *>(empty + kGnStages);
     volatile int *s_abort = s_flag + 1;
     float *s_scale = reinterpret_cast<float *>(const_cast<int *>(s_flag) + 2);
+    float *bestv = reinterpret_cast<float *>(smem + (size_t)kGnStages * kGnStageBytes + 256);
+    int *besti = reinterpret_cast<int *>(bestv + kGnConsumers);
+    float *xs = reinterpret_cast<float *>(besti + kGnConsumers);
+    float *rowpart = xs + p.cols;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
     const long long row_bytes = (long long)p.cols * ES;
-    const int rps = (int)max(1LL, min((long long)kGnMaxRowsPerStage, kGnStageBytes / row_bytes));
+    const int rps = gn_rows_per_stage(row_bytes);
+    const int parts = gn_parts(rps);
     const int r0 = (int)((long long)p.rows * blockIdx.x / G);
     const int r1 = (int)((long long)p.rows * (blockIdx.x + 1) / G);
     const int n_stages = (r1 - r0 + rps - 1) / rps;
@@ -450,11 +562,9 @@ __global__ void __launch_bounds__(kGnThreads, 1) gemv_n_kernel(const __grid_cons
     }
     named_sync(1, kGnConsumers);
 
+    // dot products: each warp owns one (row, part) of every stage; the part
+    // sums wait in shared memory until the CTA's rows are all done
     const int chunks = (int)(row_bytes / 16);
-    const int parts = rps >= kGnConsumerWarps ? 1 : kGnConsumerWarps / rps;
-    float best_v = -INFINITY;
-    int best_i = 0x7fffffff;
-
     for (int i = 0; i < n_stages; ++i) {
         const int s = i % kGnStages;
         const uint32_t use = i / kGnStages;
@@ -477,7 +587,7 @@ __global__ void __launch_bounds__(kGnThreads, 1) gemv_n_kernel(const __grid_cons
                         for (int e = 0; e < LE; ++e) acc = fmaf(f[e], xs[c * LE + e], acc);
                     }
                     acc = warp_sum(acc);
-                    if (lane == 0) rowpart[r] = acc;
+                    if (lane == 0) rowpart[rr - r0 + r] = acc;
                 }
             } else {
                 const int r = warp / parts, part = warp % parts;
@@ -485,6 +595,7 @@ __global__ void __launch_bounds__(kGnThreads, 1) gemv_n_kernel(const __grid_cons
                     const unsigned char *row = st + (size_t)r * row_bytes;
                     const int c0 = chunks * part / parts, c1 = chunks * (part + 1) / parts;
                     float acc = 0.0f;
+#pragma unroll 4
                     for (int c = c0 + lane; c < c1; c += 32) {
                         const uint4 w = *reinterpret_cast<const uint4 *>(row + c * 16);
                         float f[LE];
@@ -493,23 +604,26 @@ __global__ void __launch_bounds__(kGnThreads, 1) gemv_n_kernel(const __grid_cons
                         for (int e = 0; e < LE; ++e) acc = fmaf(f[e], xs[c * LE + e], acc);
                     }
                     acc = warp_sum(acc);
-                    if (lane == 0) rowpart[r * parts + part] = acc;
+                    if (lane == 0) rowpart[(rr - r0 + r) * parts + part] = acc;
                 }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        named_sync(1, kGnConsumers);
-        if (t < nr && !*s_abort) {
-            float logit = 0.0f;
-            for (int q = 0; q < parts; ++q) logit += rowpart[t * parts + q];
-            p.y[rr + t] = logit;
-            if (ranks_above(logit, rr + t, best_v, best_i)) {
-                best_v = logit;
-                best_i = rr + t;
-            }
+    }
+    named_sync(1, kGnConsumers);
+
+    // logits in row order, and this CTA's greedy candidate
+    float best_v = -INFINITY;
+    int best_i = 0x7fffffff;
+    for (int r = t; r < r1 - r0; r += kGnConsumers) {
+        float logit = 0.0f;
+        for (int q = 0; q < parts; ++q) logit += rowpart[r * parts + q];
+        p.y[r0 + r] = logit;
+        if (ranks_above(logit, r0 + r, best_v, best_i)) {
+            best_v = logit;
+            best_i = r0 + r;
         }
-        named_sync(1, kGnConsumers);
     }
 
     if (!p.do_argmax) return;
@@ -562,17 +676,36 @@ __global__ void gemv_n_plain_kernel(const T *W, const float *x, int rows, int co
     if (lane == 0) y[r] = acc;
 }
 
-int gemv_n_grid(int rows, int cols, int es) {
-    const long long row_bytes = (long long)cols * es;
-    const long long rps = std::max(1LL, std::min<long long>(kGnMaxRowsPerStage, kGnStageBytes / row_bytes));
-    long long g = (rows + rps - 1) / rps;
-    return (int)std::max(1LL, std::min<long long>(g, sm_count()));
+// Floats of shared memory left for per-row partial sums once the ring and x
+// are placed.
+static long long gn_rowpart_budget(int cols) {
+    return ((long long)kGnSmemMax - (long long)kGnSmemBase - (long long)cols * 4 - 16) / 4;
 }
 
-bool gemv_n_streamable(const void *W, int cols, int es) {
+int gemv_n_grid(int rows, int cols, int es) {
+    const long long row_bytes = (long long)cols * es;
+    const int rps = gn_rows_per_stage(row_bytes);
+    const int parts = gn_parts(rps);
+    long long g = (rows + rps - 1) / rps;
+    g = std::min<long long>(g, sm_count());
+    // enough CTAs that each one's row partials fit in shared memory
+    const long long per = std::max(1LL, gn_rowpart_budget(cols) / parts - 1);
+    g = std::max(g, (rows + per - 1) / per);
+    return (int)std::max(1LL, g);
+}
+
+static size_t gemv_n_smem(int rows, int cols, int es, int grid) {
+    const int rps = gn_rows_per_stage((long long)cols * es);
+    const long long rows_cap = ((long long)rows + grid - 1) / grid + 1;
+    return kGnSmemBase + (size_t)cols * 4 + align_up((size_t)rows_cap * gn_parts(rps) * 4, 16);
+}
+
+bool gemv_n_streamable(const void *W, int rows, int cols, int es) {
     if ((uintptr_t)W & 15) return false;
     const long long row_bytes = (long long)cols * es;
-    return row_bytes % 16 == 0 && row_bytes <= kGnStageBytes && cols <= kGnMaxCols;
+    if (row_bytes % 16 || row_bytes > kGnStageBytes || cols > kGnMaxCols) return false;
+    (void)rows;
+    return gn_rowpart_budget(cols) >= 4LL * gn_parts(gn_rows_per_stage(row_bytes));
 }
 
 template <typename T, int PRO>
@@ -580,7 +713,7 @@ static cudaError_t ensure_gn(bool force = false) {
     static bool done = false;
     if (done && !force) return cudaSuccess;
     cudaError_t e =
-        cudaFuncSetAttribute(gemv_n_kernel<T, PRO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGnSmem);
+        cudaFuncSetAttribute(gemv_n_kernel<T, PRO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGnSmemMax);
     if (e == cudaSuccess) done = true;
     return e;
 }
@@ -589,7 +722,8 @@ template <typename T, int PRO>
 static cudaError_t launch_gn(const GemvNArgs &a, int grid, cudaStream_t stream, bool pdl) {
     cudaError_t e = ensure_gn<T, PRO>();
     if (e != cudaSuccess) return e;
-    return launch_ex(gemv_n_kernel<T, PRO>, dim3(grid), dim3(kGnThreads), kGnSmem, stream, pdl, a);
+    const size_t smem = gemv_n_smem(a.rows, a.cols, (int)sizeof(T), grid);
+    return launch_ex(gemv_n_kernel<T, PRO>, dim3(grid), dim3(kGnThreads), smem, stream, pdl, a);
 }
 
 template <typename T>
@@ -690,6 +824,7 @@ extern "C" DS_API int ds_gemv_transposed(const void *A, int64_t a_len, int a_dty
     a.counters = reinterpret_cast<int *>(ws + kWsHeader);
     a.partials = reinterpret_cast<float *>(ws + kWsHeader + align_up((size_t)n_bands * 4, 256));
     a.y = y;
+    if (!gemv_t_make_maps(a, a_dtype)) return DS_CUDA_ERROR;
     e = launch_gemv_t(a, a_dtype, PRO_PLAIN, EPI_STORE, grid, s, false);
     return e == cudaSuccess ? DS_OK : DS_CUDA_ERROR;
 }
@@ -701,7 +836,7 @@ extern "C" DS_API int ds_gemv(const void *W, int64_t w_len, int w_dtype, const f
     const int es = w_dtype == DS_BF16 ? 2 : 4;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (!gemv_n_streamable(W, (int)cols, es)) {
+    if (!gemv_n_streamable(W, (int)rows, (int)cols, es)) {
         const int threads = 256, warps = threads / 32;
         const int blocks = (int)((rows + warps - 1) / warps);
         if (w_dtype == DS_BF16)

@@ -1,6 +1,7 @@
 // Internal interfaces between the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -46,12 +47,21 @@ enum Epi { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU = 2, EPI_QKV = 3 };
 
 // Bytes of one band's row segment in shared memory, rows per pipeline stage
 // and stages of the transposed GEMV's ring.
+#ifndef DS_GT_ROWS
+#define DS_GT_ROWS 64
+#endif
+#ifndef DS_GT_STAGES
+#define DS_GT_STAGES 4
+#endif
+constexpr int kGtBoxRows = 8;               // rows of one tensor-map box (the unit of work)
 constexpr int kGtBandBytes = 512;
-constexpr int kGtRows = 32;
-constexpr int kGtStages = 6;
+constexpr int kGtRows = DS_GT_ROWS;
+constexpr int kGtStages = DS_GT_STAGES;
 constexpr int kGtConsumerWarps = 8;
 
 struct GemvTArgs {
+    CUtensorMap tm0;      // 2-D map of sub-tile 0: {sub_cols, K}, box {band columns, kGtBoxRows}
+    CUtensorMap tm1;      // same for sub-tile 1 (EPI_SILU's up columns)
     const char *a0;       // element (k, c) of sub-tile 0 at a0 + k*row_stride + c*es
     const char *a1;       // sub-tile 1 (the up columns for EPI_SILU) or nullptr
     long long row_stride; // bytes between consecutive rows
@@ -61,6 +71,7 @@ struct GemvTArgs {
     const float *x;       // PRO_PLAIN: x[K]; PRO_RMSNORM: the residual [K]
     const float *norm_w;  // PRO_RMSNORM weight [K] (fp32)
     float eps;
+    int xs_cap;           // floats of shared memory for this CTA's slice of x
     float *partials;      // (grid + n_bands) * band_cols floats
     int *counters;        // n_bands ints, zero between launches
     int *err;
@@ -82,8 +93,11 @@ struct GemvTArgs {
 inline int gemv_t_band_cols(int es) { return kGtBandBytes / es; }
 int gemv_t_grid(int K, int n_bands);
 size_t gemv_t_partial_floats(int grid, int n_bands, int es);
-// Can the bulk-copy kernel stream this matrix?
+// Can the tensor-map kernel stream this matrix?
 bool gemv_t_streamable(const void *a0, const void *a1, long long row_stride, int sub_cols, int es);
+// Encode a.tm0 (and a.tm1 when a.a1 is set) from a0/a1, row_stride, sub_cols
+// and K for a matrix of the given dtype; false if the driver refuses.
+bool gemv_t_make_maps(GemvTArgs &a, int dtype);
 cudaError_t launch_gemv_t(const GemvTArgs &a, int dtype, int pro, int epi, int grid,
                           cudaStream_t stream, bool pdl);
 
@@ -106,7 +120,7 @@ struct GemvNArgs {
     int *err;
 };
 int gemv_n_grid(int rows, int cols, int es);
-bool gemv_n_streamable(const void *W, int cols, int es);
+bool gemv_n_streamable(const void *W, int rows, int cols, int es);
 cudaError_t launch_gemv_n(const GemvNArgs &a, int dtype, int pro, int grid, cudaStream_t stream,
                           bool pdl);
 

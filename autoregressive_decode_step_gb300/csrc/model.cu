@@ -46,6 +46,8 @@ struct ds_model {
     int nb_qkv, nb_o, nb_gu, nb_d;
     int attn_splits;
     int es;
+    // tensor maps of every projection, per layer: qkv, o, gate, up, down
+    std::vector<CUtensorMap> maps;
 };
 
 struct ds_step_graph {
@@ -83,7 +85,7 @@ int validate(const ds_model_config *c) {
         ((int64_t)c->n_kvh * c->head_dim * es) % 16)
         return DS_BAD_ARGUMENT;
     if (gemv_t_band_cols(es) % c->head_dim) return DS_BAD_ARGUMENT;
-    if (!gemv_n_streamable(nullptr, c->d, es)) return DS_BAD_ARGUMENT;
+    if (!gemv_n_streamable(nullptr, c->vocab, c->d, es)) return DS_BAD_ARGUMENT;
     if (!(c->eps >= 0.0f) || !(c->rope_base > 0.0)) return DS_BAD_ARGUMENT;
     if (c->max_seqs != 1) return DS_BAD_ARGUMENT;  // batch-1 path
     return DS_OK;
@@ -172,9 +174,11 @@ struct Recorder {
     }
 };
 
+// Launch one decode step; with only_kind >= 0 launch just the kernels of
+// that kind (DS_KIND_*), in step order, for timing.
 int run_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
              const ds_sampling *sampling, const float *u, int32_t *next_ids, float *logits_out, unsigned flags,
-             cudaStream_t s, Recorder *rec) {
+             cudaStream_t s, Recorder *rec, int only_kind = -1) {
     const ds_model_config &c = m->cfg;
     const int es = m->es;
     const int nq = c.n_qh * c.head_dim, nkv = c.n_kvh * c.head_dim;
@@ -183,11 +187,13 @@ int run_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, 
     const bool advance = (flags & DS_STEP_ADVANCE) != 0;
     float *logits = logits_out ? logits_out : m->logits;
     cudaError_t e;
-#define DS_TRY(expr, kind)                              \
-    do {                                                \
-        e = (expr);                                     \
-        if (e != cudaSuccess) return DS_CUDA_ERROR;     \
-        if (rec && !rec->record(kind)) return DS_CUDA_ERROR; \
+#define DS_TRY(expr, kind)                                   \
+    do {                                                     \
+        if (only_kind < 0 || only_kind == (kind)) {          \
+            e = (expr);                                      \
+            if (e != cudaSuccess) return DS_CUDA_ERROR;      \
+            if (rec && !rec->record(kind)) return DS_CUDA_ERROR; \
+        }                                                    \
     } while (0)
 
     if (rec && !rec->record(-1)) return DS_CUDA_ERROR;
@@ -223,6 +229,7 @@ int run_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, 
         a.block_table = kv->block_table;
         a.block_tokens = kv->block_tokens;
         a.max_blocks = kv->max_blocks;
+        a.tm0 = m->maps[5 * l + 0];
         DS_TRY(launch_gemv_t(a, c.w_dtype, PRO_RMSNORM, EPI_QKV, m->grid_qkv, s, pdl), DS_KIND_QKV);
 
         // 2. attention over positions 0..pos
@@ -257,6 +264,7 @@ int run_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, 
         a.n_bands = m->nb_o;
         a.x = m->att;
         a.y = m->x;
+        a.tm0 = m->maps[5 * l + 1];
         DS_TRY(launch_gemv_t(a, c.w_dtype, PRO_PLAIN, EPI_ADD, m->grid_o, s, pdl), DS_KIND_O_PROJ);
 
         // 4. f = silu(Wg^T h) * (Wu^T h), h = RMSNorm(x, n2)
@@ -270,6 +278,8 @@ int run_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, 
         a.x = m->x;
         a.norm_w = m->n2[l];
         a.y = m->f;
+        a.tm0 = m->maps[5 * l + 2];
+        a.tm1 = m->maps[5 * l + 3];
         DS_TRY(launch_gemv_t(a, c.w_dtype, PRO_RMSNORM, EPI_SILU, m->grid_gu, s, pdl), DS_KIND_GATE_UP);
 
         // 5. x += Wd^T f
@@ -281,6 +291,7 @@ int run_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, 
         a.n_bands = m->nb_d;
         a.x = m->f;
         a.y = m->x;
+        a.tm0 = m->maps[5 * l + 4];
         DS_TRY(launch_gemv_t(a, c.w_dtype, PRO_PLAIN, EPI_ADD, m->grid_d, s, pdl), DS_KIND_DOWN);
     }
 
@@ -412,6 +423,49 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
     m->nb_d = L.nb_d;
     m->attn_splits = L.attn_splits;
 
+    // tensor maps of every projection
+    {
+        const int es = m->es;
+        const int nq = cfg->n_qh * cfg->head_dim, nkv = cfg->n_kvh * cfg->head_dim;
+        m->maps.resize((size_t)5 * cfg->n_layer);
+        for (int l = 0; l < cfg->n_layer; ++l) {
+            GemvTArgs a = {};
+            a.a0 = static_cast<const char *>(m->wqkv[l]);
+            a.row_stride = (long long)(nq + 2 * nkv) * es;
+            a.K = cfg->d;
+            a.sub_cols = nq + 2 * nkv;
+            bool ok = gemv_t_make_maps(a, cfg->w_dtype);
+            m->maps[5 * l + 0] = a.tm0;
+            a = GemvTArgs{};
+            a.a0 = static_cast<const char *>(m->wo[l]);
+            a.row_stride = (long long)cfg->d * es;
+            a.K = nq;
+            a.sub_cols = cfg->d;
+            ok = ok && gemv_t_make_maps(a, cfg->w_dtype);
+            m->maps[5 * l + 1] = a.tm0;
+            a = GemvTArgs{};
+            a.a0 = static_cast<const char *>(m->wgu[l]);
+            a.a1 = static_cast<const char *>(m->wgu[l]) + (size_t)cfg->ff * es;
+            a.row_stride = (long long)2 * cfg->ff * es;
+            a.K = cfg->d;
+            a.sub_cols = cfg->ff;
+            ok = ok && gemv_t_make_maps(a, cfg->w_dtype);
+            m->maps[5 * l + 2] = a.tm0;
+            m->maps[5 * l + 3] = a.tm1;
+            a = GemvTArgs{};
+            a.a0 = static_cast<const char *>(m->wd[l]);
+            a.row_stride = (long long)cfg->d * es;
+            a.K = cfg->ff;
+            a.sub_cols = cfg->d;
+            ok = ok && gemv_t_make_maps(a, cfg->w_dtype);
+            m->maps[5 * l + 4] = a.tm0;
+            if (!ok) {
+                delete m;
+                return DS_CUDA_ERROR;
+            }
+        }
+    }
+
     if (prepare_kernels() != cudaSuccess || cudaMemset(workspace, 0, L.total) != cudaSuccess ||
         launch_rope_table(m->rope_cos, m->rope_sin, cfg->max_ctx, cfg->head_dim, cfg->rope_base, nullptr) !=
             cudaSuccess ||
@@ -516,5 +570,33 @@ extern "C" DS_API int ds_decode_step_profile(ds_model *m, const ds_kv_cache *kv,
         kinds_out[i] = rec.kind[i + 1];
     }
     *n_out = n;
+    return DS_OK;
+}
+
+extern "C" DS_API int ds_decode_kernel_time(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos,
+                                            int kind, int reps, float *us_per_launch, ds_stream_t stream) {
+    if (reps < 1 || !us_per_launch || kind < 0 || kind >= DS_KIND_COUNT || kind == DS_KIND_SAMPLE)
+        return DS_BAD_ARGUMENT;
+    int st = check_step(m, kv, tokens, pos, 1, nullptr, nullptr, m ? m->am_idx : nullptr);
+    if (st != DS_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // next ids go to a scratch word of the workspace, so the caller's state
+    // is not advanced
+    int32_t *scratch_ids = reinterpret_cast<int32_t *>(m->ws) + 1;
+    cudaEvent_t e0, e1;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return DS_CUDA_ERROR;
+    st = run_step(m, kv, tokens, pos, 1, nullptr, nullptr, scratch_ids, nullptr, 0, s, nullptr, kind);  // warm
+    if (st == DS_OK && cudaEventRecord(e0, s) != cudaSuccess) st = DS_CUDA_ERROR;
+    for (int r = 0; r < reps && st == DS_OK; ++r)
+        st = run_step(m, kv, tokens, pos, 1, nullptr, nullptr, scratch_ids, nullptr, 0, s, nullptr, kind);
+    float ms = 0.0f;
+    if (st == DS_OK && (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                        cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess))
+        st = DS_CUDA_ERROR;
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (st != DS_OK) return st;
+    const int per_step = (kind == DS_KIND_EMBED || kind == DS_KIND_HEAD) ? 1 : m->cfg.n_layer;
+    *us_per_launch = 1000.0f * ms / (float)(reps * std::max(per_step, 1));
     return DS_OK;
 }

@@ -153,6 +153,17 @@ class DecodeModel:
                   "ds_decode_step_profile")
         return [(abi.KIND_NAMES[kinds[i]], ms[i]) for i in range(n.value)]
 
+    def kernel_time_us(self, kind, reps=4, stream=None):
+        """Mean microseconds per launch of one kernel kind ("qkv", "attention",
+        "o_proj", "gate_up", "down", "head", "embed"), launched back to back
+        over every layer (see ds_decode_kernel_time)."""
+        us = ctypes.c_float(0.0)
+        abi.check(abi.lib.ds_decode_kernel_time(self._h, ctypes.byref(self._kv), abi.ptr(self.tokens),
+                                                abi.ptr(self.pos), abi.KIND_NAMES.index(kind), reps,
+                                                ctypes.byref(us), abi.stream_handle(stream)),
+                  "ds_decode_kernel_time")
+        return us.value
+
     def error_word(self, stream=None):
         return abi.ds_workspace_error(self.ws, stream)
 

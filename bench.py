@@ -1,0 +1,420 @@
+#!/usr/bin/env python
+"""Batch-1 decode benchmark of the Llama-3-8B-shaped random-init decoder.
+
+One step = one whole single-token decode step (32 layers of q|k|v, RoPE+KV
+write, attention, o, gate|up+SiLU, down, then the output head and greedy
+argmax) replayed from a captured CUDA graph with the token and position
+advanced on the device.  The context starts at --ctx prefilled positions
+(a random prompt run through the same decode step) and grows by one per step.
+
+Prints one JSON line (see the keys below).  `--impl reference` times the CPU
+oracle on the host cores instead (a bounded sample per step, scaled to the
+same metric).  Under torchrun each rank decodes its own replica (no data-path
+communication); rank 0 prints the aggregate.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tokens/s and % of GB300 HBM roofline; per-op us vs CPU oracle"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=256)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--ctx", type=int, default=1024, help="prefilled context before the first timed step")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layers", type=int, default=None,
+                   help="decoder layers (default: the model's 32); fewer layers make a small profiling case, "
+                        "not a benchmark number")
+    p.add_argument("--kv-fill", choices=["prefill", "synthetic"], default="prefill",
+                   help="fill the first --ctx cache positions by prefilling a random prompt through the decode "
+                        "step, or with seeded N(0,1) K/V values (same step cost, far fewer launches)")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_config(args, cfg):
+    from autoregressive_decode_step_gb300 import configs as C
+    return {"workload": "llama3-8b-shape random-init decoder, batch-1 greedy decode, context %d + %d decoded "
+                        "(positions %d..%d)" % (args.ctx, args.steps, args.ctx, args.ctx + args.steps - 1),
+            "context": args.ctx, "batch": 1, "layers": cfg["n_layer"], "d": cfg["d"], "ff": cfg["ff"],
+            "heads": "%dq/%dkv x %d" % (cfg["n_qh"], cfg["n_kvh"], cfg["head_dim"]), "vocab": cfg["vocab"],
+            "weights": "bf16", "kv_cache": "bf16", "activations": "fp32",
+            "l2": "inputs larger than L2 (%.1f GB of weights streamed per step)" % (C.weight_bytes_per_step(cfg) / 1e9),
+            "parallelism": "replicas (one independent decoder per GPU)"}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world):
+    """Largest value over all ranks (timing is taken as the slowest rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id):
+        self.samples = []
+        self.proc = None
+        self.bus_id = bus_id
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.bus_id, "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.perf_counter(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 - 0.15 <= t <= t1 + 0.15] or [s for (_, s) in self.samples[-3:]]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [x.strip() for x in r.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_token_time(cfg, ctx, reps, seed=0):
+    """Seconds per decoded token of the CPU oracle for the full model,
+    estimated from a bounded sample: the oracle's decode step on the same
+    shape with 0 layers (embedding, final norm, output head) and with 1 layer,
+    at position `ctx` over a synthetic context; per token = head part + n_layer
+    x layer part.  Returns (seconds per token, threads, description)."""
+    import torch
+
+    import oracle as O
+    from autoregressive_decode_step_gb300 import synth
+
+    one = dict(cfg, n_layer=1)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    W = synth.model_weights(one, seed=seed, device=dev)
+    st = synth.weights_to_numpy(W)
+    del W
+    ks, vs = synth.synthetic_kv(one, ctx, seed=seed + 1, device="cpu")
+    ocfg = dict(one, block_tokens=1, max_blocks=ctx + 1)
+    m1 = O.Model(ocfg, st)
+    m0 = O.Model(dict(ocfg, n_layer=0), st)
+    from autoregressive_decode_step_gb300.synth import to_numpy_storage
+    m1.k[0][:ks[0].numel()] = to_numpy_storage(ks[0])
+    m1.v[0][:vs[0].numel()] = to_numpy_storage(vs[0])
+    t_head, t_one = [], []
+    for _ in range(reps):
+        t = time.perf_counter()
+        m0.step(7, ctx)
+        t_head.append(time.perf_counter() - t)
+        t = time.perf_counter()
+        m1.step(7, ctx)
+        t_one.append(time.perf_counter() - t)
+    th, t1 = min(t_head), min(t_one)
+    per_token = th + cfg["n_layer"] * max(t1 - th, 0.0)
+    desc = ("oracle decode step at position %d over a synthetic %d-position context, timed with 0 and 1 "
+            "layers of the %s shape (best of %d); per token = head part + %d x layer part"
+            % (ctx, ctx, cfg["name"], reps, cfg["n_layer"]))
+    return per_token, O.threads(), desc, (th, t1)
+
+
+def run_reference(args, rank, world):
+    from autoregressive_decode_step_gb300 import configs as C
+    import oracle as O
+    import torch
+    from autoregressive_decode_step_gb300 import synth
+
+    if rank != 0:
+        return 0
+    cfg = C.LLAMA3_8B
+    one = dict(cfg, n_layer=1)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    W = synth.model_weights(one, seed=0, device=dev)
+    st = synth.weights_to_numpy(W)
+    del W
+    cap = args.ctx + args.warmup + args.steps + 1
+    ks, vs = synth.synthetic_kv(one, args.ctx, seed=1, device="cpu")
+    ocfg = dict(one, block_tokens=1, max_blocks=cap)
+    m1 = O.Model(ocfg, st)
+    m0 = O.Model(dict(ocfg, n_layer=0), st)
+    m1.k[0][:ks[0].numel()] = synth.to_numpy_storage(ks[0])
+    m1.v[0][:vs[0].numel()] = synth.to_numpy_storage(vs[0])
+    t = time.perf_counter()
+    m0.step(7, args.ctx)
+    t_head = time.perf_counter() - t
+    tok = 7
+    pos = args.ctx
+    for _ in range(args.warmup):
+        logits = m1.step(tok, pos)
+        tok, pos = O.argmax(logits.astype("float32"))[0], pos + 1
+    total = 0.0
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        logits = m1.step(tok, pos)
+        dt = time.perf_counter() - t
+        tok, pos = O.argmax(logits.astype("float32"))[0], pos + 1
+        total += dt + (cfg["n_layer"] - 1) * max(dt - t_head, 0.0)
+    value = args.steps / total
+    sample = ("each step: the oracle's decode step with 1 of the 32 layers plus the full output head, greedy, "
+              "context growing from %d; per token = step time + 31 x (step time - head-only time %.3f s)"
+              % (args.ctx, t_head))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(args, cfg),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def profile_summary_traffic(kernel_src_sha):
+    """DRAM bytes per launch of the gate|up projection from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "gemv_gate_up_llama3_8b.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = traffic = None
+    for line in text.splitlines():
+        if line.startswith("- kernel source sha256:"):
+            sha = line.split(":", 1)[1].strip()
+        if line.startswith("- dram bytes per launch:"):
+            try:
+                traffic = float(line.split(":", 1)[1].strip().split()[0].replace(",", ""))
+            except ValueError:
+                traffic = None
+    return traffic if sha == kernel_src_sha else None
+
+
+def run_ours(args, rank, world, local):
+    import hashlib
+
+    import torch
+
+    from autoregressive_decode_step_gb300 import build as B
+    B.build()
+    from autoregressive_decode_step_gb300 import configs as C
+    from autoregressive_decode_step_gb300 import synth
+    from autoregressive_decode_step_gb300.model import DecodeModel
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = dict(C.LLAMA3_8B)
+    if args.layers is not None:
+        cfg["n_layer"] = args.layers
+    K, Wm = args.steps, args.warmup
+    cap = args.ctx + max(Wm, K) + 8
+    W = synth.model_weights(cfg, seed=0, device=dev)
+    model = DecodeModel(cfg, W, capacity=cap, device=dev, block_tokens=16)
+    if args.kv_fill == "prefill":
+        prompt = synth.prompt_ids(cfg, args.ctx, seed=rank)
+        model.prefill(prompt)
+        first = int(model.next_ids[0])
+    else:
+        ks, vs = synth.synthetic_kv(cfg, args.ctx, seed=rank + 1, device=dev)
+        for l in range(cfg["n_layer"]):
+            model.k_cache[l][:args.ctx].copy_(ks[l])
+            model.v_cache[l][:args.ctx].copy_(vs[l])
+        del ks, vs
+        first = synth.prompt_ids(cfg, 1, seed=rank)[0]
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        replay = model.graph(advance=True, write_logits=False, stream=stream)
+
+    def reset():
+        model.set_state([first], [args.ctx])
+        torch.cuda.synchronize()
+
+    # ---------------- device-timed region: K graph replays
+    reset()
+    for _ in range(Wm):
+        replay(stream)
+    stream.synchronize()
+    reset()
+    props = torch.cuda.get_device_properties(dev)
+    bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), getattr(props, "pci_bus_id", 0),
+                                getattr(props, "pci_device_id", 0))
+    clocks = ClockSampler(bus)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(K):
+        replay(stream)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.perf_counter()
+    ms = e0.elapsed_time(e1)
+    time.sleep(0.2)
+    clocks.stop()
+    err = model.error_word()
+    if err:
+        raise RuntimeError("device error word %d during the timed region" % err)
+    ms_max = max_over_ranks(ms, world)
+    step_ms = ms_max / K
+    value = world * K / (ms_max / 1000.0)
+
+    # ---------------- end to end: host token in, id out, every step
+    tok_host = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    id_host = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    reset()
+    tok_host[0] = first
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(K):
+            model.tokens[:1].copy_(tok_host, non_blocking=True)
+            replay(stream)
+            id_host.copy_(model.next_ids[:1], non_blocking=True)
+            stream.synchronize()
+            tok_host[0] = id_host[0]
+    t1 = time.perf_counter()
+    e2e_s = max_over_ranks(t1 - t0, world)
+    e2e_value = world * K / e2e_s
+
+    # ---------------- per-kernel timing: each kind launched back to back over
+    # every layer, CUDA events around the passes, on the bench stream
+    reset()
+    kinds = ["embed", "qkv", "attention", "o_proj", "gate_up", "down", "head"]
+    us = {k: model.kernel_time_us(k, reps=4, stream=stream) for k in kinds}
+    per_step = {k: us[k] * (1 if k in ("embed", "head") else cfg["n_layer"]) for k in kinds}
+    gu_us = us["gate_up"]
+    gu_bytes = cfg["d"] * 2 * cfg["ff"] * 2 + cfg["d"] * 4 + cfg["ff"] * 4
+    peak, peak_kind = peaks()
+    src = open(os.path.join(ROOT, "autoregressive_decode_step_gb300", "csrc", "gemv.cu"), "rb").read()
+    sha = hashlib.sha256(src).hexdigest()
+    achieved = gu_bytes / (gu_us / 1e6) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profile_summary_traffic(sha),
+                "kernel": "gemv_t_kernel gate|up with SiLU epilogue, 4096x28672 bf16",
+                "peak_source": peak_kind, "algorithmic_bytes_per_launch": gu_bytes, "mean_launch_us": gu_us}
+    # the whole step against the HBM roofline (weights once + K/V read)
+    step_bytes = [C.step_bytes(cfg, args.ctx + i + 1) for i in range(K)]
+    step_gbs = sum(step_bytes) / (ms / 1000.0) / 1e9
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
+            "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (random-init weights N(0,0.02), random prompt)",
+            "config": dict(workload_config(args, cfg), kv_fill=args.kv_fill),
+            "hbm_roofline_step": {"bytes_per_step_mean": sum(step_bytes) / K, "achieved_gbs": step_gbs,
+                                  "peak_gbs": peak, "frac": step_gbs / peak,
+                                  "frac_of_nominal_7900": step_gbs / NOMINAL_HBM_GBS},
+            "roofline": roofline,
+            "per_op_us_per_launch": us, "per_op_us_per_step": per_step,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
+            "gpu_launches": K * (2 + 5 * cfg["n_layer"]),
+            "clocks": clocks.summary(t_wall0, t_wall1)}
+    del W, model
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        per_tok, threads, desc, parts = oracle_token_time(C.LLAMA3_8B, args.ctx, reps=3)
+        line["cpu_baseline"] = {"value": 1.0 / per_tok, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": desc, "head_s": parts[0], "one_layer_step_s": parts[1]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        rc = run_reference(args, rank, world)
+    else:
+        rc = run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

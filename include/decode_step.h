@@ -374,6 +374,17 @@ enum {
     DS_KIND_SAMPLE = 7,
     DS_KIND_COUNT = 8
 };
+/* Mean duration, in microseconds, of one launch of the step's kernels of one
+ * kind (DS_KIND_*, not DS_KIND_SAMPLE), measured with CUDA events around
+ * `reps` passes over all of that kind's launches of a step (every layer's),
+ * launched back to back on `stream` as in a step.  The kernels read and write
+ * the model's buffers and the cache row at pos[0] as a step would (the
+ * residual stream is left changed), but tokens and pos are not advanced.
+ * Synchronises `stream`. */
+DS_API int ds_decode_kernel_time(ds_model *model, const ds_kv_cache *kv, int32_t *tokens,
+                                 int32_t *pos, int kind, int reps, float *us_per_launch,
+                                 ds_stream_t stream);
+
 DS_API int ds_decode_step_profile(ds_model *model, const ds_kv_cache *kv, int32_t *tokens,
                                   int32_t *pos, int n_seqs, const ds_sampling *sampling,
                                   const float *u, int32_t *next_ids, float *logits_out,

@@ -31,6 +31,7 @@ def lib():
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         D = ctypes.c_double
+        L.or_threads.restype = ctypes.c_int
         L.or_f32_to_bf16.argtypes = [ctypes.c_float]
         L.or_f32_to_bf16.restype = ctypes.c_uint16
         L.or_residual_dims_check.argtypes = [I64, I64, I64]
@@ -64,6 +65,11 @@ def _c(a, dtype):
 def _stored(a, dt):
     """A stored operand: float32 values, or uint16 raw bf16 bits."""
     return _c(a, np.float32 if dt == DT_F32 else np.uint16)
+
+
+def threads():
+    """Threads the oracle's parallel loops use."""
+    return lib().or_threads()
 
 
 # ---------------------------------------------------------------- elements

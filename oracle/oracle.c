@@ -28,6 +28,9 @@
  */
 #include <math.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdlib.h>
 #include <string.h>
 
@@ -50,6 +53,15 @@
 #define OR_CACHE_CAPACITY_EXCEEDED 571
 #define OR_BAD_SAMPLING_PARAM 575
 #define OR_MAX_DIM (1LL << 24)
+
+/* Threads the OpenMP loops use (1 without OpenMP). */
+int or_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------ */
 /* element access                                                      */
