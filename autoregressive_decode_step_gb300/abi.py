@@ -88,6 +88,8 @@ _sig("ds_device_sm_count", ctypes.c_int)
 _sig("ds_gemv_workspace_bytes", SZ, I64, I64, ctypes.c_int)
 _sig("ds_gemv_transposed", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P, SZ, P)
 _sig("ds_gemv", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P)
+_sig("ds_gemv_transposed_noalloc", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P)
+_sig("ds_gemv_transposed_noalloc_max_bytes", SZ)
 _sig("ds_residual_add", ctypes.c_int, P, I64, P, I64, P, I64, P)
 _sig("ds_add_rmsnorm", ctypes.c_int, P, I64, P, I64, P, I64, ctypes.c_int, F32, P, I64, I64, P)
 _sig("ds_rope", ctypes.c_int, P, I64, P, I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, F64, ctypes.c_int, P)
@@ -173,6 +175,11 @@ def ds_gemv_workspace_bytes(rows, cols, dtype=DS_F32):
 def ds_gemv_transposed(A, x, rows, cols, y, ws, stream=None):
     check(lib.ds_gemv_transposed(ptr(A), A.numel(), dtype_code(A), ptr(x), x.numel(), rows, cols, ptr(y),
                                  y.numel(), ptr(ws), nbytes(ws), stream_handle(stream)), "ds_gemv_transposed")
+
+
+def ds_gemv_transposed_noalloc(A, x, rows, cols, y, stream=None):
+    check(lib.ds_gemv_transposed_noalloc(ptr(A), A.numel(), dtype_code(A), ptr(x), x.numel(), rows, cols, ptr(y),
+                                         y.numel(), stream_handle(stream)), "ds_gemv_transposed_noalloc")
 
 
 def ds_gemv(W, x, rows, cols, y, stream=None):

@@ -132,6 +132,27 @@ DS_API int ds_gemv_transposed(const void *A, int64_t a_len, int a_dtype, const f
                               int64_t y_len, void *workspace, size_t workspace_bytes,
                               ds_stream_t stream);
 
+/* ds_gemv_transposed for callers that cannot allocate device memory (for
+ * example a host whose device memory is all owned by its own allocator, or a
+ * plug-in handed nothing but one operation's inputs and outputs).  The pages
+ * have no counterpart of this call.  Same arguments, result and checks as
+ * ds_gemv_transposed, minus the workspace: the split-reduction scratch comes
+ * from a fixed area compiled into the library, which every GPU that loads the
+ * library keeps (ds_gemv_transposed_noalloc_max_bytes() bytes, 1 MiB) until
+ * the process exits.  A shape whose scratch (ds_gemv_workspace_bytes) does not
+ * fit in it is refused with DS_DIMENSION_TOO_LARGE.  The call allocates
+ * nothing: it clears the part of the area that must start at zero with one
+ * asynchronous memset and launches the kernel on `stream`.
+ *  - The first call on a device (that device current) looks up the area's
+ *    device address; make that first call before any stream capture.
+ *  - All calls share the one area and it keeps the last call's contents:
+ *    calls whose GPU work overlaps (other streams, other threads) race on it
+ *    and must be ordered by the caller. */
+DS_API int ds_gemv_transposed_noalloc(const void *A, int64_t a_len, int a_dtype, const float *x,
+                                      int64_t x_len, int64_t rows, int64_t cols, float *y,
+                                      int64_t y_len, ds_stream_t stream);
+DS_API size_t ds_gemv_transposed_noalloc_max_bytes(void);
+
 /* y = W x: y[r] = sum_c W[r * cols + c] * x[c] for r < rows — the
  * untransposed form the "LLM inference kernels" page uses for lm_head.
  *   W: rows*cols of w_dtype (569), x: cols fp32 (570), y: rows fp32 (562). */
