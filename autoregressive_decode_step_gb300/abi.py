@@ -44,6 +44,8 @@ DS_ROPE_HALF_SPLIT, DS_ROPE_INTERLEAVED = 0, 1
 DS_ERR_TOKEN_RANGE, DS_ERR_POSITION, DS_ERR_WAIT_TIMEOUT, DS_ERR_SAMPLING = 1, 2, 4, 8
 DS_SAMPLE_MAX_TOP_K = 1024
 DS_STEP_ADVANCE = 1
+DS_STEP_PHASE_TIMES = 2
+DS_STEP_TRACE = 4
 KIND_NAMES = ["embed", "qkv", "attention", "o_proj", "gate_up", "down", "head", "sample"]
 
 P = ctypes.c_void_p
@@ -113,6 +115,8 @@ _sig("ds_step_graph_create", ctypes.c_int, P, ctypes.POINTER(KVCache), P, P, cty
      ctypes.POINTER(Sampling), P, P, P, ctypes.c_uint, P, ctypes.POINTER(P))
 _sig("ds_step_graph_launch", ctypes.c_int, P, P)
 _sig("ds_step_graph_destroy", None, P)
+_sig("ds_model_phase_times", ctypes.c_int, P, P, ctypes.c_int, ctypes.POINTER(ctypes.c_int), P)
+_sig("ds_model_trace", ctypes.c_int, P, P, SZ, ctypes.POINTER(SZ), ctypes.POINTER(ctypes.c_int), P)
 _sig("ds_decode_kernel_time", ctypes.c_int, P, ctypes.POINTER(KVCache), P, P, ctypes.c_int, ctypes.c_int,
      ctypes.POINTER(ctypes.c_float), P)
 _sig("ds_decode_step_profile", ctypes.c_int, P, ctypes.POINTER(KVCache), P, P, ctypes.c_int,

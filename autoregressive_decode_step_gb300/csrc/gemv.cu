@@ -51,15 +51,6 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long W, int G) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-// One 2-D tensor-map box (columns c0.., rows r0..) into shared memory.
-__device__ __forceinline__ void tma_box_g2s(void *dst, const CUtensorMap *map, int c0, int r0, uint64_t *bar,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
 
 template <typename T, int PRO, int EPI>
 __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_constant__ GemvTArgs p) {

@@ -53,7 +53,10 @@ enum Epi { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU = 2, EPI_QKV = 3 };
 #ifndef DS_GT_STAGES
 #define DS_GT_STAGES 4
 #endif
-constexpr int kGtBoxRows = 8;               // rows of one tensor-map box (the unit of work)
+#ifndef DS_ST_BOX_ROWS
+#define DS_ST_BOX_ROWS 16
+#endif
+constexpr int kGtBoxRows = DS_ST_BOX_ROWS;  // rows of one tensor-map box (the unit of work)
 constexpr int kGtBandBytes = 512;
 constexpr int kGtRows = DS_GT_ROWS;
 constexpr int kGtStages = DS_GT_STAGES;
@@ -183,5 +186,59 @@ struct SampleArgs {
     int *err;
 };
 cudaError_t launch_sample(const SampleArgs &a, cudaStream_t stream, bool pdl);
+
+// ------------------------------------------------------------------ the step kernel
+constexpr int kStMaxLayers = 128;
+constexpr int kStMaxSplits = 64;
+
+struct StepLayer {  // aligned as CUtensorMap requires
+    CUtensorMap maps[5];  // q|k|v, o, gate, up, down
+    const float *n1, *n2;
+};
+
+struct StepParams {
+    const StepLayer *layers;
+    int n_layer;
+    const char *emb, *head;
+    const float *final_norm;
+    int vocab, d, nq_cols, nkv_cols, hd, ff, rope_layout, kv_dtype, n_kvh, n_qh;
+    float eps;
+    const float *rope_cos, *rope_sin;
+    int rope_rows;
+    const int *block_table;
+    int block_tokens, max_blocks;
+    int *tokens, *pos, *next_ids;
+    float *logits;
+    int advance, greedy;
+    float *x, *q, *att, *f;
+    float *partials;
+    int *counters;
+    float *ss;              // per-band square sums of the residual (n_ss bands)
+    int n_ss;
+    float *a_partials;
+    int *a_counters;
+    float *am_val;
+    int *am_idx;
+    int *am_counter;
+    unsigned *bar;          // u64 arrival count, then u64 epoch (see grid_sync)
+    int *err;
+    int *abort_flag;
+    unsigned long long *phase_times;  // optional: globaltimer at every phase start, then at the end
+    unsigned long long *trace;        // optional: [phase][cta][5] per-CTA timestamps
+    int nb_qkv, nb_o, nb_gu, nb_d;
+    int attn_splits;
+    int stages;             // ring stages in use
+    int scratch_floats;     // shared scratch after the ring
+    void *kc[kStMaxLayers];
+    void *vc[kStMaxLayers];
+};
+
+size_t step_layer_bytes();
+void step_layer_fill(void *dst, const CUtensorMap *maps5, const float *n1, const float *n2);
+int step_scratch_floats(const ds_model_config *c, int grid, int nb_qkv, int nb_o, int nb_gu, int nb_d);
+bool step_supported(const ds_model_config *c);
+int step_stages(int scratch_floats);
+size_t step_smem_bytes(int stages, int scratch_floats);
+cudaError_t launch_step(const void *params, int w_dtype, int kv_dtype, int gq, int grid, cudaStream_t stream);
 
 }  // namespace ds

@@ -48,6 +48,17 @@ struct ds_model {
     int es;
     // tensor maps of every projection, per layer: qkv, o, gate, up, down
     std::vector<CUtensorMap> maps;
+    // the persistent step kernel
+    bool step_ok;
+    int step_grid, step_splits, step_stages, step_scratch;
+    ds::StepLayer *step_layers;
+    unsigned *step_bar;
+    int *step_abort;
+    unsigned long long *phase_times;
+    int n_phase_times;
+    unsigned long long *trace;
+    size_t trace_words;
+    float *ss;
 };
 
 struct ds_step_graph {
@@ -61,8 +72,10 @@ using namespace ds;
 
 struct Layout {
     size_t x, q, att, f, logits, rope_cos, rope_sin, g_counters, g_partials, a_counters, a_partials, am_val,
-        am_idx, am_counter, total;
+        am_idx, am_counter, step_layers, step_bar, phase_times, trace, ss, total;
     int grid_qkv, grid_o, grid_gu, grid_d, grid_head, nb_qkv, nb_o, nb_gu, nb_d, attn_splits;
+    bool step_ok;
+    int step_grid, step_splits, step_stages, step_scratch, n_phase_times;
 };
 
 int validate(const ds_model_config *c) {
@@ -113,11 +126,23 @@ Layout make_layout(const ds_model_config *c) {
     L.grid_d = gemv_t_grid(c->ff, L.nb_d);
     L.grid_head = gemv_n_grid(c->vocab, c->d, es);
     L.attn_splits = attention_splits(S, c->n_kvh, c->max_ctx);
+    // the persistent step kernel: one CTA per SM
+    L.step_grid = sm_count();
+    L.step_ok = step_supported(c) && c->n_kvh <= L.step_grid;
+    if (L.step_ok) {
+        L.step_splits = std::max(1, std::min(L.step_grid / c->n_kvh, kStMaxSplits));
+        L.step_scratch = step_scratch_floats(c, L.step_grid, L.nb_qkv, L.nb_o, L.nb_gu, L.nb_d);
+        L.step_stages = step_stages(L.step_scratch);
+        L.step_ok = L.step_stages >= 2;
+    }
+    L.n_phase_times = 5 * c->n_layer + 4;
     size_t partial = 0;
     partial = std::max(partial, gemv_t_partial_floats(L.grid_qkv, L.nb_qkv, es));
     partial = std::max(partial, gemv_t_partial_floats(L.grid_o, L.nb_o, es));
     partial = std::max(partial, gemv_t_partial_floats(L.grid_gu, L.nb_gu, es));
     partial = std::max(partial, gemv_t_partial_floats(L.grid_d, L.nb_d, es));
+    const int max_nb = std::max(std::max(L.nb_qkv, L.nb_o), std::max(L.nb_gu, L.nb_d));
+    partial = std::max(partial, gemv_t_partial_floats(L.step_grid, max_nb, es));
     const int max_bands = std::max(std::max(L.nb_qkv, L.nb_o), std::max(L.nb_gu, L.nb_d));
     size_t off = kWsHeader;
     L.x = carve(off, (size_t)S * c->d * 4);
@@ -130,10 +155,16 @@ Layout make_layout(const ds_model_config *c) {
     L.g_counters = carve(off, (size_t)max_bands * 4);
     L.g_partials = carve(off, partial * 4);
     L.a_counters = carve(off, (size_t)S * c->n_kvh * 4);
-    L.a_partials = carve(off, attention_partial_floats(S, c->n_qh, c->n_kvh, c->head_dim, L.attn_splits) * 4);
-    L.am_val = carve(off, (size_t)L.grid_head * 4);
-    L.am_idx = carve(off, (size_t)L.grid_head * 4);
+    L.a_partials = carve(off, attention_partial_floats(S, c->n_qh, c->n_kvh, c->head_dim,
+                                                       std::max(L.attn_splits, L.step_splits)) * 4);
+    L.am_val = carve(off, (size_t)std::max(L.grid_head, L.step_grid) * 4);
+    L.am_idx = carve(off, (size_t)std::max(L.grid_head, L.step_grid) * 4);
     L.am_counter = carve(off, 4);
+    L.step_layers = carve(off, (size_t)std::max(c->n_layer, 1) * step_layer_bytes());
+    L.step_bar = carve(off, 32);  // arrival count (u64), epoch (u64), abort flag
+    L.phase_times = carve(off, (size_t)L.n_phase_times * 8);
+    L.trace = carve(off, (size_t)L.n_phase_times * L.step_grid * 5 * 8);
+    L.ss = carve(off, (size_t)(L.nb_o + 1) * 4);
     L.total = off;
     return L;
 }
@@ -374,9 +405,10 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
     if ((uintptr_t)workspace & 255) return DS_BAD_ARGUMENT;
     auto aligned = [](const void *p) { return p && ((uintptr_t)p & 15) == 0; };
     if (!aligned(w->emb) || (!cfg->tied && !aligned(w->out))) return DS_BAD_ARGUMENT;
+    if (!aligned(w->final_norm)) return DS_BAD_ARGUMENT;
     for (int l = 0; l < cfg->n_layer; ++l)
-        if (!aligned(w->wqkv[l]) || !aligned(w->wo[l]) || !aligned(w->wgu[l]) || !aligned(w->wd[l]) || !w->n1[l] ||
-            !w->n2[l])
+        if (!aligned(w->wqkv[l]) || !aligned(w->wo[l]) || !aligned(w->wgu[l]) || !aligned(w->wd[l]) ||
+            !aligned(w->n1[l]) || !aligned(w->n2[l]))
             return DS_BAD_ARGUMENT;
 
     ds_model *m = new (std::nothrow) ds_model();
@@ -465,8 +497,25 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
             }
         }
     }
+    m->step_ok = L.step_ok;
+    m->step_grid = L.step_grid;
+    m->step_splits = L.step_splits;
+    m->step_stages = L.step_stages;
+    m->step_scratch = L.step_scratch;
+    m->step_layers = reinterpret_cast<StepLayer *>(ws + L.step_layers);
+    m->step_bar = reinterpret_cast<unsigned *>(ws + L.step_bar);
+    m->step_abort = reinterpret_cast<int *>(ws + L.step_bar + 16);
+    m->phase_times = reinterpret_cast<unsigned long long *>(ws + L.phase_times);
+    m->n_phase_times = L.n_phase_times;
+    m->trace = reinterpret_cast<unsigned long long *>(ws + L.trace);
+    m->trace_words = (size_t)L.n_phase_times * L.step_grid * 5;
+    m->ss = reinterpret_cast<float *>(ws + L.ss);
 
+    std::vector<unsigned char> layer_img((size_t)std::max(cfg->n_layer, 1) * step_layer_bytes(), 0);
+    for (int l = 0; l < cfg->n_layer; ++l)
+        step_layer_fill(layer_img.data() + (size_t)l * step_layer_bytes(), &m->maps[5 * l], w->n1[l], w->n2[l]);
     if (prepare_kernels() != cudaSuccess || cudaMemset(workspace, 0, L.total) != cudaSuccess ||
+        cudaMemcpy(m->step_layers, layer_img.data(), layer_img.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
         launch_rope_table(m->rope_cos, m->rope_sin, cfg->max_ctx, cfg->head_dim, cfg->rope_base, nullptr) !=
             cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
@@ -481,13 +530,113 @@ extern "C" DS_API void ds_model_destroy(ds_model *m) { delete m; }
 
 extern "C" DS_API void *ds_model_workspace(ds_model *m) { return m ? m->ws : nullptr; }
 
+// One step through the persistent step kernel (and the sampler after it).
+int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
+                   const ds_sampling *sampling, const float *u, int32_t *next_ids, float *logits_out, unsigned flags,
+                   cudaStream_t s) {
+    const ds_model_config &c = m->cfg;
+    const bool greedy = sampling == nullptr || !(sampling->temperature > 0.0f);
+    const bool advance = (flags & DS_STEP_ADVANCE) != 0;
+    float *logits = logits_out ? logits_out : m->logits;
+    StepParams p;
+    std::memset(&p, 0, sizeof p);
+    p.layers = m->step_layers;
+    p.n_layer = c.n_layer;
+    p.emb = static_cast<const char *>(m->emb);
+    p.head = static_cast<const char *>(c.tied ? m->emb : m->out);
+    p.final_norm = m->final_norm;
+    p.vocab = c.vocab;
+    p.d = c.d;
+    p.nq_cols = c.n_qh * c.head_dim;
+    p.nkv_cols = c.n_kvh * c.head_dim;
+    p.hd = c.head_dim;
+    p.ff = c.ff;
+    p.rope_layout = c.rope_layout;
+    p.kv_dtype = c.kv_dtype;
+    p.n_kvh = c.n_kvh;
+    p.n_qh = c.n_qh;
+    p.eps = c.eps;
+    p.rope_cos = m->rope_cos;
+    p.rope_sin = m->rope_sin;
+    p.rope_rows = c.max_ctx;
+    p.block_table = kv->block_table;
+    p.block_tokens = kv->block_tokens;
+    p.max_blocks = kv->max_blocks;
+    p.tokens = tokens;
+    p.pos = pos;
+    p.next_ids = next_ids;
+    p.logits = logits;
+    p.advance = advance && greedy;
+    p.greedy = greedy;
+    p.x = m->x;
+    p.q = m->q;
+    p.att = m->att;
+    p.f = m->f;
+    p.partials = m->g_partials;
+    p.counters = m->g_counters;
+    p.ss = m->ss;
+    p.n_ss = m->nb_o;
+    p.a_partials = m->a_partials;
+    p.a_counters = m->a_counters;
+    p.am_val = m->am_val;
+    p.am_idx = m->am_idx;
+    p.am_counter = m->am_counter;
+    p.bar = m->step_bar;
+    p.err = m->err;
+    p.abort_flag = m->step_abort;
+    p.phase_times = (flags & (DS_STEP_PHASE_TIMES | DS_STEP_TRACE)) ? m->phase_times : nullptr;
+    p.trace = (flags & DS_STEP_TRACE) ? m->trace : nullptr;
+    p.nb_qkv = m->nb_qkv;
+    p.nb_o = m->nb_o;
+    p.nb_gu = m->nb_gu;
+    p.nb_d = m->nb_d;
+    p.attn_splits = m->step_splits;
+    p.stages = m->step_stages;
+    p.scratch_floats = m->step_scratch;
+    for (int l = 0; l < c.n_layer; ++l) {
+        p.kc[l] = kv->k[l];
+        p.vc[l] = kv->v[l];
+    }
+    if (launch_step(&p, c.w_dtype, c.kv_dtype, c.n_qh / c.n_kvh, m->step_grid, s) != cudaSuccess)
+        return DS_CUDA_ERROR;
+    if (!greedy) {
+        SampleArgs sa = {};
+        sa.logits = logits;
+        sa.n_rows = n_seqs;
+        sa.n = c.vocab;
+        sa.temperature = sampling->temperature;
+        sa.top_k = sampling->top_k;
+        sa.top_p = sampling->top_p;
+        sa.u = u;
+        sa.ids = next_ids;
+        sa.tokens_adv = advance ? tokens : nullptr;
+        sa.pos_adv = advance ? pos : nullptr;
+        sa.err = m->err;
+        if (launch_sample(sa, s, false) != cudaSuccess) return DS_CUDA_ERROR;
+    }
+    return DS_OK;
+}
+
 extern "C" DS_API int ds_decode_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
                                      const ds_sampling *sampling, const float *u, int32_t *next_ids,
                                      float *logits_out, unsigned flags, ds_stream_t stream) {
     int st = check_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids);
     if (st != DS_OK) return st;
-    return run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags,
-                    reinterpret_cast<cudaStream_t>(stream), nullptr);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (m->step_ok && n_seqs == 1)
+        return run_step_fused(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s);
+    return run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s, nullptr);
+}
+
+extern "C" DS_API int ds_model_phase_times(ds_model *m, uint64_t *ns_out, int cap, int *n_out, ds_stream_t stream) {
+    if (!m || !ns_out || !n_out || cap < 1) return DS_BAD_ARGUMENT;
+    const int n = std::min(cap, m->n_phase_times);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(ns_out, m->phase_times, (size_t)n * 8, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return DS_CUDA_ERROR;
+    *n_out = n;
+    return DS_OK;
 }
 
 extern "C" DS_API int ds_step_graph_create(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos,
@@ -501,7 +650,9 @@ extern "C" DS_API int ds_step_graph_create(ds_model *m, const ds_kv_cache *kv, i
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!s) return DS_BAD_ARGUMENT;  // the legacy stream cannot be captured
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return DS_CUDA_ERROR;
-    st = run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s, nullptr);
+    st = (m->step_ok && n_seqs == 1)
+             ? run_step_fused(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s)
+             : run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s, nullptr);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(s, &graph);
     if (st != DS_OK || e != cudaSuccess) {
@@ -598,5 +749,18 @@ extern "C" DS_API int ds_decode_kernel_time(ds_model *m, const ds_kv_cache *kv, 
     if (st != DS_OK) return st;
     const int per_step = (kind == DS_KIND_EMBED || kind == DS_KIND_HEAD) ? 1 : m->cfg.n_layer;
     *us_per_launch = 1000.0f * ms / (float)(reps * std::max(per_step, 1));
+    return DS_OK;
+}
+
+extern "C" DS_API int ds_model_trace(ds_model *m, uint64_t *out, size_t cap_words, size_t *n_words, int *n_ctas,
+                                     ds_stream_t stream) {
+    if (!m || !out || !n_words || !n_ctas) return DS_BAD_ARGUMENT;
+    const size_t n = std::min(cap_words, m->trace_words);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(out, m->trace, n * 8, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return DS_CUDA_ERROR;
+    *n_words = n;
+    *n_ctas = m->step_grid;
     return DS_OK;
 }

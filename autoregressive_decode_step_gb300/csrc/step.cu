@@ -1,0 +1,1140 @@
+// The whole batch-1 decode step as one persistent kernel.
+//
+// One CTA per SM (cooperative launch), eight consumer warps and one producer
+// warp.  The step is a fixed sequence of phases ("The forward pass end to
+// end", "What a forward step does"; "Inside the engine", section 1):
+//   embed | per layer: q|k|v (RMSNorm prologue, RoPE + K/V write epilogue) |
+//   attention | o (+ residual) | gate|up (RMSNorm prologue, SiLU epilogue) |
+//   down (+ residual) | final RMSNorm + output head + greedy argmax.
+// Consumers meet at a grid barrier between phases (every phase needs the
+// whole output of the one before).  The producer warp never waits at those
+// barriers: weights do not depend on activations, so it streams the next
+// phase's weight boxes into the shared-memory ring while consumers finish a
+// phase, wait at a barrier or run attention.  The weight stream therefore
+// runs across phase boundaries without the drain and refill a kernel launch
+// per phase would cost.
+//
+// Arithmetic per phase is the same as the standalone kernels': stream-K
+// ranges of 8-row x 512-byte tensor-map boxes for the transposed projections,
+// fixed-order cross-CTA reductions by the last CTA of each band, whole-row
+// bulk copies for the head.  Activations written by other CTAs are read
+// through L2 (ld.global.cg) so no stale L1 line is ever used.  Every wait is
+// bounded: a grid barrier or mbarrier that times out sets the error word and
+// an abort flag, after which the remaining phases run without waiting.
+#include <algorithm>
+#include <climits>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ds {
+
+constexpr int kStConsumerWarps = 8;
+constexpr int kStConsumers = kStConsumerWarps * 32;
+constexpr int kStThreads = kStConsumers + 32;
+#ifndef DS_ST_STAGE_BYTES
+#define DS_ST_STAGE_BYTES 65536
+#endif
+constexpr int kStStageBytes = DS_ST_STAGE_BYTES;
+constexpr int kStMaxStages = 16;
+#ifndef DS_ST_BOX_ROWS
+#define DS_ST_BOX_ROWS 16
+#endif
+constexpr int kStBoxRows = DS_ST_BOX_ROWS;
+constexpr int kStBandBytes = 512;
+constexpr int kStBoxesPerStage = kStStageBytes / (kStBoxRows * kStBandBytes);  // 8 boxes of 16 rows at 64 KB
+constexpr size_t kStSmemLimit = 227 * 1024;
+
+__device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
+
+__device__ __forceinline__ bool aborted(const StepParams &p) {
+    return *reinterpret_cast<volatile int *>(p.abort_flag) != 0;
+}
+
+__device__ __forceinline__ void raise_abort(const StepParams &p, int bit) {
+    flag_error(p.err, bit);
+    atomicExch(p.abort_flag, 1);
+}
+
+// Bounded mbarrier wait that also gives up once the step is aborted.
+__device__ __forceinline__ bool st_wait(uint64_t *bar, uint32_t parity, const StepParams &p) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (aborted(p)) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                raise_abort(p, DS_ERR_WAIT_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Grid barrier among the consumer warps of every CTA (the producer warps
+// never take part).  p.bar[0] is a 64-bit arrival count that only grows; a
+// launch's k-th barrier completes when the count reaches
+// base + (k + 1) * G, base = epoch * G * barriers-per-step, where the epoch
+// (p.bar[1]) is read by every CTA at its start and advanced once per launch
+// after the first barrier.  Arrivals are fire-and-forget release reductions,
+// so 152 arrivals do not queue behind one another.  Bounded; on time-out the
+// step is aborted and later barriers return at once.
+struct GridBarrier {
+    unsigned long long base;
+    int k;
+};
+
+__device__ void grid_sync(const StepParams &p, int G, GridBarrier &b) {
+    named_sync(1, kStConsumers);
+    const unsigned long long target = b.base + (unsigned long long)(b.k + 1) * (unsigned long long)G;
+    ++b.k;
+    if (threadIdx.x == 0 && !aborted(p)) {
+        unsigned long long *count = reinterpret_cast<unsigned long long *>(p.bar);
+        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(count) : "memory");
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t it = 0;; ++it) {
+            unsigned long long c;
+            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(c) : "l"(count) : "memory");
+            if (c >= target) break;
+            if ((it & 63u) == 63u) {
+                if (aborted(p)) break;
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    raise_abort(p, DS_ERR_WAIT_TIMEOUT);
+                    break;
+                }
+            }
+        }
+    }
+    named_sync(1, kStConsumers);
+}
+
+__device__ __forceinline__ void mark_phase(const StepParams &p, int &phase) {
+    if (p.phase_times && blockIdx.x == 0 && threadIdx.x == 0) p.phase_times[phase] = global_timer_ns();
+    ++phase;
+}
+
+// Per-CTA trace point k (0 phase start, 1 prologue done, 2 last stage
+// consumed, 3 epilogue done; 4 is the producer's last issue of the phase).
+__device__ __forceinline__ void trace_point(const StepParams &p, int phase, int k) {
+    if (p.trace && (threadIdx.x == 0 || k == 4))
+        p.trace[((size_t)phase * gridDim.x + blockIdx.x) * 5 + k] = global_timer_ns();
+}
+
+// ---------------------------------------------------------------- producer
+struct Ring {
+    unsigned char *base;
+    uint64_t *full, *empty;
+    int stages;
+};
+
+// Wait until ring slot `fill` is free, announce `bytes` on its full barrier;
+// returns the slot's shared-memory address or nullptr once aborted.
+__device__ __forceinline__ unsigned char *ring_acquire(const Ring &r, uint32_t fill, uint32_t bytes,
+                                                       const StepParams &p) {
+    const int s = fill % r.stages;
+    const uint32_t use = fill / r.stages;
+    if (use > 0 && !st_wait(&r.empty[s], (use - 1) & 1, p)) return nullptr;
+    mbar_arrive_expect_tx(&r.full[s], bytes);
+    return r.base + (size_t)s * kStStageBytes;
+}
+
+// Cursor over every weight stage this CTA streams in a step, in order: per
+// layer the q|k|v, o, gate|up and down boxes of this CTA's range, then its
+// rows of the head.
+struct StageCursor {
+    int l, ph;  // layer and projection (0 q|k|v, 1 o, 2 gate|up, 3 down); l == n_layer: head
+    const CUtensorMap *m0, *m1;
+    int UB, sub_band_cols;
+    uint32_t box_bytes;
+    long long u, u1;
+    int band, j, j1;
+    int rr, r1, rps;
+    long long row_bytes;
+    bool done;
+};
+
+struct StageDesc {
+    bool head;
+    const CUtensorMap *m0, *m1;
+    int col, row0, nb;
+    uint32_t box_bytes, bytes;
+    const char *src;
+};
+
+template <int ES>
+__device__ void cursor_phase(StageCursor &c, const StepParams &p) {
+    constexpr int BAND_COLS = kStBandBytes / ES;
+    const int G0 = gridDim.x;
+    for (;;) {
+        if (c.l >= p.n_layer) {
+            const long long rows = p.vocab;
+            c.row_bytes = (long long)p.d * ES;
+            c.rps = (int)max(1LL, (long long)kStStageBytes / c.row_bytes);
+            c.rr = (int)(rows * blockIdx.x / G0);
+            c.r1 = (int)(rows * (blockIdx.x + 1) / G0);
+            c.done = c.rr >= c.r1;
+            return;
+        }
+        const StepLayer &L = p.layers[c.l];
+        int K, nb;
+        c.m1 = nullptr;
+        if (c.ph == 0) { c.m0 = &L.maps[0]; K = p.d; nb = p.nb_qkv; }
+        else if (c.ph == 1) { c.m0 = &L.maps[1]; K = p.nq_cols; nb = p.nb_o; }
+        else if (c.ph == 2) { c.m0 = &L.maps[2]; c.m1 = &L.maps[3]; K = p.d; nb = p.nb_gu; }
+        else { c.m0 = &L.maps[4]; K = p.ff; nb = p.nb_d; }
+        c.sub_band_cols = c.m1 ? BAND_COLS / 2 : BAND_COLS;
+        c.box_bytes = kStBoxRows * c.sub_band_cols * ES;
+        c.UB = (K + kStBoxRows - 1) / kStBoxRows;
+        const long long W = (long long)nb * c.UB;
+        const int G = (int)min((long long)G0, W);
+        const bool in = (int)blockIdx.x < G;
+        c.u = in ? W * blockIdx.x / G : 0;
+        c.u1 = in ? W * (blockIdx.x + 1) / G : 0;
+        if (c.u < c.u1) {
+            c.band = (int)(c.u / c.UB);
+            c.j = (int)(c.u - (long long)c.band * c.UB);
+            c.j1 = (int)min((long long)c.UB, c.j + (c.u1 - c.u));
+            return;
+        }
+        if (++c.ph == 4) { c.ph = 0; ++c.l; }  // nothing for this CTA here
+    }
+}
+
+template <int ES>
+__device__ void cursor_begin(StageCursor &c, const StepParams &p) {
+    c.l = 0;
+    c.ph = 0;
+    c.done = false;
+    cursor_phase<ES>(c, p);
+}
+
+template <int ES>
+__device__ bool cursor_desc(const StageCursor &c, const StepParams &p, StageDesc &d) {
+    if (c.done) return false;
+    if (c.l >= p.n_layer) {
+        const int nr = min(c.rps, c.r1 - c.rr);
+        d.head = true;
+        d.src = p.head + (long long)c.rr * c.row_bytes;
+        d.bytes = (uint32_t)(nr * c.row_bytes);
+        return true;
+    }
+    d.head = false;
+    d.m0 = c.m0;
+    d.m1 = c.m1;
+    d.col = c.band * c.sub_band_cols;
+    d.row0 = c.j * kStBoxRows;
+    d.nb = min(kStBoxesPerStage, c.j1 - c.j);
+    d.box_bytes = c.box_bytes;
+    d.bytes = (uint32_t)d.nb * c.box_bytes * (c.m1 ? 2 : 1);
+    return true;
+}
+
+template <int ES>
+__device__ void cursor_advance(StageCursor &c, const StepParams &p) {
+    if (c.done) return;
+    if (c.l >= p.n_layer) {
+        c.rr += c.rps;
+        c.done = c.rr >= c.r1;
+        return;
+    }
+    const int nb = min(kStBoxesPerStage, c.j1 - c.j);
+    c.j += nb;
+    c.u += nb;
+    if (c.j < c.j1) return;
+    if (c.u < c.u1) {  // next segment (band) of this phase
+        c.band = (int)(c.u / c.UB);
+        c.j = (int)(c.u - (long long)c.band * c.UB);
+        c.j1 = (int)min((long long)c.UB, c.j + (c.u1 - c.u));
+        return;
+    }
+    if (++c.ph == 4) {
+        c.ph = 0;
+        ++c.l;
+    }
+    cursor_phase<ES>(c, p);
+}
+
+// Issue the copies of one stage into ring slot `s`.
+__device__ __forceinline__ void issue_stage(const StageDesc &d, unsigned char *dst, uint64_t *bar, uint64_t pol) {
+    if (d.head) {
+        bulk_g2s(dst, d.src, d.bytes, bar, pol);
+        return;
+    }
+    for (int b = 0; b < d.nb; ++b) {
+        tma_box_g2s(dst + b * d.box_bytes, d.m0, d.col, d.row0 + b * kStBoxRows, bar, pol);
+        if (d.m1) tma_box_g2s(dst + kStStageBytes / 2 + b * d.box_bytes, d.m1, d.col, d.row0 + b * kStBoxRows, bar, pol);
+    }
+}
+
+// The producer: every weight stage of the step, in order, through the ring.
+template <int ES>
+__device__ void produce_all(const Ring &r, const StepParams &p) {
+    const uint64_t pol = policy_evict_first();
+    StageCursor fc;
+    cursor_begin<ES>(fc, p);
+    uint32_t fill = 0;
+    StageDesc d;
+    while (cursor_desc<ES>(fc, p, d)) {
+        const int s = fill % r.stages;
+        const uint32_t use = fill / r.stages;
+        if (use > 0 && !st_wait(&r.empty[s], (use - 1) & 1, p)) break;
+        mbar_arrive_expect_tx(&r.full[s], d.bytes);
+        issue_stage(d, r.base + (size_t)s * kStStageBytes, &r.full[s], pol);
+        cursor_advance<ES>(fc, p);
+        ++fill;
+    }
+    const uint32_t first = fill > (uint32_t)r.stages ? fill - r.stages : 0;
+    for (uint32_t f = first; f < fill; ++f)
+        if (!st_wait(&r.full[f % r.stages], (f / r.stages) & 1, p)) break;
+}
+
+// ---------------------------------------------------------------- consumers
+__device__ __forceinline__ float silu_st(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+
+// RMS scale of v[0..n) (square sum in fp32, fixed order), read through L2;
+// n a multiple of 4.  Each thread's loads are issued together.
+__device__ float rms_scale(const float *v, int n, float eps, float *red) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    float ss = 0.0f;
+    for (int base = 0; base < n; base += 4 * 4 * kStConsumers) {
+        float4 r[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = base + (q * kStConsumers + t) * 4;
+            r[q] = i < n ? ldcg4(v + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            ss = fmaf(r[q].x, r[q].x, ss);
+            ss = fmaf(r[q].y, r[q].y, ss);
+            ss = fmaf(r[q].z, r[q].z, ss);
+            ss = fmaf(r[q].w, r[q].w, ss);
+        }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    named_sync(1, kStConsumers);
+    float tot = 0.0f;
+    for (int w = 0; w < kStConsumerWarps; ++w) tot += red[w];
+    named_sync(1, kStConsumers);
+    return 1.0f / sqrtf(tot / (float)n + eps);
+}
+
+enum { ST_STORE = 0, ST_ADD = 1, ST_SILU = 2, ST_QKV = 3 };
+
+// One transposed projection phase: this CTA's boxes from the ring, the
+// cross-CTA reduction, and the fused epilogue.
+// RMS scale of the residual from its per-band square sums p.ss[0..n_ss)
+// (written by whichever phase last wrote the residual), summed in band order.
+__device__ float scale_from_ss(const StepParams &p, int n, float *red) {
+    const int t = threadIdx.x;
+    float v = 0.0f;
+    if (t < 32) {
+        for (int b = t; b < p.n_ss; b += 32) v += ldcg(p.ss + b);  // lane-order partials
+        v = warp_sum(v);
+        if (t == 0) red[0] = v;
+    }
+    named_sync(1, kStConsumers);
+    const float tot = red[0];
+    named_sync(1, kStConsumers);
+    return 1.0f / sqrtf(tot / (float)n + p.eps);
+}
+
+// Sum of squares of v over the 256 consumer threads (t >= count adds 0).
+__device__ float block_sumsq(float v, float *red) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    float s2 = warp_sum(v * v);
+    if (lane == 0) red[warp] = s2;
+    named_sync(1, kStConsumers);
+    float tot = 0.0f;
+    for (int w = 0; w < kStConsumerWarps; ++w) tot += red[w];
+    named_sync(1, kStConsumers);
+    return tot;
+}
+
+// One transposed projection phase: this CTA's boxes from the ring, the
+// cross-CTA reduction, and the fused epilogue.  Bands this CTA covers whole
+// finish as soon as they are streamed; a band shared with other CTAs (only a
+// CTA's first and last segment can be) publishes its partial sums at once and
+// is settled after the whole range is streamed, so that waiting for the other
+// CTAs never stalls the stream.
+template <typename T, int EPI, bool NORM>
+__device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, int n_bands, const float *xin,
+                           const float *norm_w, float *y, int layer, float *scratch, const StepParams &p,
+                           int phase) {
+    constexpr int ES = sizeof(T);
+    constexpr int LE = 16 / ES;
+    constexpr int BAND_COLS = kStBandBytes / ES;
+    constexpr bool PAIRED = EPI == ST_SILU;
+    constexpr int SUB_BAND_COLS = PAIRED ? BAND_COLS / 2 : BAND_COLS;
+    constexpr int SUB_ROW_BYTES = SUB_BAND_COLS * ES;
+    float *red = scratch;                  // [8][256]
+    float *vals = red + kStConsumerWarps * 256;
+    volatile int *s_flag = reinterpret_cast<volatile int *>(vals + 256);  // [2]
+    float *xs = vals + 256 + 16;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int UB = (K + kStBoxRows - 1) / kStBoxRows;
+    const long long W = (long long)n_bands * UB;
+    // only min(grid, W) CTAs take part, so that every one has a non-empty
+    // range and the contributors to a band are consecutive CTAs
+    const int G = (int)min((long long)gridDim.x, W);
+    const bool in = (int)blockIdx.x < G;
+    const long long u0 = in ? W * blockIdx.x / G : 0, u1 = in ? W * (blockIdx.x + 1) / G : 0;
+    trace_point(p, phase, 0);
+    if (!in) return;
+
+    const float scale = NORM ? scale_from_ss(p, K, red) : 1.0f;
+    {   // this CTA's slice of x (normalised; zero past K), four floats per
+        // thread per pass with every pass's loads issued together
+        int off = 0;
+        for (long long u = u0; u < u1;) {
+            const int band = (int)(u / UB);
+            const int j0 = (int)(u - (long long)band * UB);
+            const int j1 = (int)min((long long)UB, j0 + (u1 - u));
+            u += j1 - j0;
+            const int k0 = j0 * kStBoxRows, k1 = j1 * kStBoxRows;
+            for (int kb = k0; kb < k1; kb += 4 * 4 * kStConsumers) {
+                float4 v[4], w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int k = kb + (q * kStConsumers + t) * 4;
+                    const bool ok = k < k1 && k < K;
+                    v[q] = ok ? ldcg4(xin + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    w[q] = (NORM && ok) ? *reinterpret_cast<const float4 *>(norm_w + k) : make_float4(1.f, 1.f, 1.f, 1.f);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int k = kb + (q * kStConsumers + t) * 4;
+                    if (k < k1) {
+                        float4 o = v[q];
+                        if (NORM) {
+                            o.x = o.x * scale * w[q].x;
+                            o.y = o.y * scale * w[q].y;
+                            o.z = o.z * scale * w[q].z;
+                            o.w = o.w * scale * w[q].w;
+                        }
+                        *reinterpret_cast<float4 *>(xs + off + k - k0) = o;
+                    }
+                }
+            }
+            off += k1 - k0;
+        }
+        named_sync(1, kStConsumers);
+    }
+    trace_point(p, phase, 1);
+
+    // the fused epilogue of one band whose column sums v (thread t < BAND_COLS)
+    // are final; y_old is the residual value already loaded (ST_ADD) or NAN
+    auto epilogue = [&](int band, float v, float y_old) {
+        if (EPI == ST_STORE || EPI == ST_ADD) {
+            const int col = band * BAND_COLS + t;
+            const bool ok = t < BAND_COLS && col < sub_cols;
+            float out = v;
+            if (EPI == ST_ADD) out = ok ? (y_old == y_old ? y_old : ldcg(y + col)) + v : 0.0f;
+            if (ok) y[col] = out;
+            if (EPI == ST_ADD) {  // this band's share of the next RMSNorm
+                const float ss = block_sumsq(ok ? out : 0.0f, red);
+                if (t == 0) p.ss[band] = ss;
+            }
+        } else if (EPI == ST_SILU) {
+            vals[t] = v;
+            named_sync(1, kStConsumers);
+            const int col = band * SUB_BAND_COLS + t;
+            if (t < SUB_BAND_COLS && col < sub_cols) y[col] = silu_st(vals[t]) * vals[t + SUB_BAND_COLS];
+            named_sync(1, kStConsumers);
+        } else {  // ST_QKV: RoPE on q and k, K/V written at pos
+            vals[t] = v;
+            named_sync(1, kStConsumers);
+            const int col = band * BAND_COLS + t;
+            const int total = p.nq_cols + 2 * p.nkv_cols;
+            const int pos = __ldcg(p.pos);
+            const int cap = p.max_blocks * p.block_tokens;
+            const bool pos_ok = pos >= 0 && pos < p.rope_rows && pos < cap;
+            if (!pos_ok && t == 0 && blockIdx.x == 0) flag_error(p.err, DS_ERR_POSITION);
+            if (t < BAND_COLS && col < total) {
+                float out = v;
+                if (col < p.nq_cols + p.nkv_cols) {
+                    const int hd = p.hd, half = hd >> 1;
+                    const int region = col < p.nq_cols ? 0 : p.nq_cols;
+                    const int i = (col - region) % hd;
+                    int pair;
+                    float a, b;
+                    bool first_of_pair;
+                    if (p.rope_layout == DS_ROPE_HALF_SPLIT) {
+                        first_of_pair = i < half;
+                        pair = first_of_pair ? i : i - half;
+                        a = first_of_pair ? vals[t] : vals[t - half];
+                        b = first_of_pair ? vals[t + half] : vals[t];
+                    } else {
+                        first_of_pair = (i & 1) == 0;
+                        pair = i >> 1;
+                        a = first_of_pair ? vals[t] : vals[t - 1];
+                        b = first_of_pair ? vals[t + 1] : vals[t];
+                    }
+                    float c = 1.0f, sn = 0.0f;
+                    if (pos_ok) {
+                        c = p.rope_cos[(size_t)pos * half + pair];
+                        sn = p.rope_sin[(size_t)pos * half + pair];
+                    }
+                    out = first_of_pair ? a * c - b * sn : a * sn + b * c;
+                }
+                if (col < p.nq_cols) {
+                    y[col] = out;
+                } else if (pos_ok) {
+                    const int blk = p.block_table ? __ldcg(p.block_table + pos / p.block_tokens) : pos / p.block_tokens;
+                    const long long row = (long long)blk * p.block_tokens + pos % p.block_tokens;
+                    if (col < p.nq_cols + p.nkv_cols)
+                        store_as(p.kc[layer], row * p.nkv_cols + (col - p.nq_cols), p.kv_dtype, out);
+                    else
+                        store_as(p.vc[layer], row * p.nkv_cols + (col - p.nq_cols - p.nkv_cols), p.kv_dtype, out);
+                }
+            }
+            named_sync(1, kStConsumers);
+        }
+    };
+
+    int pend_band[2], pend_first[2], pend_n[2];
+    int npend = 0;
+    int seg_off = 0;
+    for (long long u = u0; u < u1;) {
+        const int band = (int)(u / UB);
+        const int j0 = (int)(u - (long long)band * UB);
+        const int j1 = (int)min((long long)UB, j0 + (u1 - u));
+        u += j1 - j0;
+        const float *xseg = xs + seg_off - j0 * kStBoxRows;
+        seg_off += (j1 - j0) * kStBoxRows;
+
+        float acc[LE];
+#pragma unroll
+        for (int e = 0; e < LE; ++e) acc[e] = 0.0f;
+        for (int j = j0; j < j1; j += kStBoxesPerStage) {
+            const int nr = min(kStBoxesPerStage, j1 - j) * kStBoxRows;
+            const int s = fill % r.stages;
+            const uint32_t use = fill / r.stages;
+            if (st_wait(&r.full[s], use & 1, p)) {
+                const unsigned char *st = r.base + (size_t)s * kStStageBytes;
+                const unsigned char *lane_base =
+                    PAIRED ? st + (lane >> 4) * (kStStageBytes / 2) + (lane & 15) * 16 : st + lane * 16;
+                const int kr = j * kStBoxRows;
+#pragma unroll 4
+                for (int rr = warp; rr < nr; rr += kStConsumerWarps) {
+                    const float xk = xseg[kr + rr];
+                    const uint4 w = *reinterpret_cast<const uint4 *>(lane_base + rr * SUB_ROW_BYTES);
+                    float fv[LE];
+                    widen16(w, fv);
+#pragma unroll
+                    for (int e = 0; e < LE; ++e) acc[e] = fmaf(fv[e], xk, acc[e]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&r.empty[s]);
+            ++fill;
+        }
+        if (u >= u1) trace_point(p, phase, 2);
+
+        // cross-warp reduction of the band's column sums, fixed order
+#pragma unroll
+        for (int e = 0; e < LE; ++e) red[warp * BAND_COLS + lane * LE + e] = acc[e];
+        named_sync(1, kStConsumers);
+        float v = 0.0f;
+        if (t < BAND_COLS)
+            for (int w = 0; w < kStConsumerWarps; ++w) v += red[w * BAND_COLS + t];
+        named_sync(1, kStConsumers);
+
+        if (j0 == 0 && j1 == UB) {
+            epilogue(band, v, NAN);  // whole band here: final now
+        } else {
+            if (t < BAND_COLS) p.partials[(size_t)(blockIdx.x + band) * BAND_COLS + t] = v;
+            pend_band[npend] = band;
+            pend_first[npend] = (int)((((long long)band * UB + 1) * G - 1) / W);
+            const int last = (int)((((long long)(band + 1) * UB) * G - 1) / W);
+            pend_n[npend] = last - pend_first[npend] + 1;
+            ++npend;
+        }
+    }
+
+    if (npend > 0) {
+        // publish this CTA's partials and learn which shared bands it closes:
+        // one round trip for both, then one for the partial sums.  The old
+        // residual values of those bands (stable until their closing CTA
+        // writes them) are fetched alongside.
+        float yo0 = NAN, yo1 = NAN;
+        if (EPI == ST_ADD && t < BAND_COLS) {
+            const int c0 = pend_band[0] * BAND_COLS + t;
+            if (c0 < sub_cols) yo0 = ldcg(y + c0);
+            if (npend > 1) {
+                const int c1 = pend_band[1] * BAND_COLS + t;
+                if (c1 < sub_cols) yo1 = ldcg(y + c1);
+            }
+        }
+        named_sync(1, kStConsumers);
+        if (t == 0) {
+            int prev0 = -1, prev1 = -1;  // both requests in flight together
+            asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev0) : "l"(&p.counters[pend_band[0]])
+                         : "memory");
+            if (npend > 1)
+                asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev1)
+                             : "l"(&p.counters[pend_band[1]])
+                             : "memory");
+            s_flag[0] = prev0 == pend_n[0] - 1;
+            s_flag[1] = npend > 1 && prev1 == pend_n[1] - 1;
+            if (prev0 == pend_n[0] - 1) p.counters[pend_band[0]] = 0;
+            if (npend > 1 && prev1 == pend_n[1] - 1) p.counters[pend_band[1]] = 0;
+        }
+        named_sync(1, kStConsumers);
+        const bool last0 = s_flag[0] != 0, last1 = npend > 1 && s_flag[1] != 0;
+        named_sync(1, kStConsumers);
+        float v0 = 0.0f, v1 = 0.0f;
+        if (t < BAND_COLS) {
+            const int nmax = max(last0 ? pend_n[0] : 0, last1 ? pend_n[1] : 0);
+#pragma unroll 4
+            for (int c = 0; c < nmax; ++c) {
+                if (last0 && c < pend_n[0])
+                    v0 += ldcg(&p.partials[(size_t)(pend_first[0] + c + pend_band[0]) * BAND_COLS + t]);
+                if (last1 && c < pend_n[1])
+                    v1 += ldcg(&p.partials[(size_t)(pend_first[1] + c + pend_band[1]) * BAND_COLS + t]);
+            }
+        }
+        if (last0) epilogue(pend_band[0], v0, yo0);
+        if (last1) epilogue(pend_band[1], v1, yo1);
+    }
+    trace_point(p, phase, 3);
+}
+
+// K or V dims [d0, d0+4) of one cache row, through L2.
+template <typename KT>
+__device__ __forceinline__ void load4(const KT *base, long long off, bool ok, float (&f)[4]) {
+    if (!ok) {
+        f[0] = f[1] = f[2] = f[3] = 0.0f;
+        return;
+    }
+    if (sizeof(KT) == 2) {
+        uint2 w;
+        asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(w.x), "=r"(w.y) : "l"(base + off));
+        f[0] = __uint_as_float(w.x << 16);
+        f[1] = __uint_as_float(w.x & 0xffff0000u);
+        f[2] = __uint_as_float(w.y << 16);
+        f[3] = __uint_as_float(w.y & 0xffff0000u);
+    } else {
+        const float4 w = __ldcg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(base) + off));
+        f[0] = w.x;
+        f[1] = w.y;
+        f[2] = w.z;
+        f[3] = w.w;
+    }
+}
+
+// Before the barrier that opens the attention phase: request this CTA's
+// share of the K/V rows into L2.  Rows before the current position were
+// written by earlier steps and do not change during this one.
+template <typename KT>
+__device__ void prefetch_attention(int layer, const StepParams &p) {
+    const int n_items = p.n_kvh * p.attn_splits;
+    if ((int)blockIdx.x >= n_items) return;
+    const int g = blockIdx.x / p.attn_splits, split = blockIdx.x % p.attn_splits;
+    const int cap = p.max_blocks * p.block_tokens;
+    const int n_ctx = min(max(__ldcg(p.pos), 0), cap - 1);  // positions before pos
+    const int per = max(64, (n_ctx + 1 + p.attn_splits - 1) / p.attn_splits);
+    const int t0 = min(n_ctx, split * per), t1 = min(n_ctx, t0 + per);
+    const int row_bytes = p.hd * (int)sizeof(KT);  // one head's row
+    const int lines = (row_bytes + 127) / 128;
+    const int n = (t1 - t0) * lines * 2;
+    for (int i = threadIdx.x; i < n; i += kStConsumers) {
+        const int kv = i & 1, rest = i >> 1;
+        const int tt = t0 + rest / lines, line = rest % lines;
+        const int b = tt / p.block_tokens;
+        const long long blk = p.block_table ? (long long)__ldcg(p.block_table + b) : (long long)b;
+        const long long off = ((blk * p.block_tokens + tt % p.block_tokens) * p.n_kvh + g) * (long long)row_bytes + line * 128;
+        const char *base = static_cast<const char *>(kv ? p.vc[layer] : p.kc[layer]);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
+    }
+}
+
+// One CTA's share of the attention phase: item (kv head g, split) = this CTA
+// (CTAs past the items idle); eight warps take runs of eight positions with an
+// online softmax; warps merge in shared memory; the last CTA of a head merges
+// the splits in split order.
+template <typename KT, int GQ>
+__device__ void consume_attention(int layer, float *scratch, const StepParams &p, int phase) {
+    constexpr int RUN = 8;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int hd = p.hd;
+    const int n_items = p.n_kvh * p.attn_splits;
+    trace_point(p, phase, 0);
+    if ((int)blockIdx.x >= n_items) return;
+    const int g = blockIdx.x / p.attn_splits, split = blockIdx.x % p.attn_splits;
+    float *s_acc = scratch;                                   // [8][GQ][hd]
+    float *s_m = s_acc + kStConsumerWarps * GQ * hd;          // [8][GQ]
+    float *s_l = s_m + kStConsumerWarps * GQ;                 // [8][GQ]
+    volatile int *s_flag = reinterpret_cast<volatile int *>(s_l + kStConsumerWarps * GQ);
+
+    const int cap = p.max_blocks * p.block_tokens;
+    int n_ctx = __ldcg(p.pos) + 1;
+    n_ctx = min(max(n_ctx, 1), cap);
+    const int per = max(64, (n_ctx + p.attn_splits - 1) / p.attn_splits);
+    const int n_eff = (n_ctx + per - 1) / per;
+    const int t0 = min(n_ctx, split * per), t1 = min(n_ctx, t0 + per);
+    const bool active = lane * 4 < hd;
+    const int d0 = lane * 4;
+    const long long row_elems = (long long)p.n_kvh * hd;
+    const KT *kc = static_cast<const KT *>(p.kc[layer]);
+    const KT *vc = static_cast<const KT *>(p.vc[layer]);
+
+    float q[GQ][4];
+#pragma unroll
+    for (int j = 0; j < GQ; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) q[j][e] = active ? ldcg(p.q + (g * GQ + j) * hd + d0 + e) : 0.0f;
+    const float scale = 1.0f / sqrtf((float)hd);
+    float m[GQ], l[GQ], acc[GQ][4];
+#pragma unroll
+    for (int j = 0; j < GQ; ++j) {
+        m[j] = -INFINITY;
+        l[j] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
+    }
+    for (int tb = t0 + warp * RUN; tb < t1; tb += kStConsumerWarps * RUN) {
+        const int nt = min(RUN, t1 - tb);
+        float kf[RUN][4], vf[RUN][4];
+#pragma unroll
+        for (int i = 0; i < RUN; ++i) {
+            const bool ok = active && i < nt;
+            long long off = 0;
+            if (ok) {
+                const int tt = tb + i, b = tt / p.block_tokens;
+                const long long blk = p.block_table ? (long long)__ldcg(p.block_table + b) : (long long)b;
+                off = (blk * p.block_tokens + tt % p.block_tokens) * row_elems + (long long)g * hd + d0;
+            }
+            load4<KT>(kc, off, ok, kf[i]);
+            load4<KT>(vc, off, ok, vf[i]);
+        }
+#pragma unroll
+        for (int j = 0; j < GQ; ++j) {
+            float sc[RUN];
+#pragma unroll
+            for (int i = 0; i < RUN; ++i) {
+                float dd = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dd = fmaf(q[j][e], kf[i][e], dd);
+                sc[i] = warp_sum(dd) * scale;
+            }
+            float mx = m[j];
+#pragma unroll
+            for (int i = 0; i < RUN; ++i)
+                if (i < nt) mx = fmaxf(mx, sc[i]);
+            const float corr = expf(m[j] - mx);
+            l[j] *= corr;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][e] *= corr;
+#pragma unroll
+            for (int i = 0; i < RUN; ++i)
+                if (i < nt) {
+                    const float w = expf(sc[i] - mx);
+                    l[j] += w;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[j][e] = fmaf(w, vf[i][e], acc[j][e]);
+                }
+            m[j] = mx;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < GQ; ++j) {
+        if (lane == 0) {
+            s_m[warp * GQ + j] = m[j];
+            s_l[warp * GQ + j] = l[j];
+        }
+        if (active)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s_acc[(warp * GQ + j) * hd + d0 + e] = acc[j][e];
+    }
+    named_sync(1, kStConsumers);
+    trace_point(p, phase, 2);
+
+    const int rec = GQ * (hd + 2);
+    float *part = p.a_partials + (size_t)(g * p.attn_splits + split) * rec;
+    for (int idx = t; split < n_eff && idx < GQ * hd; idx += kStConsumers) {
+        const int j = idx / hd;
+        float M = -INFINITY;
+        for (int w = 0; w < kStConsumerWarps; ++w) M = fmaxf(M, s_m[w * GQ + j]);
+        float L = 0.0f, A = 0.0f;
+        if (M != -INFINITY)
+            for (int w = 0; w < kStConsumerWarps; ++w) {
+                const float c = expf(s_m[w * GQ + j] - M);
+                L = fmaf(s_l[w * GQ + j], c, L);
+                A = fmaf(s_acc[(w * GQ + j) * hd + idx % hd], c, A);
+            }
+        part[2 * GQ + idx] = A;
+        if (idx % hd == 0) {
+            part[j] = M;
+            part[GQ + j] = L;
+        }
+    }
+    named_sync(1, kStConsumers);
+    if (t == 0) {
+        int prev;
+        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev) : "l"(&p.a_counters[g]) : "memory");
+        const bool last = prev == p.attn_splits - 1;
+        if (last) p.a_counters[g] = 0;
+        *s_flag = last;
+    }
+    named_sync(1, kStConsumers);
+    const bool last = *s_flag != 0;
+    named_sync(1, kStConsumers);
+    trace_point(p, phase, 1);
+    if (!last) return;
+
+    const float *base = p.a_partials + (size_t)g * p.attn_splits * rec;
+    float *sm = s_acc;                       // reuse: [n_eff][GQ] weights
+    float *sl = s_acc + kStMaxSplits * GQ;   // [n_eff][GQ]
+    float *sM = sl + kStMaxSplits * GQ;      // [2][GQ]
+    for (int i = t; i < n_eff * GQ; i += kStConsumers) {
+        const int sp = i / GQ, j = i % GQ;
+        sm[i] = ldcg(base + (size_t)sp * rec + j);
+        sl[i] = ldcg(base + (size_t)sp * rec + GQ + j);
+    }
+    named_sync(1, kStConsumers);
+    if (t < GQ) {
+        float M = -INFINITY;
+        for (int sp = 0; sp < n_eff; ++sp) M = fmaxf(M, sm[sp * GQ + t]);
+        sM[t] = M;
+    }
+    named_sync(1, kStConsumers);
+    for (int i = t; i < n_eff * GQ; i += kStConsumers) {
+        const float ms = sm[i];
+        sm[i] = ms == -INFINITY ? 0.0f : expf(ms - sM[i % GQ]);
+    }
+    named_sync(1, kStConsumers);
+    if (t < GQ) {
+        float L = 0.0f;
+        for (int sp = 0; sp < n_eff; ++sp) L = fmaf(sl[sp * GQ + t], sm[sp * GQ + t], L);
+        sM[GQ + t] = L;
+    }
+    named_sync(1, kStConsumers);
+    for (int idx = t; idx < GQ * hd; idx += 2 * kStConsumers) {
+        const int idx2 = idx + kStConsumers;
+        const bool two = idx2 < GQ * hd;
+        const int j = idx / hd, j2 = two ? idx2 / hd : j;
+        float A = 0.0f, A2 = 0.0f;
+#pragma unroll 8
+        for (int sp = 0; sp < n_eff; ++sp) {
+            const float *rp = base + (size_t)sp * rec + 2 * GQ;
+            A = fmaf(ldcg(rp + idx), sm[sp * GQ + j], A);
+            if (two) A2 = fmaf(ldcg(rp + idx2), sm[sp * GQ + j2], A2);
+        }
+        p.att[(g * GQ + j) * hd + idx % hd] = A / sM[GQ + j];
+        if (two) p.att[(g * GQ + j2) * hd + idx2 % hd] = A2 / sM[GQ + j2];
+    }
+    trace_point(p, phase, 3);
+}
+
+// The head phase: logits of this CTA's rows, then the greedy pick.
+template <typename T>
+__device__ void consume_gn(const Ring &r, uint32_t &fill, float *scratch, const StepParams &p) {
+    constexpr int LE = 16 / sizeof(T);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int G = gridDim.x;
+    const int cols = p.d, rows = p.vocab;
+    const long long row_bytes = (long long)cols * sizeof(T);
+    const int rps = (int)max(1LL, (long long)kStStageBytes / row_bytes);
+    const int parts = rps >= kStConsumerWarps ? 1 : kStConsumerWarps / rps;
+    const int r0 = (int)((long long)rows * blockIdx.x / G), r1 = (int)((long long)rows * (blockIdx.x + 1) / G);
+    float *bestv = scratch;                              // [256]
+    int *besti = reinterpret_cast<int *>(bestv + 256);   // [256]
+    float *xs = bestv + 512;                             // [cols]
+    float *rowpart = xs + cols;                          // [rows of this CTA][parts]
+
+    const float scale = scale_from_ss(p, cols, bestv);
+    for (int i = t; i < cols; i += kStConsumers) xs[i] = ldcg(p.x + i) * scale * p.final_norm[i];
+    named_sync(1, kStConsumers);
+
+    const int chunks = (int)(row_bytes / 16);
+    for (int rr = r0; rr < r1; rr += rps) {
+        const int nr = min(rps, r1 - rr);
+        const int s = fill % r.stages;
+        const uint32_t use = fill / r.stages;
+        if (st_wait(&r.full[s], use & 1, p)) {
+            const unsigned char *st = r.base + (size_t)s * kStStageBytes;
+            if (parts == 1) {
+                for (int q = warp; q < nr; q += kStConsumerWarps) {
+                    const unsigned char *row = st + (size_t)q * row_bytes;
+                    float a = 0.0f;
+                    for (int c = lane; c < chunks; c += 32) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(row + c * 16);
+                        float fv[LE];
+                        widen16(w, fv);
+#pragma unroll
+                        for (int e = 0; e < LE; ++e) a = fmaf(fv[e], xs[c * LE + e], a);
+                    }
+                    a = warp_sum(a);
+                    if (lane == 0) rowpart[rr - r0 + q] = a;
+                }
+            } else {
+                const int q = warp / parts, part = warp % parts;
+                if (q < nr) {
+                    const unsigned char *row = st + (size_t)q * row_bytes;
+                    const int c0 = chunks * part / parts, c1 = chunks * (part + 1) / parts;
+                    float a = 0.0f;
+#pragma unroll 4
+                    for (int c = c0 + lane; c < c1; c += 32) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(row + c * 16);
+                        float fv[LE];
+                        widen16(w, fv);
+#pragma unroll
+                        for (int e = 0; e < LE; ++e) a = fmaf(fv[e], xs[c * LE + e], a);
+                    }
+                    a = warp_sum(a);
+                    if (lane == 0) rowpart[(rr - r0 + q) * parts + part] = a;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r.empty[s]);
+        ++fill;
+    }
+    named_sync(1, kStConsumers);
+
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int q = t; q < r1 - r0; q += kStConsumers) {
+        float logit = 0.0f;
+        for (int k = 0; k < parts; ++k) logit += rowpart[q * parts + k];
+        p.logits[r0 + q] = logit;
+        if (ranks_above(logit, r0 + q, bv, bi)) {
+            bv = logit;
+            bi = r0 + q;
+        }
+    }
+    if (!p.greedy) return;
+    bestv[t] = bv;
+    besti[t] = bi;
+    named_sync(1, kStConsumers);
+    if (t == 0) {
+        bv = bestv[0];
+        bi = besti[0];
+        for (int j = 1; j < kStConsumers; ++j)
+            if (ranks_above(bestv[j], besti[j], bv, bi)) {
+                bv = bestv[j];
+                bi = besti[j];
+            }
+        p.am_val[blockIdx.x] = bv;
+        p.am_idx[blockIdx.x] = bi;
+        __threadfence();
+        if (atomicAdd(p.am_counter, 1) == G - 1) {
+            __threadfence();
+            bv = ldcg(&p.am_val[0]);
+            bi = __ldcg(&p.am_idx[0]);
+            for (int j = 1; j < G; ++j) {
+                const float v = ldcg(&p.am_val[j]);
+                const int ix = __ldcg(&p.am_idx[j]);
+                if (ranks_above(v, ix, bv, bi)) {
+                    bv = v;
+                    bi = ix;
+                }
+            }
+            *p.am_counter = 0;
+            p.next_ids[0] = bi;
+            if (p.advance) {
+                p.tokens[0] = bi;
+                p.pos[0] += 1;
+            }
+        }
+    }
+}
+
+template <typename T, typename KT, int GQ>
+__global__ void __launch_bounds__(kStThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    Ring r;
+    r.base = smem;
+    r.stages = p.stages;
+    r.full = reinterpret_cast<uint64_t *>(smem + (size_t)p.stages * kStStageBytes);
+    r.empty = r.full + kStMaxStages;  // 16 + 16 barriers: 256 bytes
+    float *scratch = reinterpret_cast<float *>(smem + (size_t)p.stages * kStStageBytes + 256);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x;
+    constexpr int ES = sizeof(T);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < r.stages; ++s) {
+            mbar_init(&r.full[s], 1);
+            mbar_init(&r.empty[s], kStConsumerWarps);
+        }
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kStConsumerWarps) {
+        // ---------------- producer: every weight byte of the step, in phase order
+        if (lane == 0) produce_all<ES>(r, p);
+        return;
+    }
+
+    // ---------------- consumers
+    int phase = 0;
+    uint32_t fill = 0;
+    GridBarrier gb;
+    {
+        __shared__ unsigned long long s_epoch;
+        if (threadIdx.x == 0) {
+            unsigned long long e;
+            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(e) : "l"(reinterpret_cast<unsigned long long *>(p.bar) + 1) : "memory");
+            s_epoch = e;
+        }
+        named_sync(1, kStConsumers);
+        gb.base = s_epoch * (unsigned long long)G * (unsigned long long)(1 + 5 * p.n_layer);
+        gb.k = 0;
+    }
+    mark_phase(p, phase);
+    {   // embed: x = E[token]; every CTA copies a slice
+        int tok = __ldcg(p.tokens);
+        if (tok < 0 || tok >= p.vocab) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(p.err, DS_ERR_TOKEN_RANGE);
+            tok = min(max(tok, 0), p.vocab - 1);
+        }
+        const T *row = reinterpret_cast<const T *>(p.emb) + (long long)tok * p.d;
+        const int i0 = (int)((long long)p.d * blockIdx.x / G), i1 = (int)((long long)p.d * (blockIdx.x + 1) / G);
+        for (int i = i0 + threadIdx.x; i < i1; i += kStConsumers) p.x[i] = to_f32(row[i]);
+        // the square sum of band b of the row (the bands the residual
+        // projections use), for the first RMSNorm
+        if ((int)blockIdx.x < p.n_ss) {
+            const int bc = kStBandBytes / (int)sizeof(T);
+            const int col = blockIdx.x * bc + threadIdx.x;
+            const float v = (threadIdx.x < bc && col < p.d) ? to_f32(row[col]) : 0.0f;
+            const float ss = block_sumsq(v, scratch);
+            if (threadIdx.x == 0) p.ss[blockIdx.x] = ss;
+        }
+    }
+    grid_sync(p, G, gb);
+    // every CTA has read the epoch: advance it for the next launch
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(reinterpret_cast<unsigned long long *>(p.bar) + 1) : "memory");
+    for (int l = 0; l < p.n_layer; ++l) {
+        const StepLayer &L = p.layers[l];
+        mark_phase(p, phase);
+        consume_gt<T, ST_QKV, true>(r, fill, p.d, p.nq_cols + 2 * p.nkv_cols, p.nb_qkv, p.x, L.n1, p.q, l, scratch, p,
+                                    phase - 1);
+        prefetch_attention<KT>(l, p);
+        grid_sync(p, G, gb);
+        mark_phase(p, phase);
+        consume_attention<KT, GQ>(l, scratch, p, phase - 1);
+        grid_sync(p, G, gb);
+        mark_phase(p, phase);
+        consume_gt<T, ST_ADD, false>(r, fill, p.nq_cols, p.d, p.nb_o, p.att, nullptr, p.x, l, scratch, p, phase - 1);
+        grid_sync(p, G, gb);
+        mark_phase(p, phase);
+        consume_gt<T, ST_SILU, true>(r, fill, p.d, p.ff, p.nb_gu, p.x, L.n2, p.f, l, scratch, p, phase - 1);
+        grid_sync(p, G, gb);
+        mark_phase(p, phase);
+        consume_gt<T, ST_ADD, false>(r, fill, p.ff, p.d, p.nb_d, p.f, nullptr, p.x, l, scratch, p, phase - 1);
+        grid_sync(p, G, gb);
+    }
+    mark_phase(p, phase);
+    consume_gn<T>(r, fill, scratch, p);
+    mark_phase(p, phase);
+}
+
+// ---------------------------------------------------------------- host
+size_t step_layer_bytes() { return sizeof(StepLayer); }
+
+// Host image of one layer's step descriptor: its five tensor maps and norms.
+void step_layer_fill(void *dst, const CUtensorMap *maps5, const float *n1, const float *n2) {
+    StepLayer L;
+    std::memset(&L, 0, sizeof L);
+    for (int i = 0; i < 5; ++i) L.maps[i] = maps5[i];
+    L.n1 = n1;
+    L.n2 = n2;
+    std::memcpy(dst, &L, sizeof L);
+}
+
+int step_max_layers() { return kStMaxLayers; }
+int step_max_splits() { return kStMaxSplits; }
+
+// Shared-memory floats the consumers need after the ring, for a config.
+int step_scratch_floats(const ds_model_config *c, int grid, int nb_qkv, int nb_o, int nb_gu, int nb_d) {
+    const int es = c->w_dtype == DS_BF16 ? 2 : 4;
+    auto slice = [&](int K, int nb) {
+        const long long UB = (K + kStBoxRows - 1) / kStBoxRows;
+        return (long long)(((UB * nb + grid - 1) / grid + 1) * kStBoxRows);
+    };
+    const int nq = c->n_qh * c->head_dim;
+    long long gt = std::max(std::max(slice(c->d, nb_qkv), slice(nq, nb_o)), std::max(slice(c->d, nb_gu), slice(c->ff, nb_d)));
+    gt += kStConsumerWarps * 256 + 256 + 16;
+    const int gq = c->n_qh / c->n_kvh;
+    const long long at = std::max((long long)kStConsumerWarps * gq * c->head_dim, 2LL * kStMaxSplits * gq + 2 * gq) +
+                         2LL * kStConsumerWarps * gq + 16;
+    const long long row_bytes = (long long)c->d * es;
+    const long long rps = std::max(1LL, (long long)kStStageBytes / row_bytes);
+    const long long parts = rps >= kStConsumerWarps ? 1 : kStConsumerWarps / rps;
+    const long long rows_cap = (c->vocab + grid - 1) / grid + 1;
+    const long long gn = 512 + c->d + rows_cap * parts;
+    return (int)std::max(std::max(gt, at), gn);
+}
+
+bool step_supported(const ds_model_config *c) {
+    const int es = c->w_dtype == DS_BF16 ? 2 : 4;
+    if (c->n_layer > kStMaxLayers || c->max_seqs != 1) return false;
+    if ((long long)c->d * es > kStStageBytes) return false;
+    const int gq = c->n_qh / c->n_kvh;
+    if (gq != 1 && gq != 2 && gq != 4 && gq != 8) return false;
+    if (c->head_dim > 128) return false;
+    return true;
+}
+
+// Shared memory of the step kernel with `stages` ring stages.
+size_t step_smem_bytes(int stages, int scratch_floats) {
+    return (size_t)stages * kStStageBytes + 256 + (size_t)scratch_floats * 4 + 64;
+}
+
+// Ring stages that fit beside `scratch_floats` of scratch (0 if none).
+int step_stages(int scratch_floats) {
+    for (int s = kStMaxStages; s >= 2; --s)
+        if (step_smem_bytes(s, scratch_floats) <= kStSmemLimit) return s;
+    return 0;
+}
+
+template <typename T, typename KT, int GQ>
+static cudaError_t launch_step_t(const StepParams &p, int grid, cudaStream_t stream) {
+    const size_t smem = step_smem_bytes(p.stages, p.scratch_floats);
+    if (smem > kStSmemLimit) return cudaErrorInvalidValue;
+    cudaError_t e =
+        cudaFuncSetAttribute(step_kernel<T, KT, GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kStThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, step_kernel<T, KT, GQ>, p);
+}
+
+template <typename T, typename KT>
+static cudaError_t launch_step_g(const StepParams &p, int gq, int grid, cudaStream_t stream) {
+    switch (gq) {
+        case 1: return launch_step_t<T, KT, 1>(p, grid, stream);
+        case 2: return launch_step_t<T, KT, 2>(p, grid, stream);
+        case 4: return launch_step_t<T, KT, 4>(p, grid, stream);
+        case 8: return launch_step_t<T, KT, 8>(p, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_step(const void *params, int w_dtype, int kv_dtype, int gq, int grid, cudaStream_t stream) {
+    const StepParams &p = *static_cast<const StepParams *>(params);
+    if (w_dtype == DS_BF16)
+        return kv_dtype == DS_BF16 ? launch_step_g<__nv_bfloat16, __nv_bfloat16>(p, gq, grid, stream)
+                                   : launch_step_g<__nv_bfloat16, float>(p, gq, grid, stream);
+    return kv_dtype == DS_BF16 ? launch_step_g<float, __nv_bfloat16>(p, gq, grid, stream)
+                               : launch_step_g<float, float>(p, gq, grid, stream);
+}
+
+}  // namespace ds

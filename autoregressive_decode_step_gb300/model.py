@@ -105,10 +105,12 @@ class DecodeModel:
         s.temperature, s.top_k, s.top_p = sampling
         return ctypes.byref(s)
 
-    def step(self, n_seqs=1, sampling=None, advance=False, write_logits=True, stream=None):
+    def step(self, n_seqs=1, sampling=None, advance=False, write_logits=True, stream=None, phase_times=False,
+             trace=False):
         """One decode step of tokens[:n_seqs] at pos[:n_seqs]; ids go to
         next_ids (and logits to self.logits)."""
-        flags = abi.DS_STEP_ADVANCE if advance else 0
+        flags = ((abi.DS_STEP_ADVANCE if advance else 0) | (abi.DS_STEP_PHASE_TIMES if phase_times else 0) |
+                 (abi.DS_STEP_TRACE if trace else 0))
         abi.check(abi.lib.ds_decode_step(self._h, ctypes.byref(self._kv), abi.ptr(self.tokens), abi.ptr(self.pos),
                                          n_seqs, self._sampling(sampling), abi.ptr(self.u), abi.ptr(self.next_ids),
                                          abi.ptr(self.logits) if write_logits else None, flags,
@@ -152,6 +154,33 @@ class DecodeModel:
                                                  kinds, cap, ctypes.byref(n), abi.stream_handle(stream)),
                   "ds_decode_step_profile")
         return [(abi.KIND_NAMES[kinds[i]], ms[i]) for i in range(n.value)]
+
+    def phase_times_us(self, stream=None):
+        """Per-phase durations (µs) of the last step run with phase_times=True:
+        [("embed", t), ("qkv", t), ("attention", t), ..., ("head", t)]."""
+        n_layer = self.cfg["n_layer"]
+        cap = 5 * n_layer + 4
+        buf = (ctypes.c_uint64 * cap)()
+        n = ctypes.c_int(0)
+        abi.check(abi.lib.ds_model_phase_times(self._h, buf, cap, ctypes.byref(n), abi.stream_handle(stream)),
+                  "ds_model_phase_times")
+        names = ["embed"] + ["qkv", "attention", "o_proj", "gate_up", "down"] * n_layer + ["head"]
+        ts = [buf[i] for i in range(n.value)]
+        return [(names[i], (ts[i + 1] - ts[i]) / 1000.0) for i in range(min(len(names), len(ts) - 1))]
+
+    def trace(self, stream=None):
+        """Per-CTA timestamps of the last traced step as an int64 tensor
+        [phase, cta, 5] (see ds_model_trace)."""
+        n_layer = self.cfg["n_layer"]
+        n_phase = 5 * n_layer + 4
+        cap = n_phase * 1024 * 5
+        buf = (ctypes.c_uint64 * cap)()
+        nw = ctypes.c_size_t(0)
+        nc = ctypes.c_int(0)
+        abi.check(abi.lib.ds_model_trace(self._h, buf, cap, ctypes.byref(nw), ctypes.byref(nc),
+                                         abi.stream_handle(stream)), "ds_model_trace")
+        t = torch.tensor(list(buf[:nw.value]), dtype=torch.int64)
+        return t.reshape(-1, nc.value, 5)
 
     def kernel_time_us(self, kind, reps=4, stream=None):
         """Mean microseconds per launch of one kernel kind ("qkv", "attention",

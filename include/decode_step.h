@@ -345,7 +345,9 @@ DS_API void ds_model_destroy(ds_model *model);
 DS_API void *ds_model_workspace(ds_model *model);
 
 /* Flags of ds_decode_step. */
-#define DS_STEP_ADVANCE 1u /* after picking: tokens[s] = next_ids[s], pos[s] += 1 (on device) */
+#define DS_STEP_ADVANCE 1u     /* after picking: tokens[s] = next_ids[s], pos[s] += 1 (on device) */
+#define DS_STEP_PHASE_TIMES 2u /* record a device timestamp at every phase boundary of the step */
+#define DS_STEP_TRACE 4u       /* also record per-CTA timestamps inside every phase (see ds_model_trace) */
 
 /* One decode step for n_seqs sequences: for each sequence s, token
  * tokens[s] at position pos[s] ("The forward pass end to end", "What a
@@ -365,6 +367,22 @@ DS_API int ds_decode_step(ds_model *model, const ds_kv_cache *kv, int32_t *token
                           int n_seqs, const ds_sampling *sampling, const float *u,
                           int32_t *next_ids, float *logits_out, unsigned flags,
                           ds_stream_t stream);
+
+/* Device timestamps (ns, globaltimer) of the last step run with
+ * DS_STEP_PHASE_TIMES: [0] start, then the start of every phase in order
+ * (per layer: q|k|v, attention, o, gate|up, down), then the head, then the
+ * end — 5*n_layer + 3 values for a batch-1 step.  Copies at most cap values
+ * to ns_out (host), the count to *n_out; synchronises `stream`. */
+DS_API int ds_model_phase_times(ds_model *model, uint64_t *ns_out, int cap, int *n_out,
+                                ds_stream_t stream);
+
+/* Per-CTA timestamps (ns) of the last step run with DS_STEP_TRACE, laid out
+ * [phase][cta][5]: phase start, prologue done, last weight stage consumed,
+ * epilogue done, and the producer warp's last weight request of the phase
+ * (zero where a point does not apply).  Phases as in ds_model_phase_times.
+ * Copies at most cap_words values; *n_ctas gets the CTA count. */
+DS_API int ds_model_trace(ds_model *model, uint64_t *out, size_t cap_words, size_t *n_words,
+                          int *n_ctas, ds_stream_t stream);
 
 /* A decode step captured once as a CUDA graph and replayed ("Inside the
  * engine", section 4: the launch sequence of a step replayed as a captured
