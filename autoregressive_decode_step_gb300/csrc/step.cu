@@ -43,6 +43,10 @@ constexpr int kStMaxStages = 16;
 #endif
 constexpr int kStBoxRows = DS_ST_BOX_ROWS;
 constexpr int kStBandBytes = 512;
+#ifndef DS_ST_ATTN_MIN_PER
+#define DS_ST_ATTN_MIN_PER 64
+#endif
+constexpr int kStAttnMinPer = DS_ST_ATTN_MIN_PER;  // fewest positions per attention split
 constexpr int kStBoxesPerStage = kStStageBytes / (kStBoxRows * kStBandBytes);  // 8 boxes of 16 rows at 64 KB
 constexpr size_t kStSmemLimit = 227 * 1024;
 
@@ -362,10 +366,16 @@ __device__ float block_sumsq(float v, float *red) {
 // CTA's first and last segment can be) publishes its partial sums at once and
 // is settled after the whole range is streamed, so that waiting for the other
 // CTAs never stalls the stream.
-template <typename T, int EPI, bool NORM>
+enum { SRC_PLAIN = 0, SRC_NORM = 1, SRC_ATTN = 2 };
+
+template <int GQ>
+__device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, const StepParams &p);
+
+template <typename T, int EPI, int SRC, int GQ>
 __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, int n_bands, const float *xin,
                            const float *norm_w, float *y, int layer, float *scratch, const StepParams &p,
                            int phase) {
+    constexpr bool NORM = SRC == SRC_NORM;
     constexpr int ES = sizeof(T);
     constexpr int LE = 16 / ES;
     constexpr int BAND_COLS = kStBandBytes / ES;
@@ -388,7 +398,20 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
     if (!in) return;
 
     const float scale = NORM ? scale_from_ss(p, K, red) : 1.0f;
-    {   // this CTA's slice of x (normalised; zero past K), four floats per
+    if (SRC == SRC_ATTN) {  // the slice of the attention output, merged here
+        int off = 0;
+        for (long long u = u0; u < u1;) {
+            const int band = (int)(u / UB);
+            const int j0 = (int)(u - (long long)band * UB);
+            const int j1 = (int)min((long long)UB, j0 + (u1 - u));
+            u += j1 - j0;
+            const int k0 = j0 * kStBoxRows, k1 = j1 * kStBoxRows;
+            stage_attention_rows<GQ>(k0, min(k1, K), xs + off, red, p);
+            for (int k = K + t; k < k1; k += kStConsumers) xs[off + k - k0] = 0.0f;
+            off += k1 - k0;
+        }
+        named_sync(1, kStConsumers);
+    } else {   // this CTA's slice of x (normalised; zero past K), four floats per
         // thread per pass with every pass's loads issued together
         int off = 0;
         for (long long u = u0; u < u1;) {
@@ -591,7 +614,7 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
         float v0 = 0.0f, v1 = 0.0f;
         if (t < BAND_COLS) {
             const int nmax = max(last0 ? pend_n[0] : 0, last1 ? pend_n[1] : 0);
-#pragma unroll 4
+#pragma unroll 16
             for (int c = 0; c < nmax; ++c) {
                 if (last0 && c < pend_n[0])
                     v0 += ldcg(&p.partials[(size_t)(pend_first[0] + c + pend_band[0]) * BAND_COLS + t]);
@@ -638,7 +661,7 @@ __device__ void prefetch_attention(int layer, const StepParams &p) {
     const int g = blockIdx.x / p.attn_splits, split = blockIdx.x % p.attn_splits;
     const int cap = p.max_blocks * p.block_tokens;
     const int n_ctx = min(max(__ldcg(p.pos), 0), cap - 1);  // positions before pos
-    const int per = max(64, (n_ctx + 1 + p.attn_splits - 1) / p.attn_splits);
+    const int per = max(kStAttnMinPer, (n_ctx + 1 + p.attn_splits - 1) / p.attn_splits);
     const int t0 = min(n_ctx, split * per), t1 = min(n_ctx, t0 + per);
     const int row_bytes = p.hd * (int)sizeof(KT);  // one head's row
     const int lines = (row_bytes + 127) / 128;
@@ -655,9 +678,11 @@ __device__ void prefetch_attention(int layer, const StepParams &p) {
 }
 
 // One CTA's share of the attention phase: item (kv head g, split) = this CTA
-// (CTAs past the items idle); eight warps take runs of eight positions with an
-// online softmax; warps merge in shared memory; the last CTA of a head merges
-// the splits in split order.
+// (CTAs past the items idle).  Eight warps take runs of eight positions with
+// an online softmax, merged across warps in shared memory; the CTA publishes
+// its split's (max, sum, accumulator) and is done.  The splits of a head are
+// merged, in split order, by whoever reads the attention output next (the o
+// projection's prologue), so no CTA waits on another here.
 template <typename KT, int GQ>
 __device__ void consume_attention(int layer, float *scratch, const StepParams &p, int phase) {
     constexpr int RUN = 8;
@@ -670,13 +695,13 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
     float *s_acc = scratch;                                   // [8][GQ][hd]
     float *s_m = s_acc + kStConsumerWarps * GQ * hd;          // [8][GQ]
     float *s_l = s_m + kStConsumerWarps * GQ;                 // [8][GQ]
-    volatile int *s_flag = reinterpret_cast<volatile int *>(s_l + kStConsumerWarps * GQ);
 
     const int cap = p.max_blocks * p.block_tokens;
     int n_ctx = __ldcg(p.pos) + 1;
     n_ctx = min(max(n_ctx, 1), cap);
-    const int per = max(64, (n_ctx + p.attn_splits - 1) / p.attn_splits);
+    const int per = max(kStAttnMinPer, (n_ctx + p.attn_splits - 1) / p.attn_splits);
     const int n_eff = (n_ctx + per - 1) / per;
+    if (split >= n_eff) return;
     const int t0 = min(n_ctx, split * per), t1 = min(n_ctx, t0 + per);
     const bool active = lane * 4 < hd;
     const int d0 = lane * 4;
@@ -684,6 +709,24 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
     const KT *kc = static_cast<const KT *>(p.kc[layer]);
     const KT *vc = static_cast<const KT *>(p.vc[layer]);
 
+    float kf[RUN][4], vf[RUN][4];
+    auto load_run = [&](int tb) {
+        const int nt = min(RUN, t1 - tb);
+#pragma unroll
+        for (int i = 0; i < RUN; ++i) {
+            const bool ok = active && i < nt;
+            long long off = 0;
+            if (ok) {
+                const int tt = tb + i, b = tt / p.block_tokens;
+                const long long blk = p.block_table ? (long long)__ldcg(p.block_table + b) : (long long)b;
+                off = (blk * p.block_tokens + tt % p.block_tokens) * row_elems + (long long)g * hd + d0;
+            }
+            load4<KT>(kc, off, ok, kf[i]);
+            load4<KT>(vc, off, ok, vf[i]);
+        }
+    };
+    int tb = t0 + warp * RUN;
+    if (tb < t1) load_run(tb);  // K/V requests go out before q's
     float q[GQ][4];
 #pragma unroll
     for (int j = 0; j < GQ; ++j)
@@ -698,21 +741,8 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
     }
-    for (int tb = t0 + warp * RUN; tb < t1; tb += kStConsumerWarps * RUN) {
+    while (tb < t1) {
         const int nt = min(RUN, t1 - tb);
-        float kf[RUN][4], vf[RUN][4];
-#pragma unroll
-        for (int i = 0; i < RUN; ++i) {
-            const bool ok = active && i < nt;
-            long long off = 0;
-            if (ok) {
-                const int tt = tb + i, b = tt / p.block_tokens;
-                const long long blk = p.block_table ? (long long)__ldcg(p.block_table + b) : (long long)b;
-                off = (blk * p.block_tokens + tt % p.block_tokens) * row_elems + (long long)g * hd + d0;
-            }
-            load4<KT>(kc, off, ok, kf[i]);
-            load4<KT>(vc, off, ok, vf[i]);
-        }
 #pragma unroll
         for (int j = 0; j < GQ; ++j) {
             float sc[RUN];
@@ -741,6 +771,8 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
                 }
             m[j] = mx;
         }
+        tb += kStConsumerWarps * RUN;
+        if (tb < t1) load_run(tb);
     }
 #pragma unroll
     for (int j = 0; j < GQ; ++j) {
@@ -757,7 +789,7 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
 
     const int rec = GQ * (hd + 2);
     float *part = p.a_partials + (size_t)(g * p.attn_splits + split) * rec;
-    for (int idx = t; split < n_eff && idx < GQ * hd; idx += kStConsumers) {
+    for (int idx = t; idx < GQ * hd; idx += kStConsumers) {
         const int j = idx / hd;
         float M = -INFINITY;
         for (int w = 0; w < kStConsumerWarps; ++w) M = fmaxf(M, s_m[w * GQ + j]);
@@ -774,62 +806,56 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
             part[GQ + j] = L;
         }
     }
-    named_sync(1, kStConsumers);
-    if (t == 0) {
-        int prev;
-        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev) : "l"(&p.a_counters[g]) : "memory");
-        const bool last = prev == p.attn_splits - 1;
-        if (last) p.a_counters[g] = 0;
-        *s_flag = last;
-    }
-    named_sync(1, kStConsumers);
-    const bool last = *s_flag != 0;
-    named_sync(1, kStConsumers);
-    trace_point(p, phase, 1);
-    if (!last) return;
-
-    const float *base = p.a_partials + (size_t)g * p.attn_splits * rec;
-    float *sm = s_acc;                       // reuse: [n_eff][GQ] weights
-    float *sl = s_acc + kStMaxSplits * GQ;   // [n_eff][GQ]
-    float *sM = sl + kStMaxSplits * GQ;      // [2][GQ]
-    for (int i = t; i < n_eff * GQ; i += kStConsumers) {
-        const int sp = i / GQ, j = i % GQ;
-        sm[i] = ldcg(base + (size_t)sp * rec + j);
-        sl[i] = ldcg(base + (size_t)sp * rec + GQ + j);
-    }
-    named_sync(1, kStConsumers);
-    if (t < GQ) {
-        float M = -INFINITY;
-        for (int sp = 0; sp < n_eff; ++sp) M = fmaxf(M, sm[sp * GQ + t]);
-        sM[t] = M;
-    }
-    named_sync(1, kStConsumers);
-    for (int i = t; i < n_eff * GQ; i += kStConsumers) {
-        const float ms = sm[i];
-        sm[i] = ms == -INFINITY ? 0.0f : expf(ms - sM[i % GQ]);
-    }
-    named_sync(1, kStConsumers);
-    if (t < GQ) {
-        float L = 0.0f;
-        for (int sp = 0; sp < n_eff; ++sp) L = fmaf(sl[sp * GQ + t], sm[sp * GQ + t], L);
-        sM[GQ + t] = L;
-    }
-    named_sync(1, kStConsumers);
-    for (int idx = t; idx < GQ * hd; idx += 2 * kStConsumers) {
-        const int idx2 = idx + kStConsumers;
-        const bool two = idx2 < GQ * hd;
-        const int j = idx / hd, j2 = two ? idx2 / hd : j;
-        float A = 0.0f, A2 = 0.0f;
-#pragma unroll 8
-        for (int sp = 0; sp < n_eff; ++sp) {
-            const float *rp = base + (size_t)sp * rec + 2 * GQ;
-            A = fmaf(ldcg(rp + idx), sm[sp * GQ + j], A);
-            if (two) A2 = fmaf(ldcg(rp + idx2), sm[sp * GQ + j2], A2);
-        }
-        p.att[(g * GQ + j) * hd + idx % hd] = A / sM[GQ + j];
-        if (two) p.att[(g * GQ + j2) * hd + idx2 % hd] = A2 / sM[GQ + j2];
-    }
     trace_point(p, phase, 3);
+}
+
+// Attention output rows [k0, k1) (k indexes query head h = k / hd, dim
+// k % hd), merged from the published splits of their KV heads in split order:
+// out = sum_s w_s acc_s / sum_s w_s l_s with w_s = exp(m_s - max m), written
+// to xs.  `red` holds the per-head weights.
+template <int GQ>
+__device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, const StepParams &p) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int hd = p.hd;
+    const int cap = p.max_blocks * p.block_tokens;
+    const int n_ctx = min(max(__ldcg(p.pos) + 1, 1), cap);
+    const int per = max(kStAttnMinPer, (n_ctx + p.attn_splits - 1) / p.attn_splits);
+    const int n_eff = (n_ctx + per - 1) / per;
+    const int rec = GQ * (hd + 2);
+    const int h_lo = k0 / hd, h_hi = (k1 - 1) / hd;
+    const int nh = h_hi - h_lo + 1;
+    float *wt = red;                      // [nh][kStMaxSplits]
+    float *Lh = red + nh * kStMaxSplits;  // [nh]
+    for (int hl = warp; hl < nh; hl += kStConsumerWarps) {
+        const int h = h_lo + hl, g = h / GQ, j = h % GQ;
+        const float *base = p.a_partials + (size_t)g * p.attn_splits * rec;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+        if (lane < n_eff) {
+            m0 = ldcg(base + (size_t)lane * rec + j);
+            l0 = ldcg(base + (size_t)lane * rec + GQ + j);
+        }
+        if (lane + 32 < n_eff) {
+            m1 = ldcg(base + (size_t)(lane + 32) * rec + j);
+            l1 = ldcg(base + (size_t)(lane + 32) * rec + GQ + j);
+        }
+        const float M = warp_max(fmaxf(m0, m1));
+        const float w0 = (lane < n_eff && m0 != -INFINITY) ? expf(m0 - M) : 0.0f;
+        const float w1 = (lane + 32 < n_eff && m1 != -INFINITY) ? expf(m1 - M) : 0.0f;
+        wt[hl * kStMaxSplits + lane] = w0;
+        wt[hl * kStMaxSplits + lane + 32] = w1;
+        const float L = warp_sum(fmaf(w1, l1, w0 * l0));
+        if (lane == 0) Lh[hl] = L;
+    }
+    named_sync(1, kStConsumers);
+    for (int k = k0 + t; k < k1; k += kStConsumers) {
+        const int h = k / hd, g = h / GQ, j = h % GQ, hl = h - h_lo;
+        const float *rp = p.a_partials + (size_t)g * p.attn_splits * rec + 2 * GQ + j * hd + k % hd;
+        float A = 0.0f;
+#pragma unroll 16
+        for (int sp = 0; sp < n_eff; ++sp) A = fmaf(ldcg(rp + (size_t)sp * rec), wt[hl * kStMaxSplits + sp], A);
+        xs[k - k0] = A / Lh[hl];
+    }
+    named_sync(1, kStConsumers);
 }
 
 // The head phase: logits of this CTA's rows, then the greedy pick.
@@ -1016,7 +1042,7 @@ __global__ void __launch_bounds__(kStThreads, 1) step_kernel(const __grid_consta
     for (int l = 0; l < p.n_layer; ++l) {
         const StepLayer &L = p.layers[l];
         mark_phase(p, phase);
-        consume_gt<T, ST_QKV, true>(r, fill, p.d, p.nq_cols + 2 * p.nkv_cols, p.nb_qkv, p.x, L.n1, p.q, l, scratch, p,
+        consume_gt<T, ST_QKV, SRC_NORM, GQ>(r, fill, p.d, p.nq_cols + 2 * p.nkv_cols, p.nb_qkv, p.x, L.n1, p.q, l, scratch, p,
                                     phase - 1);
         prefetch_attention<KT>(l, p);
         grid_sync(p, G, gb);
@@ -1024,13 +1050,14 @@ __global__ void __launch_bounds__(kStThreads, 1) step_kernel(const __grid_consta
         consume_attention<KT, GQ>(l, scratch, p, phase - 1);
         grid_sync(p, G, gb);
         mark_phase(p, phase);
-        consume_gt<T, ST_ADD, false>(r, fill, p.nq_cols, p.d, p.nb_o, p.att, nullptr, p.x, l, scratch, p, phase - 1);
+        consume_gt<T, ST_ADD, SRC_ATTN, GQ>(r, fill, p.nq_cols, p.d, p.nb_o, nullptr, nullptr, p.x, l, scratch, p,
+                                            phase - 1);
         grid_sync(p, G, gb);
         mark_phase(p, phase);
-        consume_gt<T, ST_SILU, true>(r, fill, p.d, p.ff, p.nb_gu, p.x, L.n2, p.f, l, scratch, p, phase - 1);
+        consume_gt<T, ST_SILU, SRC_NORM, GQ>(r, fill, p.d, p.ff, p.nb_gu, p.x, L.n2, p.f, l, scratch, p, phase - 1);
         grid_sync(p, G, gb);
         mark_phase(p, phase);
-        consume_gt<T, ST_ADD, false>(r, fill, p.ff, p.d, p.nb_d, p.f, nullptr, p.x, l, scratch, p, phase - 1);
+        consume_gt<T, ST_ADD, SRC_PLAIN, GQ>(r, fill, p.ff, p.d, p.nb_d, p.f, nullptr, p.x, l, scratch, p, phase - 1);
         grid_sync(p, G, gb);
     }
     mark_phase(p, phase);
