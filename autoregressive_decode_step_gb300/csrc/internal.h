@@ -210,17 +210,20 @@ struct StepParams {
     int *tokens, *pos, *next_ids;
     float *logits;
     int advance, greedy;
-    float *x, *q, *att, *f;
-    float *partials;
-    int *counters;
-    float *ss;              // per-band square sums of the residual (n_ss bands)
+    // activations handed between CTAs, as tagged 64-bit words (value, phase tag)
+    unsigned long long *xt;   // residual [d]
+    unsigned long long *qt;   // rotated q [n_qh * hd]
+    unsigned long long *kvt;  // this position's k then v [2 * n_kvh * hd], as the cache holds them
+    unsigned long long *ft;   // SiLU(gate) * up [ff]
+    unsigned long long *sst;  // per-band square sums of the residual [n_ss]
     int n_ss;
-    float *a_partials;
-    int *a_counters;
+    unsigned long long *pt;   // projection partials: 4 buffers (one per kind) of pt_stride words
+    size_t pt_stride;
+    unsigned long long *at;   // attention split records [n_kvh][attn_splits][GQ * (hd + 2)]
     float *am_val;
     int *am_idx;
     int *am_counter;
-    unsigned *bar;          // u64 arrival count, then u64 epoch (see grid_sync)
+    unsigned long long *epoch;  // launches completed (tags derive from it)
     int *err;
     int *abort_flag;
     unsigned long long *phase_times;  // optional: globaltimer at every phase start, then at the end

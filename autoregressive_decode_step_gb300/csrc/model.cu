@@ -58,7 +58,9 @@ struct ds_model {
     int n_phase_times;
     unsigned long long *trace;
     size_t trace_words;
-    float *ss;
+    // tagged activation words and partials of the step kernel
+    unsigned long long *st_x, *st_q, *st_kv, *st_f, *st_ss, *st_part, *st_att;
+    size_t st_part_stride;
 };
 
 struct ds_step_graph {
@@ -72,7 +74,9 @@ using namespace ds;
 
 struct Layout {
     size_t x, q, att, f, logits, rope_cos, rope_sin, g_counters, g_partials, a_counters, a_partials, am_val,
-        am_idx, am_counter, step_layers, step_bar, phase_times, trace, ss, total;
+        am_idx, am_counter, step_layers, step_bar, phase_times, trace, st_x, st_q, st_kv, st_f, st_ss, st_part,
+        st_att, total;
+    size_t st_part_stride;
     int grid_qkv, grid_o, grid_gu, grid_d, grid_head, nb_qkv, nb_o, nb_gu, nb_d, attn_splits;
     bool step_ok;
     int step_grid, step_splits, step_stages, step_scratch, n_phase_times;
@@ -164,7 +168,18 @@ Layout make_layout(const ds_model_config *c) {
     L.step_bar = carve(off, 32);  // arrival count (u64), epoch (u64), abort flag
     L.phase_times = carve(off, (size_t)L.n_phase_times * 8);
     L.trace = carve(off, (size_t)L.n_phase_times * L.step_grid * 5 * 8);
-    L.ss = carve(off, (size_t)(L.nb_o + 1) * 4);
+    if (L.step_ok) {
+        const int gq = c->n_qh / c->n_kvh;
+        L.st_x = carve(off, (size_t)c->d * 8);
+        L.st_q = carve(off, (size_t)nq * 8);
+        L.st_kv = carve(off, (size_t)2 * nkv * 8);
+        L.st_f = carve(off, (size_t)c->ff * 8);
+        L.st_ss = carve(off, (size_t)L.nb_o * 8);
+        // partial slot = CTA + band, one buffer per projection kind
+        L.st_part_stride = (size_t)(L.step_grid + max_bands) * bc;
+        L.st_part = carve(off, 4 * L.st_part_stride * 8);
+        L.st_att = carve(off, (size_t)c->n_kvh * L.step_splits * gq * (c->head_dim + 2) * 8);
+    }
     L.total = off;
     return L;
 }
@@ -509,7 +524,14 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
     m->n_phase_times = L.n_phase_times;
     m->trace = reinterpret_cast<unsigned long long *>(ws + L.trace);
     m->trace_words = (size_t)L.n_phase_times * L.step_grid * 5;
-    m->ss = reinterpret_cast<float *>(ws + L.ss);
+    m->st_x = reinterpret_cast<unsigned long long *>(ws + L.st_x);
+    m->st_q = reinterpret_cast<unsigned long long *>(ws + L.st_q);
+    m->st_kv = reinterpret_cast<unsigned long long *>(ws + L.st_kv);
+    m->st_f = reinterpret_cast<unsigned long long *>(ws + L.st_f);
+    m->st_ss = reinterpret_cast<unsigned long long *>(ws + L.st_ss);
+    m->st_part = reinterpret_cast<unsigned long long *>(ws + L.st_part);
+    m->st_att = reinterpret_cast<unsigned long long *>(ws + L.st_att);
+    m->st_part_stride = L.st_part_stride;
 
     std::vector<unsigned char> layer_img((size_t)std::max(cfg->n_layer, 1) * step_layer_bytes(), 0);
     for (int l = 0; l < cfg->n_layer; ++l)
@@ -568,20 +590,19 @@ int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t 
     p.logits = logits;
     p.advance = advance && greedy;
     p.greedy = greedy;
-    p.x = m->x;
-    p.q = m->q;
-    p.att = m->att;
-    p.f = m->f;
-    p.partials = m->g_partials;
-    p.counters = m->g_counters;
-    p.ss = m->ss;
+    p.xt = m->st_x;
+    p.qt = m->st_q;
+    p.kvt = m->st_kv;
+    p.ft = m->st_f;
+    p.sst = m->st_ss;
     p.n_ss = m->nb_o;
-    p.a_partials = m->a_partials;
-    p.a_counters = m->a_counters;
+    p.pt = m->st_part;
+    p.pt_stride = m->st_part_stride;
+    p.at = m->st_att;
     p.am_val = m->am_val;
     p.am_idx = m->am_idx;
     p.am_counter = m->am_counter;
-    p.bar = m->step_bar;
+    p.epoch = reinterpret_cast<unsigned long long *>(m->step_bar) + 1;
     p.err = m->err;
     p.abort_flag = m->step_abort;
     p.phase_times = (flags & (DS_STEP_PHASE_TIMES | DS_STEP_TRACE)) ? m->phase_times : nullptr;

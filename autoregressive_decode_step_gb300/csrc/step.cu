@@ -77,43 +77,6 @@ __device__ __forceinline__ bool st_wait(uint64_t *bar, uint32_t parity, const St
     }
 }
 
-// Grid barrier among the consumer warps of every CTA (the producer warps
-// never take part).  p.bar[0] is a 64-bit arrival count that only grows; a
-// launch's k-th barrier completes when the count reaches
-// base + (k + 1) * G, base = epoch * G * barriers-per-step, where the epoch
-// (p.bar[1]) is read by every CTA at its start and advanced once per launch
-// after the first barrier.  Arrivals are fire-and-forget release reductions,
-// so 152 arrivals do not queue behind one another.  Bounded; on time-out the
-// step is aborted and later barriers return at once.
-struct GridBarrier {
-    unsigned long long base;
-    int k;
-};
-
-__device__ void grid_sync(const StepParams &p, int G, GridBarrier &b) {
-    named_sync(1, kStConsumers);
-    const unsigned long long target = b.base + (unsigned long long)(b.k + 1) * (unsigned long long)G;
-    ++b.k;
-    if (threadIdx.x == 0 && !aborted(p)) {
-        unsigned long long *count = reinterpret_cast<unsigned long long *>(p.bar);
-        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(count) : "memory");
-        const uint64_t t0 = global_timer_ns();
-        for (uint32_t it = 0;; ++it) {
-            unsigned long long c;
-            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(c) : "l"(count) : "memory");
-            if (c >= target) break;
-            if ((it & 63u) == 63u) {
-                if (aborted(p)) break;
-                if (global_timer_ns() - t0 > kWaitLimitNs) {
-                    raise_abort(p, DS_ERR_WAIT_TIMEOUT);
-                    break;
-                }
-            }
-        }
-    }
-    named_sync(1, kStConsumers);
-}
-
 __device__ __forceinline__ void mark_phase(const StepParams &p, int &phase) {
     if (p.phase_times && blockIdx.x == 0 && threadIdx.x == 0) p.phase_times[phase] = global_timer_ns();
     ++phase;
@@ -294,51 +257,96 @@ __device__ void produce_all(const Ring &r, const StepParams &p) {
         if (!st_wait(&r.full[f % r.stages], (f / r.stages) & 1, p)) break;
 }
 
+// ---------------------------------------------------------------- tagged words
+// Every activation one CTA hands to another within a step travels as one
+// 64-bit word: the fp32 value in the low half and, in the high half, the
+// sequence number of the phase that wrote it.  A reader polls the word until
+// the tag it expects appears, so readiness arrives with the data: no flag, no
+// fence, no counter and no grid barrier between phases.  Tags are
+// seq(id) = (epoch mod 2^22) * 1024 + id + 1 for phase id `id` of the launch
+// numbered `epoch`.  Every tagged word is rewritten in every launch, so a
+// stale word carries an earlier phase's tag or the previous launch's, never
+// the one its reader waits for.
+using u64 = unsigned long long;
+
+struct Seq {
+    uint32_t base;
+    __device__ __forceinline__ uint32_t operator()(int id) const { return base + (uint32_t)id + 1u; }
+};
+// phase ids: 0 embed; layer l: 1+5l q|k|v, 2+5l attention, 3+5l o, 4+5l gate|up,
+// 5+5l down; 1+5L the head.  The residual layer l reads was written by phase 5l.
+__device__ __forceinline__ int ph_qkv(int l) { return 1 + 5 * l; }
+
+__device__ __forceinline__ u64 tag_pack(float v, uint32_t tag) {
+    return ((u64)tag << 32) | (u64)__float_as_uint(v);
+}
+__device__ __forceinline__ void st_tag(u64 *a, float v, uint32_t tag) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(tag_pack(v, tag)) : "memory");
+}
+__device__ __forceinline__ u64 ld_tag(const u64 *a) {
+    u64 v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+    return v;
+}
+// Poll `a` until it carries `tag` (bounded; gives up once the step is aborted).
+__device__ __forceinline__ u64 tag_wait_slow(const u64 *a, uint32_t tag, const StepParams &p) {
+    if (aborted(p)) return 0;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        const u64 v = ld_tag(a);
+        if ((uint32_t)(v >> 32) == tag) return v;
+        if ((it & 31u) == 0) {
+            if (aborted(p)) return 0;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                raise_abort(p, DS_ERR_WAIT_TIMEOUT);
+                return 0;
+            }
+        }
+    }
+}
+// The value of word `v` already loaded from `a`, polling if it lacked `tag`.
+__device__ __forceinline__ float tag_value(u64 v, const u64 *a, uint32_t tag, const StepParams &p) {
+    if ((uint32_t)(v >> 32) != tag) v = tag_wait_slow(a, tag, p);
+    return __uint_as_float((uint32_t)v);
+}
+__device__ __forceinline__ float ld_wait(const u64 *a, uint32_t tag, const StepParams &p) {
+    return tag_value(ld_tag(a), a, tag, p);
+}
+// Words w[0..n) loaded from base[i * stride]: poll the ones that lacked `tag`
+// (addresses are recomputed only on that rare path).
+template <int N>
+__device__ __forceinline__ void tag_fix(u64 (&w)[N], const u64 *base, size_t stride, int n, uint32_t tag,
+                                        const StepParams &p) {
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (i < n) ok = ok && (uint32_t)(w[i] >> 32) == tag;
+    if (!ok) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (i < n && (uint32_t)(w[i] >> 32) != tag) w[i] = tag_wait_slow(base + (size_t)i * stride, tag, p);
+    }
+}
+__device__ __forceinline__ float tag_f(u64 w) { return __uint_as_float((uint32_t)w); }
+
+// Values of the launch every consumer thread keeps: the position and the tag base.
+struct StepCtx {
+    Seq seq;
+    int pos;     // the position this step writes and attends up to
+    bool pos_ok;
+    int n_ctx;   // positions attended: pos + 1, clamped to the cache
+};
+
 // ---------------------------------------------------------------- consumers
 __device__ __forceinline__ float silu_st(float z) { return z / (1.0f + expf(-z)); }
 
-__device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
-
-// RMS scale of v[0..n) (square sum in fp32, fixed order), read through L2;
-// n a multiple of 4.  Each thread's loads are issued together.
-__device__ float rms_scale(const float *v, int n, float eps, float *red) {
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    float ss = 0.0f;
-    for (int base = 0; base < n; base += 4 * 4 * kStConsumers) {
-        float4 r[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = base + (q * kStConsumers + t) * 4;
-            r[q] = i < n ? ldcg4(v + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            ss = fmaf(r[q].x, r[q].x, ss);
-            ss = fmaf(r[q].y, r[q].y, ss);
-            ss = fmaf(r[q].z, r[q].z, ss);
-            ss = fmaf(r[q].w, r[q].w, ss);
-        }
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    named_sync(1, kStConsumers);
-    float tot = 0.0f;
-    for (int w = 0; w < kStConsumerWarps; ++w) tot += red[w];
-    named_sync(1, kStConsumers);
-    return 1.0f / sqrtf(tot / (float)n + eps);
-}
-
-enum { ST_STORE = 0, ST_ADD = 1, ST_SILU = 2, ST_QKV = 3 };
-
-// One transposed projection phase: this CTA's boxes from the ring, the
-// cross-CTA reduction, and the fused epilogue.
-// RMS scale of the residual from its per-band square sums p.ss[0..n_ss)
-// (written by whichever phase last wrote the residual), summed in band order.
-__device__ float scale_from_ss(const StepParams &p, int n, float *red) {
+// RMS scale 1/sqrt(mean(r^2) + eps) of the residual whose per-band square sums
+// (tagged `tag`) are p.sst[0..n_ss), summed in lane order then across lanes.
+__device__ float scale_from_sst(const StepParams &p, int n, uint32_t tag, float *red) {
     const int t = threadIdx.x;
-    float v = 0.0f;
     if (t < 32) {
-        for (int b = t; b < p.n_ss; b += 32) v += ldcg(p.ss + b);  // lane-order partials
+        float v = 0.0f;
+        for (int b = t; b < p.n_ss; b += 32) v += ld_wait(p.sst + b, tag, p);
         v = warp_sum(v);
         if (t == 0) red[0] = v;
     }
@@ -360,21 +368,28 @@ __device__ float block_sumsq(float v, float *red) {
     return tot;
 }
 
-// One transposed projection phase: this CTA's boxes from the ring, the
-// cross-CTA reduction, and the fused epilogue.  Bands this CTA covers whole
-// finish as soon as they are streamed; a band shared with other CTAs (only a
-// CTA's first and last segment can be) publishes its partial sums at once and
-// is settled after the whole range is streamed, so that waiting for the other
-// CTAs never stalls the stream.
+enum { ST_STORE = 0, ST_ADD = 1, ST_SILU = 2, ST_QKV = 3 };
 enum { SRC_PLAIN = 0, SRC_NORM = 1, SRC_ATTN = 2 };
 
 template <int GQ>
-__device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, const StepParams &p);
+__device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, uint32_t tag, const StepCtx &cx,
+                                     const StepParams &p);
 
+// One transposed projection phase (id `pid`): this CTA's stream-K range of
+// boxes from the ring, the cross-CTA reduction and the fused epilogue.
+//  - The input slice this range needs is polled from the tagged input (or
+//    merged from the attention splits) and kept in shared memory; an
+//    RMSNorm's weight is applied there and its 1/rms scale, a scalar, in the
+//    epilogue, so a phase never waits for the whole previous output.
+//  - A band this CTA covers whole is finished as soon as it is streamed.  A
+//    band shared by several CTAs is settled by the CTA holding its last box:
+//    the others store their column sums as tagged partials and move on; the
+//    settler, after its own range, polls those partials, adds them in CTA
+//    order with its own, and runs the epilogue.
 template <typename T, int EPI, int SRC, int GQ>
-__device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, int n_bands, const float *xin,
-                           const float *norm_w, float *y, int layer, float *scratch, const StepParams &p,
-                           int phase) {
+__device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, int n_bands, const u64 *xin,
+                           uint32_t in_tag, const float *norm_w, u64 *y, uint32_t yold_tag, int layer, int pid,
+                           const StepCtx &cx, float *scratch, const StepParams &p, int phase) {
     constexpr bool NORM = SRC == SRC_NORM;
     constexpr int ES = sizeof(T);
     constexpr int LE = 16 / ES;
@@ -384,7 +399,6 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
     constexpr int SUB_ROW_BYTES = SUB_BAND_COLS * ES;
     float *red = scratch;                  // [8][256]
     float *vals = red + kStConsumerWarps * 256;
-    volatile int *s_flag = reinterpret_cast<volatile int *>(vals + 256);  // [2]
     float *xs = vals + 256 + 16;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int UB = (K + kStBoxRows - 1) / kStBoxRows;
@@ -394,10 +408,14 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
     const int G = (int)min((long long)gridDim.x, W);
     const bool in = (int)blockIdx.x < G;
     const long long u0 = in ? W * blockIdx.x / G : 0, u1 = in ? W * (blockIdx.x + 1) / G : 0;
+    const uint32_t out_tag = cx.seq(pid);
+    // one partial buffer per projection kind: the same kind of the next layer
+    // cannot start writing before every settlement of this one has read it
+    const int kind = (pid - 1) % 5;  // 0 q|k|v, 2 o, 3 gate|up, 4 down
+    u64 *part = p.pt + (size_t)(kind == 0 ? 0 : kind - 1) * p.pt_stride;
     trace_point(p, phase, 0);
     if (!in) return;
 
-    const float scale = NORM ? scale_from_ss(p, K, red) : 1.0f;
     if (SRC == SRC_ATTN) {  // the slice of the attention output, merged here
         int off = 0;
         for (long long u = u0; u < u1;) {
@@ -406,13 +424,12 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
             const int j1 = (int)min((long long)UB, j0 + (u1 - u));
             u += j1 - j0;
             const int k0 = j0 * kStBoxRows, k1 = j1 * kStBoxRows;
-            stage_attention_rows<GQ>(k0, min(k1, K), xs + off, red, p);
+            stage_attention_rows<GQ>(k0, min(k1, K), xs + off, red, in_tag, cx, p);
             for (int k = K + t; k < k1; k += kStConsumers) xs[off + k - k0] = 0.0f;
             off += k1 - k0;
         }
         named_sync(1, kStConsumers);
-    } else {   // this CTA's slice of x (normalised; zero past K), four floats per
-        // thread per pass with every pass's loads issued together
+    } else {  // this CTA's slice of the input (times the norm weight; zero past K)
         int off = 0;
         for (long long u = u0; u < u1;) {
             const int band = (int)(u / UB);
@@ -420,27 +437,23 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
             const int j1 = (int)min((long long)UB, j0 + (u1 - u));
             u += j1 - j0;
             const int k0 = j0 * kStBoxRows, k1 = j1 * kStBoxRows;
-            for (int kb = k0; kb < k1; kb += 4 * 4 * kStConsumers) {
-                float4 v[4], w[4];
+            for (int kb = k0; kb < k1; kb += 8 * kStConsumers) {
+                u64 v[8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int k = kb + (q * kStConsumers + t) * 4;
-                    const bool ok = k < k1 && k < K;
-                    v[q] = ok ? ldcg4(xin + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    w[q] = (NORM && ok) ? *reinterpret_cast<const float4 *>(norm_w + k) : make_float4(1.f, 1.f, 1.f, 1.f);
+                for (int q = 0; q < 8; ++q) {
+                    const int k = kb + q * kStConsumers + t;
+                    v[q] = (k < k1 && k < K) ? ld_tag(xin + k) : 0ull;
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int k = kb + (q * kStConsumers + t) * 4;
+                for (int q = 0; q < 8; ++q) {
+                    const int k = kb + q * kStConsumers + t;
                     if (k < k1) {
-                        float4 o = v[q];
-                        if (NORM) {
-                            o.x = o.x * scale * w[q].x;
-                            o.y = o.y * scale * w[q].y;
-                            o.z = o.z * scale * w[q].z;
-                            o.w = o.w * scale * w[q].w;
+                        float o = 0.0f;
+                        if (k < K) {
+                            o = tag_value(v[q], xin + k, in_tag, p);
+                            if (NORM) o *= __ldg(norm_w + k);
                         }
-                        *reinterpret_cast<float4 *>(xs + off + k - k0) = o;
+                        xs[off + k - k0] = o;
                     }
                 }
             }
@@ -450,36 +463,38 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
     }
     trace_point(p, phase, 1);
 
+    float scale = 1.0f;
+    bool have_scale = !NORM;
     // the fused epilogue of one band whose column sums v (thread t < BAND_COLS)
-    // are final; y_old is the residual value already loaded (ST_ADD) or NAN
-    auto epilogue = [&](int band, float v, float y_old) {
+    // are final; yw is the residual word already loaded (ST_ADD)
+    auto epilogue = [&](int band, float v, u64 yw) {
+        if (NORM && !have_scale) {
+            scale = scale_from_sst(p, K, in_tag, red);
+            have_scale = true;
+        }
         if (EPI == ST_STORE || EPI == ST_ADD) {
             const int col = band * BAND_COLS + t;
             const bool ok = t < BAND_COLS && col < sub_cols;
-            float out = v;
-            if (EPI == ST_ADD) out = ok ? (y_old == y_old ? y_old : ldcg(y + col)) + v : 0.0f;
-            if (ok) y[col] = out;
+            float out = v * scale;
+            if (EPI == ST_ADD && ok) out += tag_value(yw, y + col, yold_tag, p);
+            if (ok) st_tag(y + col, out, out_tag);
             if (EPI == ST_ADD) {  // this band's share of the next RMSNorm
                 const float ss = block_sumsq(ok ? out : 0.0f, red);
-                if (t == 0) p.ss[band] = ss;
+                if (t == 0) st_tag(p.sst + band, ss, out_tag);
             }
         } else if (EPI == ST_SILU) {
-            vals[t] = v;
+            vals[t] = v * scale;
             named_sync(1, kStConsumers);
             const int col = band * SUB_BAND_COLS + t;
-            if (t < SUB_BAND_COLS && col < sub_cols) y[col] = silu_st(vals[t]) * vals[t + SUB_BAND_COLS];
+            if (t < SUB_BAND_COLS && col < sub_cols) st_tag(y + col, silu_st(vals[t]) * vals[t + SUB_BAND_COLS], out_tag);
             named_sync(1, kStConsumers);
-        } else {  // ST_QKV: RoPE on q and k, K/V written at pos
-            vals[t] = v;
+        } else {  // ST_QKV: RoPE on q and k; K/V written at pos and handed to attention
+            vals[t] = v * scale;
             named_sync(1, kStConsumers);
             const int col = band * BAND_COLS + t;
             const int total = p.nq_cols + 2 * p.nkv_cols;
-            const int pos = __ldcg(p.pos);
-            const int cap = p.max_blocks * p.block_tokens;
-            const bool pos_ok = pos >= 0 && pos < p.rope_rows && pos < cap;
-            if (!pos_ok && t == 0 && blockIdx.x == 0) flag_error(p.err, DS_ERR_POSITION);
             if (t < BAND_COLS && col < total) {
-                float out = v;
+                float out = vals[t];
                 if (col < p.nq_cols + p.nkv_cols) {
                     const int hd = p.hd, half = hd >> 1;
                     const int region = col < p.nq_cols ? 0 : p.nq_cols;
@@ -499,29 +514,36 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
                         b = first_of_pair ? vals[t + 1] : vals[t];
                     }
                     float c = 1.0f, sn = 0.0f;
-                    if (pos_ok) {
-                        c = p.rope_cos[(size_t)pos * half + pair];
-                        sn = p.rope_sin[(size_t)pos * half + pair];
+                    if (cx.pos_ok) {
+                        c = p.rope_cos[(size_t)cx.pos * half + pair];
+                        sn = p.rope_sin[(size_t)cx.pos * half + pair];
                     }
                     out = first_of_pair ? a * c - b * sn : a * sn + b * c;
                 }
                 if (col < p.nq_cols) {
-                    y[col] = out;
-                } else if (pos_ok) {
-                    const int blk = p.block_table ? __ldcg(p.block_table + pos / p.block_tokens) : pos / p.block_tokens;
-                    const long long row = (long long)blk * p.block_tokens + pos % p.block_tokens;
-                    if (col < p.nq_cols + p.nkv_cols)
-                        store_as(p.kc[layer], row * p.nkv_cols + (col - p.nq_cols), p.kv_dtype, out);
-                    else
-                        store_as(p.vc[layer], row * p.nkv_cols + (col - p.nq_cols - p.nkv_cols), p.kv_dtype, out);
+                    st_tag(y + col, out, out_tag);
+                } else {
+                    const int kv = col - p.nq_cols;  // k then v
+                    if (cx.pos_ok) {
+                        const int blk = p.block_table ? __ldcg(p.block_table + cx.pos / p.block_tokens)
+                                                      : cx.pos / p.block_tokens;
+                        const long long row = (long long)blk * p.block_tokens + cx.pos % p.block_tokens;
+                        if (kv < p.nkv_cols)
+                            store_as(p.kc[layer], row * p.nkv_cols + kv, p.kv_dtype, out);
+                        else
+                            store_as(p.vc[layer], row * p.nkv_cols + kv - p.nkv_cols, p.kv_dtype, out);
+                    }
+                    // attention reads this position from here, as the cache holds it
+                    const float held = p.kv_dtype == DS_BF16 ? __bfloat162float(__float2bfloat16_rn(out)) : out;
+                    st_tag(p.kvt + kv, held, out_tag);
                 }
             }
             named_sync(1, kStConsumers);
         }
     };
 
-    int pend_band[2], pend_first[2], pend_n[2];
-    int npend = 0;
+    int own_band = -1, own_first = 0;  // the shared band this CTA settles
+    float own_v = 0.0f;
     int seg_off = 0;
     for (long long u = u0; u < u1;) {
         const int band = (int)(u / UB);
@@ -568,62 +590,41 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
             for (int w = 0; w < kStConsumerWarps; ++w) v += red[w * BAND_COLS + t];
         named_sync(1, kStConsumers);
 
-        if (j0 == 0 && j1 == UB) {
-            epilogue(band, v, NAN);  // whole band here: final now
-        } else {
-            if (t < BAND_COLS) p.partials[(size_t)(blockIdx.x + band) * BAND_COLS + t] = v;
-            pend_band[npend] = band;
-            pend_first[npend] = (int)((((long long)band * UB + 1) * G - 1) / W);
-            const int last = (int)((((long long)(band + 1) * UB) * G - 1) / W);
-            pend_n[npend] = last - pend_first[npend] + 1;
-            ++npend;
+        if (j0 == 0 && j1 == UB) {  // whole band here: final now
+            u64 yw = 0;
+            if (EPI == ST_ADD && t < BAND_COLS && band * BAND_COLS + t < sub_cols) yw = ld_tag(y + band * BAND_COLS + t);
+            epilogue(band, v, yw);
+        } else if (j1 == UB) {  // this CTA holds the band's last box: it settles
+            own_band = band;
+            own_v = v;
+            own_first = (int)((((long long)band * UB + 1) * G - 1) / W);
+        } else if (t < BAND_COLS) {
+            st_tag(part + (size_t)(blockIdx.x + band) * BAND_COLS + t, v, out_tag);
         }
     }
 
-    if (npend > 0) {
-        // publish this CTA's partials and learn which shared bands it closes:
-        // one round trip for both, then one for the partial sums.  The old
-        // residual values of those bands (stable until their closing CTA
-        // writes them) are fetched alongside.
-        float yo0 = NAN, yo1 = NAN;
-        if (EPI == ST_ADD && t < BAND_COLS) {
-            const int c0 = pend_band[0] * BAND_COLS + t;
-            if (c0 < sub_cols) yo0 = ldcg(y + c0);
-            if (npend > 1) {
-                const int c1 = pend_band[1] * BAND_COLS + t;
-                if (c1 < sub_cols) yo1 = ldcg(y + c1);
-            }
-        }
-        named_sync(1, kStConsumers);
-        if (t == 0) {
-            int prev0 = -1, prev1 = -1;  // both requests in flight together
-            asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev0) : "l"(&p.counters[pend_band[0]])
-                         : "memory");
-            if (npend > 1)
-                asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev1)
-                             : "l"(&p.counters[pend_band[1]])
-                             : "memory");
-            s_flag[0] = prev0 == pend_n[0] - 1;
-            s_flag[1] = npend > 1 && prev1 == pend_n[1] - 1;
-            if (prev0 == pend_n[0] - 1) p.counters[pend_band[0]] = 0;
-            if (npend > 1 && prev1 == pend_n[1] - 1) p.counters[pend_band[1]] = 0;
-        }
-        named_sync(1, kStConsumers);
-        const bool last0 = s_flag[0] != 0, last1 = npend > 1 && s_flag[1] != 0;
-        named_sync(1, kStConsumers);
-        float v0 = 0.0f, v1 = 0.0f;
+    if (own_band >= 0) {
+        // the other contributors are CTAs own_first .. this one - 1, partial
+        // slot CTA + band; their loads go out together with the residual's
+        u64 yw = 0;
+        const int col = own_band * BAND_COLS + t;
+        if (EPI == ST_ADD && t < BAND_COLS && col < sub_cols) yw = ld_tag(y + col);
+        float tot = 0.0f;
         if (t < BAND_COLS) {
-            const int nmax = max(last0 ? pend_n[0] : 0, last1 ? pend_n[1] : 0);
-#pragma unroll 16
-            for (int c = 0; c < nmax; ++c) {
-                if (last0 && c < pend_n[0])
-                    v0 += ldcg(&p.partials[(size_t)(pend_first[0] + c + pend_band[0]) * BAND_COLS + t]);
-                if (last1 && c < pend_n[1])
-                    v1 += ldcg(&p.partials[(size_t)(pend_first[1] + c + pend_band[1]) * BAND_COLS + t]);
+            const int n = (int)blockIdx.x - own_first;
+            const u64 *base = part + (size_t)(own_first + own_band) * BAND_COLS + t;
+            for (int c0 = 0; c0 < n; c0 += 8) {
+                u64 w[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) w[c] = c0 + c < n ? ld_tag(base + (size_t)(c0 + c) * BAND_COLS) : 0ull;
+                tag_fix<8>(w, base + (size_t)c0 * BAND_COLS, BAND_COLS, n - c0, out_tag, p);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    if (c0 + c < n) tot += tag_f(w[c]);
             }
+            tot += own_v;
         }
-        if (last0) epilogue(pend_band[0], v0, yo0);
-        if (last1) epilogue(pend_band[1], v1, yo1);
+        epilogue(own_band, tot, yw);
     }
     trace_point(p, phase, 3);
 }
@@ -651,18 +652,23 @@ __device__ __forceinline__ void load4(const KT *base, long long off, bool ok, fl
     }
 }
 
-// Before the barrier that opens the attention phase: request this CTA's
-// share of the K/V rows into L2.  Rows before the current position were
-// written by earlier steps and do not change during this one.
+// Positions per attention split and the number of splits in use.
+__device__ __forceinline__ void attention_split(const StepCtx &cx, const StepParams &p, int &per, int &n_eff) {
+    per = max(kStAttnMinPer, (cx.n_ctx + p.attn_splits - 1) / p.attn_splits);
+    n_eff = (cx.n_ctx + per - 1) / per;
+}
+
+// Request into L2 the K/V rows of this CTA's attention item of `layer`:
+// rows before the current position, written by earlier steps.
 template <typename KT>
-__device__ void prefetch_attention(int layer, const StepParams &p) {
+__device__ void prefetch_attention(int layer, const StepCtx &cx, const StepParams &p) {
     const int n_items = p.n_kvh * p.attn_splits;
     if ((int)blockIdx.x >= n_items) return;
     const int g = blockIdx.x / p.attn_splits, split = blockIdx.x % p.attn_splits;
-    const int cap = p.max_blocks * p.block_tokens;
-    const int n_ctx = min(max(__ldcg(p.pos), 0), cap - 1);  // positions before pos
-    const int per = max(kStAttnMinPer, (n_ctx + 1 + p.attn_splits - 1) / p.attn_splits);
-    const int t0 = min(n_ctx, split * per), t1 = min(n_ctx, t0 + per);
+    int per, n_eff;
+    attention_split(cx, p, per, n_eff);
+    const int n_old = cx.n_ctx - 1;
+    const int t0 = min(n_old, split * per), t1 = min(n_old, t0 + per);
     const int row_bytes = p.hd * (int)sizeof(KT);  // one head's row
     const int lines = (row_bytes + 127) / 128;
     const int n = (t1 - t0) * lines * 2;
@@ -677,14 +683,17 @@ __device__ void prefetch_attention(int layer, const StepParams &p) {
     }
 }
 
-// One CTA's share of the attention phase: item (kv head g, split) = this CTA
-// (CTAs past the items idle).  Eight warps take runs of eight positions with
-// an online softmax, merged across warps in shared memory; the CTA publishes
-// its split's (max, sum, accumulator) and is done.  The splits of a head are
+// One CTA's share of the attention phase (id `pid`): item (kv head g, split)
+// = this CTA (CTAs past the items have none).  Eight warps take runs of eight
+// cached positions with an online softmax; the current position comes from
+// the tagged copy the q|k|v phase handed over.  Warps merge in shared memory
+// and the CTA publishes its split's (max, sum, accumulator) as tagged words;
+// splits past the context publish an empty record.  The splits of a head are
 // merged, in split order, by whoever reads the attention output next (the o
-// projection's prologue), so no CTA waits on another here.
+// projection's prologue).
 template <typename KT, int GQ>
-__device__ void consume_attention(int layer, float *scratch, const StepParams &p, int phase) {
+__device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *scratch, const StepParams &p,
+                                  int phase) {
     constexpr int RUN = 8;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int hd = p.hd;
@@ -692,17 +701,25 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
     trace_point(p, phase, 0);
     if ((int)blockIdx.x >= n_items) return;
     const int g = blockIdx.x / p.attn_splits, split = blockIdx.x % p.attn_splits;
+    const uint32_t q_tag = cx.seq(pid - 1), out_tag = cx.seq(pid);
+    const int rec = GQ * (hd + 2);
+    u64 *out = p.at + (size_t)(g * p.attn_splits + split) * rec;
     float *s_acc = scratch;                                   // [8][GQ][hd]
     float *s_m = s_acc + kStConsumerWarps * GQ * hd;          // [8][GQ]
     float *s_l = s_m + kStConsumerWarps * GQ;                 // [8][GQ]
+    float *s_q = s_l + kStConsumerWarps * GQ;                 // [GQ][hd]
 
-    const int cap = p.max_blocks * p.block_tokens;
-    int n_ctx = __ldcg(p.pos) + 1;
-    n_ctx = min(max(n_ctx, 1), cap);
-    const int per = max(kStAttnMinPer, (n_ctx + p.attn_splits - 1) / p.attn_splits);
-    const int n_eff = (n_ctx + per - 1) / per;
-    if (split >= n_eff) return;
-    const int t0 = min(n_ctx, split * per), t1 = min(n_ctx, t0 + per);
+    int per, n_eff;
+    attention_split(cx, p, per, n_eff);
+    if (split >= n_eff) {  // no positions: an empty record
+        for (int idx = t; idx < rec; idx += kStConsumers)
+            st_tag(out + idx, idx < GQ ? -INFINITY : 0.0f, out_tag);
+        trace_point(p, phase, 3);
+        return;
+    }
+    const int t0 = min(cx.n_ctx, split * per), t1 = min(cx.n_ctx, t0 + per);
+    const int tc = min(t1, cx.n_ctx - 1);  // cached positions [t0, tc)
+    const bool has_cur = t1 == cx.n_ctx;
     const bool active = lane * 4 < hd;
     const int d0 = lane * 4;
     const long long row_elems = (long long)p.n_kvh * hd;
@@ -711,7 +728,7 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
 
     float kf[RUN][4], vf[RUN][4];
     auto load_run = [&](int tb) {
-        const int nt = min(RUN, t1 - tb);
+        const int nt = min(RUN, tc - tb);
 #pragma unroll
         for (int i = 0; i < RUN; ++i) {
             const bool ok = active && i < nt;
@@ -726,12 +743,21 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
         }
     };
     int tb = t0 + warp * RUN;
-    if (tb < t1) load_run(tb);  // K/V requests go out before q's
-    float q[GQ][4];
+    if (tb < tc) load_run(tb);  // K/V requests go out before q is polled
+    {   // the group's q rows, polled once by the whole CTA into shared memory
+        const u64 *qg = p.qt + (size_t)g * GQ * hd;
+        for (int i0 = 0; i0 < GQ * hd; i0 += 2 * kStConsumers) {
+            u64 w[2];
 #pragma unroll
-    for (int j = 0; j < GQ; ++j)
+            for (int k = 0; k < 2; ++k) w[k] = i0 + k * kStConsumers + t < GQ * hd ? ld_tag(qg + i0 + k * kStConsumers + t) : 0ull;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) q[j][e] = active ? ldcg(p.q + (g * GQ + j) * hd + d0 + e) : 0.0f;
+            for (int k = 0; k < 2; ++k) {
+                const int i = i0 + k * kStConsumers + t;
+                if (i < GQ * hd) s_q[i] = tag_value(w[k], qg + i, q_tag, p);
+            }
+        }
+        named_sync(1, kStConsumers);
+    }
     const float scale = 1.0f / sqrtf((float)hd);
     float m[GQ], l[GQ], acc[GQ][4];
 #pragma unroll
@@ -741,16 +767,19 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
     }
-    while (tb < t1) {
-        const int nt = min(RUN, t1 - tb);
+    // one online-softmax update by `nt` positions whose K/V rows are in kf/vf
+    auto update = [&](int nt) {
 #pragma unroll
         for (int j = 0; j < GQ; ++j) {
+            // q of head j, dims d0.. (read from shared memory where it was staged)
+            const float4 qj = active ? *reinterpret_cast<const float4 *>(s_q + j * hd + d0) : make_float4(0.f, 0.f, 0.f, 0.f);
             float sc[RUN];
 #pragma unroll
             for (int i = 0; i < RUN; ++i) {
-                float dd = 0.0f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) dd = fmaf(q[j][e], kf[i][e], dd);
+                float dd = fmaf(qj.x, kf[i][0], 0.0f);
+                dd = fmaf(qj.y, kf[i][1], dd);
+                dd = fmaf(qj.z, kf[i][2], dd);
+                dd = fmaf(qj.w, kf[i][3], dd);
                 sc[i] = warp_sum(dd) * scale;
             }
             float mx = m[j];
@@ -771,8 +800,26 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
                 }
             m[j] = mx;
         }
+    };
+    while (tb < tc) {
+        update(min(RUN, tc - tb));
         tb += kStConsumerWarps * RUN;
-        if (tb < t1) load_run(tb);
+        if (tb < tc) load_run(tb);
+    }
+    if (has_cur && warp == kStConsumerWarps - 1) {  // the current position
+        const u64 *kt = p.kvt + (size_t)g * hd + d0, *vt = p.kvt + p.nkv_cols + (size_t)g * hd + d0;
+        u64 kw[4], vw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            kw[e] = active ? ld_tag(kt + e) : 0ull;
+            vw[e] = active ? ld_tag(vt + e) : 0ull;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            kf[0][e] = active ? tag_value(kw[e], kt + e, q_tag, p) : 0.0f;
+            vf[0][e] = active ? tag_value(vw[e], vt + e, q_tag, p) : 0.0f;
+        }
+        update(1);
     }
 #pragma unroll
     for (int j = 0; j < GQ; ++j) {
@@ -787,8 +834,6 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
     named_sync(1, kStConsumers);
     trace_point(p, phase, 2);
 
-    const int rec = GQ * (hd + 2);
-    float *part = p.a_partials + (size_t)(g * p.attn_splits + split) * rec;
     for (int idx = t; idx < GQ * hd; idx += kStConsumers) {
         const int j = idx / hd;
         float M = -INFINITY;
@@ -800,27 +845,26 @@ __device__ void consume_attention(int layer, float *scratch, const StepParams &p
                 L = fmaf(s_l[w * GQ + j], c, L);
                 A = fmaf(s_acc[(w * GQ + j) * hd + idx % hd], c, A);
             }
-        part[2 * GQ + idx] = A;
+        st_tag(out + 2 * GQ + idx, A, out_tag);
         if (idx % hd == 0) {
-            part[j] = M;
-            part[GQ + j] = L;
+            st_tag(out + j, M, out_tag);
+            st_tag(out + GQ + j, L, out_tag);
         }
     }
     trace_point(p, phase, 3);
 }
 
 // Attention output rows [k0, k1) (k indexes query head h = k / hd, dim
-// k % hd), merged from the published splits of their KV heads in split order:
-// out = sum_s w_s acc_s / sum_s w_s l_s with w_s = exp(m_s - max m), written
-// to xs.  `red` holds the per-head weights.
+// k % hd), merged from the tagged split records of their KV heads in split
+// order: out = sum_s w_s acc_s / sum_s w_s l_s with w_s = exp(m_s - max m),
+// written to xs.  `red` holds the per-head weights.
 template <int GQ>
-__device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, const StepParams &p) {
+__device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, uint32_t tag, const StepCtx &cx,
+                                     const StepParams &p) {
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int hd = p.hd;
-    const int cap = p.max_blocks * p.block_tokens;
-    const int n_ctx = min(max(__ldcg(p.pos) + 1, 1), cap);
-    const int per = max(kStAttnMinPer, (n_ctx + p.attn_splits - 1) / p.attn_splits);
-    const int n_eff = (n_ctx + per - 1) / per;
+    int per, n_eff;
+    attention_split(cx, p, per, n_eff);
     const int rec = GQ * (hd + 2);
     const int h_lo = k0 / hd, h_hi = (k1 - 1) / hd;
     const int nh = h_hi - h_lo + 1;
@@ -828,15 +872,24 @@ __device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, cons
     float *Lh = red + nh * kStMaxSplits;  // [nh]
     for (int hl = warp; hl < nh; hl += kStConsumerWarps) {
         const int h = h_lo + hl, g = h / GQ, j = h % GQ;
-        const float *base = p.a_partials + (size_t)g * p.attn_splits * rec;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+        const u64 *base = p.at + (size_t)g * p.attn_splits * rec;
+        u64 mw0 = 0, lw0 = 0, mw1 = 0, lw1 = 0;
         if (lane < n_eff) {
-            m0 = ldcg(base + (size_t)lane * rec + j);
-            l0 = ldcg(base + (size_t)lane * rec + GQ + j);
+            mw0 = ld_tag(base + (size_t)lane * rec + j);
+            lw0 = ld_tag(base + (size_t)lane * rec + GQ + j);
         }
         if (lane + 32 < n_eff) {
-            m1 = ldcg(base + (size_t)(lane + 32) * rec + j);
-            l1 = ldcg(base + (size_t)(lane + 32) * rec + GQ + j);
+            mw1 = ld_tag(base + (size_t)(lane + 32) * rec + j);
+            lw1 = ld_tag(base + (size_t)(lane + 32) * rec + GQ + j);
+        }
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+        if (lane < n_eff) {
+            m0 = tag_value(mw0, base + (size_t)lane * rec + j, tag, p);
+            l0 = tag_value(lw0, base + (size_t)lane * rec + GQ + j, tag, p);
+        }
+        if (lane + 32 < n_eff) {
+            m1 = tag_value(mw1, base + (size_t)(lane + 32) * rec + j, tag, p);
+            l1 = tag_value(lw1, base + (size_t)(lane + 32) * rec + GQ + j, tag, p);
         }
         const float M = warp_max(fmaxf(m0, m1));
         const float w0 = (lane < n_eff && m0 != -INFINITY) ? expf(m0 - M) : 0.0f;
@@ -849,18 +902,26 @@ __device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, cons
     named_sync(1, kStConsumers);
     for (int k = k0 + t; k < k1; k += kStConsumers) {
         const int h = k / hd, g = h / GQ, j = h % GQ, hl = h - h_lo;
-        const float *rp = p.a_partials + (size_t)g * p.attn_splits * rec + 2 * GQ + j * hd + k % hd;
+        const u64 *rp = p.at + (size_t)g * p.attn_splits * rec + 2 * GQ + j * hd + k % hd;
         float A = 0.0f;
-#pragma unroll 16
-        for (int sp = 0; sp < n_eff; ++sp) A = fmaf(ldcg(rp + (size_t)sp * rec), wt[hl * kStMaxSplits + sp], A);
+        for (int s0 = 0; s0 < n_eff; s0 += 16) {
+            u64 w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = s0 + i < n_eff ? ld_tag(rp + (size_t)(s0 + i) * rec) : 0ull;
+            tag_fix<16>(w, rp + (size_t)s0 * rec, rec, n_eff - s0, tag, p);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (s0 + i < n_eff) A = fmaf(tag_f(w[i]), wt[hl * kStMaxSplits + s0 + i], A);
+        }
         xs[k - k0] = A / Lh[hl];
     }
     named_sync(1, kStConsumers);
 }
 
-// The head phase: logits of this CTA's rows, then the greedy pick.
+// The head phase: logits of this CTA's rows, then (once every CTA has
+// finished) the greedy pick and the launch's epoch advance.
 template <typename T>
-__device__ void consume_gn(const Ring &r, uint32_t &fill, float *scratch, const StepParams &p) {
+__device__ void consume_gn(const Ring &r, uint32_t &fill, uint32_t in_tag, float *scratch, const StepParams &p) {
     constexpr int LE = 16 / sizeof(T);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int G = gridDim.x;
@@ -874,9 +935,21 @@ __device__ void consume_gn(const Ring &r, uint32_t &fill, float *scratch, const 
     float *xs = bestv + 512;                             // [cols]
     float *rowpart = xs + cols;                          // [rows of this CTA][parts]
 
-    const float scale = scale_from_ss(p, cols, bestv);
-    for (int i = t; i < cols; i += kStConsumers) xs[i] = ldcg(p.x + i) * scale * p.final_norm[i];
+    for (int i0 = 0; i0 < cols; i0 += 8 * kStConsumers) {
+        u64 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * kStConsumers + t;
+            v[q] = i < cols ? ld_tag(p.xt + i) : 0ull;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * kStConsumers + t;
+            if (i < cols) xs[i] = tag_value(v[q], p.xt + i, in_tag, p) * __ldg(p.final_norm + i);
+        }
+    }
     named_sync(1, kStConsumers);
+    const float scale = scale_from_sst(p, cols, in_tag, bestv);
 
     const int chunks = (int)(row_bytes / 16);
     for (int rr = r0; rr < r1; rr += rps) {
@@ -929,13 +1002,13 @@ __device__ void consume_gn(const Ring &r, uint32_t &fill, float *scratch, const 
     for (int q = t; q < r1 - r0; q += kStConsumers) {
         float logit = 0.0f;
         for (int k = 0; k < parts; ++k) logit += rowpart[q * parts + k];
+        logit *= scale;
         p.logits[r0 + q] = logit;
         if (ranks_above(logit, r0 + q, bv, bi)) {
             bv = logit;
             bi = r0 + q;
         }
     }
-    if (!p.greedy) return;
     bestv[t] = bv;
     besti[t] = bi;
     named_sync(1, kStConsumers);
@@ -950,24 +1023,28 @@ __device__ void consume_gn(const Ring &r, uint32_t &fill, float *scratch, const 
         p.am_val[blockIdx.x] = bv;
         p.am_idx[blockIdx.x] = bi;
         __threadfence();
-        if (atomicAdd(p.am_counter, 1) == G - 1) {
+        if (atomicAdd(p.am_counter, 1) == G - 1) {  // every CTA is done with the step
             __threadfence();
-            bv = ldcg(&p.am_val[0]);
-            bi = __ldcg(&p.am_idx[0]);
-            for (int j = 1; j < G; ++j) {
-                const float v = ldcg(&p.am_val[j]);
-                const int ix = __ldcg(&p.am_idx[j]);
-                if (ranks_above(v, ix, bv, bi)) {
-                    bv = v;
-                    bi = ix;
+            if (p.greedy) {
+                bv = ldcg(&p.am_val[0]);
+                bi = __ldcg(&p.am_idx[0]);
+                for (int j = 1; j < G; ++j) {
+                    const float v = ldcg(&p.am_val[j]);
+                    const int ix = __ldcg(&p.am_idx[j]);
+                    if (ranks_above(v, ix, bv, bi)) {
+                        bv = v;
+                        bi = ix;
+                    }
+                }
+                p.next_ids[0] = bi;
+                if (p.advance) {
+                    p.tokens[0] = bi;
+                    p.pos[0] += 1;
                 }
             }
             *p.am_counter = 0;
-            p.next_ids[0] = bi;
-            if (p.advance) {
-                p.tokens[0] = bi;
-                p.pos[0] += 1;
-            }
+            // every CTA read this launch's epoch at its start: advance it
+            asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(p.epoch) : "memory");
         }
     }
 }
@@ -1001,67 +1078,73 @@ __global__ void __launch_bounds__(kStThreads, 1) step_kernel(const __grid_consta
     }
 
     // ---------------- consumers
-    int phase = 0;
-    uint32_t fill = 0;
-    GridBarrier gb;
+    StepCtx cx;
+    int tok;
     {
         __shared__ unsigned long long s_epoch;
+        __shared__ int s_pos, s_tok;
         if (threadIdx.x == 0) {
             unsigned long long e;
-            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(e) : "l"(reinterpret_cast<unsigned long long *>(p.bar) + 1) : "memory");
+            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(e) : "l"(p.epoch) : "memory");
             s_epoch = e;
+            s_pos = __ldcg(p.pos);
+            s_tok = __ldcg(p.tokens);
         }
         named_sync(1, kStConsumers);
-        gb.base = s_epoch * (unsigned long long)G * (unsigned long long)(1 + 5 * p.n_layer);
-        gb.k = 0;
+        cx.seq.base = (uint32_t)(s_epoch & 0x3FFFFFull) << 10;
+        cx.pos = s_pos;
+        tok = s_tok;
+        named_sync(1, kStConsumers);
     }
+    const int cap = p.max_blocks * p.block_tokens;
+    cx.pos_ok = cx.pos >= 0 && cx.pos < p.rope_rows && cx.pos < cap;
+    if (!cx.pos_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_error(p.err, DS_ERR_POSITION);
+    cx.n_ctx = min(max(cx.pos + 1, 1), cap);
+
+    int phase = 0;
+    uint32_t fill = 0;
     mark_phase(p, phase);
-    {   // embed: x = E[token]; every CTA copies a slice
-        int tok = __ldcg(p.tokens);
+    {   // embed (phase id 0): x = E[token]; every CTA writes a slice
         if (tok < 0 || tok >= p.vocab) {
             if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(p.err, DS_ERR_TOKEN_RANGE);
             tok = min(max(tok, 0), p.vocab - 1);
         }
+        const uint32_t tag = cx.seq(0);
         const T *row = reinterpret_cast<const T *>(p.emb) + (long long)tok * p.d;
         const int i0 = (int)((long long)p.d * blockIdx.x / G), i1 = (int)((long long)p.d * (blockIdx.x + 1) / G);
-        for (int i = i0 + threadIdx.x; i < i1; i += kStConsumers) p.x[i] = to_f32(row[i]);
+        for (int i = i0 + threadIdx.x; i < i1; i += kStConsumers) st_tag(p.xt + i, to_f32(row[i]), tag);
         // the square sum of band b of the row (the bands the residual
         // projections use), for the first RMSNorm
-        if ((int)blockIdx.x < p.n_ss) {
+        for (int b = blockIdx.x; b < p.n_ss; b += G) {
             const int bc = kStBandBytes / (int)sizeof(T);
-            const int col = blockIdx.x * bc + threadIdx.x;
+            const int col = b * bc + threadIdx.x;
             const float v = (threadIdx.x < bc && col < p.d) ? to_f32(row[col]) : 0.0f;
             const float ss = block_sumsq(v, scratch);
-            if (threadIdx.x == 0) p.ss[blockIdx.x] = ss;
+            if (threadIdx.x == 0) st_tag(p.sst + b, ss, tag);
         }
     }
-    grid_sync(p, G, gb);
-    // every CTA has read the epoch: advance it for the next launch
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-        asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(reinterpret_cast<unsigned long long *>(p.bar) + 1) : "memory");
     for (int l = 0; l < p.n_layer; ++l) {
         const StepLayer &L = p.layers[l];
+        const int ph = ph_qkv(l);
+        const uint32_t x_in = cx.seq(5 * l);  // the residual as the previous layer left it
+        prefetch_attention<KT>(l, cx, p);
         mark_phase(p, phase);
-        consume_gt<T, ST_QKV, SRC_NORM, GQ>(r, fill, p.d, p.nq_cols + 2 * p.nkv_cols, p.nb_qkv, p.x, L.n1, p.q, l, scratch, p,
-                                    phase - 1);
-        prefetch_attention<KT>(l, p);
-        grid_sync(p, G, gb);
+        consume_gt<T, ST_QKV, SRC_NORM, GQ>(r, fill, p.d, p.nq_cols + 2 * p.nkv_cols, p.nb_qkv, p.xt, x_in, L.n1,
+                                            p.qt, 0, l, ph, cx, scratch, p, phase - 1);
         mark_phase(p, phase);
-        consume_attention<KT, GQ>(l, scratch, p, phase - 1);
-        grid_sync(p, G, gb);
+        consume_attention<KT, GQ>(l, ph + 1, cx, scratch, p, phase - 1);
         mark_phase(p, phase);
-        consume_gt<T, ST_ADD, SRC_ATTN, GQ>(r, fill, p.nq_cols, p.d, p.nb_o, nullptr, nullptr, p.x, l, scratch, p,
-                                            phase - 1);
-        grid_sync(p, G, gb);
+        consume_gt<T, ST_ADD, SRC_ATTN, GQ>(r, fill, p.nq_cols, p.d, p.nb_o, nullptr, cx.seq(ph + 1), nullptr, p.xt,
+                                            x_in, l, ph + 2, cx, scratch, p, phase - 1);
         mark_phase(p, phase);
-        consume_gt<T, ST_SILU, SRC_NORM, GQ>(r, fill, p.d, p.ff, p.nb_gu, p.x, L.n2, p.f, l, scratch, p, phase - 1);
-        grid_sync(p, G, gb);
+        consume_gt<T, ST_SILU, SRC_NORM, GQ>(r, fill, p.d, p.ff, p.nb_gu, p.xt, cx.seq(ph + 2), L.n2, p.ft, 0, l,
+                                             ph + 3, cx, scratch, p, phase - 1);
         mark_phase(p, phase);
-        consume_gt<T, ST_ADD, SRC_PLAIN, GQ>(r, fill, p.ff, p.d, p.nb_d, p.f, nullptr, p.x, l, scratch, p, phase - 1);
-        grid_sync(p, G, gb);
+        consume_gt<T, ST_ADD, SRC_PLAIN, GQ>(r, fill, p.ff, p.d, p.nb_d, p.ft, cx.seq(ph + 3), nullptr, p.xt,
+                                             cx.seq(ph + 2), l, ph + 4, cx, scratch, p, phase - 1);
     }
     mark_phase(p, phase);
-    consume_gn<T>(r, fill, scratch, p);
+    consume_gn<T>(r, fill, cx.seq(5 * p.n_layer), scratch, p);
     mark_phase(p, phase);
 }
 
@@ -1093,7 +1176,7 @@ int step_scratch_floats(const ds_model_config *c, int grid, int nb_qkv, int nb_o
     gt += kStConsumerWarps * 256 + 256 + 16;
     const int gq = c->n_qh / c->n_kvh;
     const long long at = std::max((long long)kStConsumerWarps * gq * c->head_dim, 2LL * kStMaxSplits * gq + 2 * gq) +
-                         2LL * kStConsumerWarps * gq + 16;
+                         2LL * kStConsumerWarps * gq + (long long)gq * c->head_dim + 16;
     const long long row_bytes = (long long)c->d * es;
     const long long rps = std::max(1LL, (long long)kStStageBytes / row_bytes);
     const long long parts = rps >= kStConsumerWarps ? 1 : kStConsumerWarps / rps;

@@ -246,12 +246,25 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ GPU arm
+STEP_PROFILE = os.path.join(ROOT, "profiles", "step_kernel_llama3_8b.md")
+
+
+def kernel_source_sha():
+    """sha256 over the sources of the persistent step kernel (the dominant
+    kernel); the committed ncu summary records the value it was taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("step.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "autoregressive_decode_step_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def profile_summary_traffic(kernel_src_sha):
-    """DRAM bytes per launch of the gate|up projection from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "gemv_gate_up_llama3_8b.md")
+    """DRAM bytes per full-size step-kernel launch from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
     try:
-        text = open(path).read()
+        text = open(STEP_PROFILE).read()
     except OSError:
         return None
     sha = traffic = None
@@ -267,8 +280,6 @@ def profile_summary_traffic(kernel_src_sha):
 
 
 def run_ours(args, rank, world, local):
-    import hashlib
-
     import torch
 
     from autoregressive_decode_step_gb300 import build as B
@@ -360,37 +371,50 @@ def run_ours(args, rank, world, local):
     e2e_s = max_over_ranks(t1 - t0, world)
     e2e_value = world * K / e2e_s
 
-    # ---------------- per-kernel timing: each kind launched back to back over
-    # every layer, CUDA events around the passes, on the bench stream
+    # ---------------- per-op breakdown inside the step kernel: device
+    # timestamps (globaltimer) at every phase boundary, a few untimed steps
     reset()
-    kinds = ["embed", "qkv", "attention", "o_proj", "gate_up", "down", "head"]
-    us = {k: model.kernel_time_us(k, reps=4, stream=stream) for k in kinds}
-    per_step = {k: us[k] * (1 if k in ("embed", "head") else cfg["n_layer"]) for k in kinds}
-    gu_us = us["gate_up"]
-    gu_bytes = cfg["d"] * 2 * cfg["ff"] * 2 + cfg["d"] * 4 + cfg["ff"] * 4
+    names = []
+    acc = {}
+    n_pt = 8
+    with torch.cuda.stream(stream):
+        for _ in range(n_pt):
+            model.step(advance=True, stream=stream, phase_times=True)
+            for name, t in model.phase_times_us(stream=stream):
+                if name not in acc:
+                    names.append(name)
+                    acc[name] = []
+                acc[name].append(t)
+    per_step = {k: sum(acc[k]) / n_pt for k in names}
+    per_launch = {k: per_step[k] / (1 if k in ("embed", "head") else cfg["n_layer"]) for k in names}
+
+    # the dominant (and only) kernel of a greedy step is the persistent step
+    # kernel: one launch per step, so its mean launch duration is the
+    # CUDA-event time of the K replays / K
     peak, peak_kind = peaks()
-    src = open(os.path.join(ROOT, "autoregressive_decode_step_gb300", "csrc", "gemv.cu"), "rb").read()
-    sha = hashlib.sha256(src).hexdigest()
-    achieved = gu_bytes / (gu_us / 1e6) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profile_summary_traffic(sha),
-                "kernel": "gemv_t_kernel gate|up with SiLU epilogue, 4096x28672 bf16",
-                "peak_source": peak_kind, "algorithmic_bytes_per_launch": gu_bytes, "mean_launch_us": gu_us}
-    # the whole step against the HBM roofline (weights once + K/V read)
     step_bytes = [C.step_bytes(cfg, args.ctx + i + 1) for i in range(K)]
-    step_gbs = sum(step_bytes) / (ms / 1000.0) / 1e9
+    alg_bytes = sum(step_bytes) / K
+    launch_us = ms * 1000.0 / K
+    achieved = alg_bytes / (launch_us / 1e6) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profile_summary_traffic(kernel_source_sha()) if args.layers is None else None,
+                "kernel": "step_kernel: persistent cooperative decode step (all layers + head + argmax), "
+                          "one launch per token",
+                "peak_source": peak_kind + " (MEASURED_PEAKS hbm_gbs copy)" if peak_kind == "measured" else peak_kind,
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "algorithmic_bytes": "every weight byte once + K/V of every attended position",
+                "mean_launch_us": launch_us}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
             "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (random-init weights N(0,0.02), random prompt)",
             "config": dict(workload_config(args, cfg), kv_fill=args.kv_fill),
-            "hbm_roofline_step": {"bytes_per_step_mean": sum(step_bytes) / K, "achieved_gbs": step_gbs,
-                                  "peak_gbs": peak, "frac": step_gbs / peak,
-                                  "frac_of_nominal_7900": step_gbs / NOMINAL_HBM_GBS},
             "roofline": roofline,
-            "per_op_us_per_launch": us, "per_op_us_per_step": per_step,
+            "frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
+            "per_op_us_per_launch": per_launch, "per_op_us_per_step": per_step,
+            "per_op_source": "device phase timestamps inside the step kernel, mean of %d steps" % n_pt,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
-            "gpu_launches": K * (2 + 5 * cfg["n_layer"]),
+            "gpu_launches": K,
             "clocks": clocks.summary(t_wall0, t_wall1)}
     del W, model
     torch.cuda.empty_cache()
