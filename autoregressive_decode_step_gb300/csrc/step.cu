@@ -312,8 +312,36 @@ __device__ __forceinline__ float tag_value(u64 v, const u64 *a, uint32_t tag, co
 __device__ __forceinline__ float ld_wait(const u64 *a, uint32_t tag, const StepParams &p) {
     return tag_value(ld_tag(a), a, tag, p);
 }
-// Words w[0..n) loaded from base[i * stride]: poll the ones that lacked `tag`
-// (addresses are recomputed only on that rare path).
+// Words w[i] loaded from a[i] (a[i] == nullptr: unused slot): until every
+// one carries `tag`, reload all the stale ones together, so a batch that
+// arrived late costs one L2 round trip per poll, not one per word.  Gives up
+// (stale words read as 0) once the step is aborted or the wait limit passes.
+template <int N>
+__device__ __forceinline__ void tag_fix_at(u64 (&w)[N], const u64 *const (&a)[N], uint32_t tag,
+                                           const StepParams &p) {
+    auto stale = [&]() {
+        bool st = false;
+#pragma unroll
+        for (int i = 0; i < N; ++i) st = st || (a[i] && (uint32_t)(w[i] >> 32) != tag);
+        return st;
+    };
+    if (!stale()) return;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (a[i] && (uint32_t)(w[i] >> 32) != tag) w[i] = ld_tag(a[i]);
+        if (!stale()) return;
+        if ((it & 15u) == 0 && (aborted(p) || global_timer_ns() - t0 > kWaitLimitNs)) {
+            if (!aborted(p)) raise_abort(p, DS_ERR_WAIT_TIMEOUT);
+#pragma unroll
+            for (int i = 0; i < N; ++i)
+                if (a[i] && (uint32_t)(w[i] >> 32) != tag) w[i] = 0;
+            return;
+        }
+    }
+}
+// The same for words w[0..n) loaded from base[i * stride].
 template <int N>
 __device__ __forceinline__ void tag_fix(u64 (&w)[N], const u64 *base, size_t stride, int n, uint32_t tag,
                                         const StepParams &p) {
@@ -321,11 +349,11 @@ __device__ __forceinline__ void tag_fix(u64 (&w)[N], const u64 *base, size_t str
 #pragma unroll
     for (int i = 0; i < N; ++i)
         if (i < n) ok = ok && (uint32_t)(w[i] >> 32) == tag;
-    if (!ok) {
+    if (ok) return;
+    const u64 *a[N];
 #pragma unroll
-        for (int i = 0; i < N; ++i)
-            if (i < n && (uint32_t)(w[i] >> 32) != tag) w[i] = tag_wait_slow(base + (size_t)i * stride, tag, p);
-    }
+    for (int i = 0; i < N; ++i) a[i] = i < n ? base + (size_t)i * stride : nullptr;
+    tag_fix_at<N>(w, a, tag, p);
 }
 __device__ __forceinline__ float tag_f(u64 w) { return __uint_as_float((uint32_t)w); }
 
@@ -444,13 +472,15 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
                     const int k = kb + q * kStConsumers + t;
                     v[q] = (k < k1 && k < K) ? ld_tag(xin + k) : 0ull;
                 }
+                const int nv = min(8, max(0, (min(k1, K) - kb - t + kStConsumers - 1) / kStConsumers));
+                tag_fix<8>(v, xin + kb + t, kStConsumers, nv, in_tag, p);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const int k = kb + q * kStConsumers + t;
                     if (k < k1) {
                         float o = 0.0f;
                         if (k < K) {
-                            o = tag_value(v[q], xin + k, in_tag, p);
+                            o = tag_f(v[q]);
                             if (NORM) o *= __ldg(norm_w + k);
                         }
                         xs[off + k - k0] = o;
@@ -750,10 +780,12 @@ __device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *
             u64 w[2];
 #pragma unroll
             for (int k = 0; k < 2; ++k) w[k] = i0 + k * kStConsumers + t < GQ * hd ? ld_tag(qg + i0 + k * kStConsumers + t) : 0ull;
+            const int nv = min(2, max(0, (GQ * hd - i0 - t + kStConsumers - 1) / kStConsumers));
+            tag_fix<2>(w, qg + i0 + t, kStConsumers, nv, q_tag, p);
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int i = i0 + k * kStConsumers + t;
-                if (i < GQ * hd) s_q[i] = tag_value(w[k], qg + i, q_tag, p);
+                if (i < GQ * hd) s_q[i] = tag_f(w[k]);
             }
         }
         named_sync(1, kStConsumers);
@@ -808,16 +840,20 @@ __device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *
     }
     if (has_cur && warp == kStConsumerWarps - 1) {  // the current position
         const u64 *kt = p.kvt + (size_t)g * hd + d0, *vt = p.kvt + p.nkv_cols + (size_t)g * hd + d0;
-        u64 kw[4], vw[4];
+        u64 w[8];
+        const u64 *a[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            kw[e] = active ? ld_tag(kt + e) : 0ull;
-            vw[e] = active ? ld_tag(vt + e) : 0ull;
+            a[e] = active ? kt + e : nullptr;
+            a[4 + e] = active ? vt + e : nullptr;
         }
 #pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = a[e] ? ld_tag(a[e]) : 0ull;
+        tag_fix_at<8>(w, a, q_tag, p);
+#pragma unroll
         for (int e = 0; e < 4; ++e) {
-            kf[0][e] = active ? tag_value(kw[e], kt + e, q_tag, p) : 0.0f;
-            vf[0][e] = active ? tag_value(vw[e], vt + e, q_tag, p) : 0.0f;
+            kf[0][e] = active ? tag_f(w[e]) : 0.0f;
+            vf[0][e] = active ? tag_f(w[4 + e]) : 0.0f;
         }
         update(1);
     }
@@ -873,23 +909,23 @@ __device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, uint
     for (int hl = warp; hl < nh; hl += kStConsumerWarps) {
         const int h = h_lo + hl, g = h / GQ, j = h % GQ;
         const u64 *base = p.at + (size_t)g * p.attn_splits * rec;
-        u64 mw0 = 0, lw0 = 0, mw1 = 0, lw1 = 0;
-        if (lane < n_eff) {
-            mw0 = ld_tag(base + (size_t)lane * rec + j);
-            lw0 = ld_tag(base + (size_t)lane * rec + GQ + j);
-        }
-        if (lane + 32 < n_eff) {
-            mw1 = ld_tag(base + (size_t)(lane + 32) * rec + j);
-            lw1 = ld_tag(base + (size_t)(lane + 32) * rec + GQ + j);
-        }
+        const u64 *a[4];
+        a[0] = lane < n_eff ? base + (size_t)lane * rec + j : nullptr;
+        a[1] = lane < n_eff ? base + (size_t)lane * rec + GQ + j : nullptr;
+        a[2] = lane + 32 < n_eff ? base + (size_t)(lane + 32) * rec + j : nullptr;
+        a[3] = lane + 32 < n_eff ? base + (size_t)(lane + 32) * rec + GQ + j : nullptr;
+        u64 w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = a[i] ? ld_tag(a[i]) : 0ull;
+        tag_fix_at<4>(w, a, tag, p);
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
         if (lane < n_eff) {
-            m0 = tag_value(mw0, base + (size_t)lane * rec + j, tag, p);
-            l0 = tag_value(lw0, base + (size_t)lane * rec + GQ + j, tag, p);
+            m0 = tag_f(w[0]);
+            l0 = tag_f(w[1]);
         }
         if (lane + 32 < n_eff) {
-            m1 = tag_value(mw1, base + (size_t)(lane + 32) * rec + j, tag, p);
-            l1 = tag_value(lw1, base + (size_t)(lane + 32) * rec + GQ + j, tag, p);
+            m1 = tag_f(w[2]);
+            l1 = tag_f(w[3]);
         }
         const float M = warp_max(fmaxf(m0, m1));
         const float w0 = (lane < n_eff && m0 != -INFINITY) ? expf(m0 - M) : 0.0f;
@@ -942,10 +978,12 @@ __device__ void consume_gn(const Ring &r, uint32_t &fill, uint32_t in_tag, float
             const int i = i0 + q * kStConsumers + t;
             v[q] = i < cols ? ld_tag(p.xt + i) : 0ull;
         }
+        const int nv = min(8, max(0, (cols - i0 - t + kStConsumers - 1) / kStConsumers));
+        tag_fix<8>(v, p.xt + i0 + t, kStConsumers, nv, in_tag, p);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int i = i0 + q * kStConsumers + t;
-            if (i < cols) xs[i] = tag_value(v[q], p.xt + i, in_tag, p) * __ldg(p.final_norm + i);
+            if (i < cols) xs[i] = tag_f(v[q]) * __ldg(p.final_norm + i);
         }
     }
     named_sync(1, kStConsumers);
