@@ -90,6 +90,9 @@ _sig("ds_device_sm_count", ctypes.c_int)
 _sig("ds_gemv_workspace_bytes", SZ, I64, I64, ctypes.c_int)
 _sig("ds_gemv_transposed", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P, SZ, P)
 _sig("ds_gemv", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P)
+_sig("ds_gemm_workspace_bytes", SZ, I64, I64, I64)
+_sig("ds_gemm_transposed", ctypes.c_int, P, I64, P, I64, I64, I64, I64, P, I64, P, SZ, P)
+_sig("ds_gemm", ctypes.c_int, P, I64, P, I64, I64, I64, I64, P, I64, P, SZ, P)
 _sig("ds_gemv_transposed_noalloc", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P)
 _sig("ds_gemv_transposed_noalloc_max_bytes", SZ)
 _sig("ds_residual_add", ctypes.c_int, P, I64, P, I64, P, I64, P)
@@ -189,6 +192,16 @@ def ds_gemv_transposed_noalloc(A, x, rows, cols, y, stream=None):
 def ds_gemv(W, x, rows, cols, y, stream=None):
     check(lib.ds_gemv(ptr(W), W.numel(), dtype_code(W), ptr(x), x.numel(), rows, cols, ptr(y), y.numel(),
                       stream_handle(stream)), "ds_gemv")
+
+
+def ds_gemm_transposed(A, X, n, rows, cols, Y, ws, stream=None):
+    check(lib.ds_gemm_transposed(ptr(A), A.numel(), ptr(X), X.numel(), n, rows, cols, ptr(Y), Y.numel(), ptr(ws),
+                                 nbytes(ws), stream_handle(stream)), "ds_gemm_transposed")
+
+
+def ds_gemm(W, X, n, rows, cols, Y, ws, stream=None):
+    check(lib.ds_gemm(ptr(W), W.numel(), ptr(X), X.numel(), n, rows, cols, ptr(Y), Y.numel(), ptr(ws), nbytes(ws),
+                      stream_handle(stream)), "ds_gemm")
 
 
 def ds_residual_add(a, b, out, n, stream=None):

@@ -1,0 +1,665 @@
+// Batched projections on the fifth-generation tensor cores (tcgen05).
+//
+// When a decode step serves n sequences at once ("Inside the engine",
+// section 4: batched decode, one token per sequence per step), every
+// projection y_s = A^T x_s of the step ("LLM inference kernels", "A parallel
+// path for one frozen kernel's known-slow shape") is applied to n vectors and
+// becomes a skinny GEMM: Y[s][j] = sum_i A[i][j] X[s][i].  The weight matrix
+// goes on the MMA's M side (128 output features per tile) and the n <= 256
+// activation rows on its N side, so one weight byte is fetched once for all n
+// sequences and the accumulator (128 lanes x n columns of fp32) lives in
+// tensor memory.  Operands are bf16 (activations are rounded to bf16 when
+// they are written for this kernel), accumulation fp32.
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0, one thread: TMA producer.  Per 64-row k-block it loads the weight
+//     tile (two 64 x 64 boxes of an [in][out] matrix, or one 128 x 64 box of
+//     a [vocab][d] head) and the activation tile (n_pad x 64) into one stage
+//     of a shared-memory ring, 128-byte swizzled, completing on the stage's
+//     mbarrier.  With programmatic dependent launch the weight boxes of the
+//     first stages are requested before the previous kernel has finished.
+//   warp 1: allocates the tensor memory (two accumulator buffers) and, from
+//     one thread, issues tcgen05.mma (kind::f16, M = 128, N = n_pad, K = 16)
+//     four times per stage; tcgen05.commit frees the stage and, after a
+//     tile's last stage, signals its accumulator buffer full.
+//   warps 2-5: read the accumulator (tcgen05.ld, warp w owns lanes
+//     32 (w % 4) ..) and run the fused epilogue: store, residual add,
+//     SiLU-gate to bf16, or RoPE + K/V write for the q|k|v projection.
+//
+// Work split: the (tile, k-block) units are cut into equal contiguous ranges,
+// one per CTA (every CTA streams the same weight bytes whatever the shape).
+// A tile whose k-blocks fall to several CTAs is finished by the last of them
+// to arrive (an atomic counter, never a wait): it adds the partial
+// accumulators the contributors left in the workspace in CTA order, so results
+// are bit-stable run to run.  Every mbarrier wait is bounded; a wait that
+// times out flags DS_ERR_WAIT_TIMEOUT and the kernel winds down, draining its
+// copies and MMAs in flight and freeing its tensor memory before it exits.
+#include <algorithm>
+
+#include "common.cuh"
+#include "tc.h"
+
+namespace ds {
+
+constexpr int kTcBM = 128;        // output features per tile (MMA M)
+constexpr int kTcBK = 64;         // reduced rows per stage: 128 bytes of bf16, one swizzle span
+constexpr int kTcThreads = 192;
+constexpr int kTcEpiThreads = 128;
+constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
+constexpr int kTcMaxStages = 8;
+constexpr int kTcXchStride = 33;  // floats per feature row of the epilogue exchange buffer
+constexpr size_t kTcSmemLimit = 227 * 1024;
+
+// ---------------------------------------------------------------- tcgen05 PTX
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] x B[smem]: one MMA of kind::f16 on this CTA's SM.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+// 32 consecutive accumulator columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets, the fixed tcgen05 version field and 128-byte swizzling.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A
+// MN-major (a_mn) or K-major, B K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t tc_idesc(int a_mn, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(kTcBM >> 4) << 24);
+}
+
+// Bounded mbarrier wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                flag_error(err, DS_ERR_WAIT_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_box_g2s_nohint(void *dst, const void *map, int c0, int r0, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Segment of a CTA's unit range that lies in one tile.
+struct TcSeg {
+    int tile, kb0, kb1;
+};
+
+__device__ __forceinline__ bool tc_next_seg(long long &u, long long u1, int KB, TcSeg &s) {
+    if (u >= u1) return false;
+    s.tile = (int)(u / KB);
+    s.kb0 = (int)(u - (long long)s.tile * KB);
+    s.kb1 = (int)std::min((long long)KB, s.kb0 + (u1 - u));
+    u += s.kb1 - s.kb0;
+    return true;
+}
+
+__device__ __forceinline__ float silu_tc(float z) { return z / (1.0f + expf(-z)); }
+
+// One chunk (32 sequences) of the fused epilogue for the tile's feature of
+// this thread (row r of the accumulator).
+template <int EPI>
+__device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const float (&v)[32], float *xch,
+                                  int *s_row, int r) {
+    const int j0 = chunk * 32;
+    if constexpr (EPI == TC_STORE || EPI == TC_ADD) {
+        const int m = tile * kTcBM + r;
+        if (m < p.M) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int j = j0 + i;
+                if (j < p.n) {
+                    float *dst = p.y + (long long)j * p.ldy + m;
+                    *dst = EPI == TC_ADD ? *dst + v[i] : v[i];
+                }
+            }
+        }
+        return;
+    } else {
+    // SILU and QKV exchange values between partner features through shared memory
+#pragma unroll
+    for (int i = 0; i < 32; ++i) xch[r * kTcXchStride + i] = v[i];
+    if (EPI == TC_QKV && r < 32) {  // cache rows of this chunk's sequences
+        const int j = j0 + r;
+        int row = -1;
+        if (j < p.n) {
+            const int pos = __ldcg(p.pos + j);
+            const int cap = p.max_blocks * p.block_tokens;
+            if (pos >= 0 && pos < cap && pos < p.rope_rows) {
+                const int b = pos / p.block_tokens;
+                const long long blk = p.block_table ? (long long)__ldcg(p.block_table + (long long)j * p.max_blocks + b)
+                                                    : (long long)j * p.max_blocks + b;
+                const long long rr = blk * p.block_tokens + pos % p.block_tokens;
+                if (blk >= 0 && rr < p.cache_rows) row = (int)rr;
+            }
+            if (row < 0 && tile == 0) flag_error(p.err, DS_ERR_POSITION);
+            s_row[32 + r] = pos;
+        }
+        s_row[r] = row;
+    }
+    named_sync(1, kTcEpiThreads);
+    if constexpr (EPI == TC_SILU) {
+        const int g = tile * (kTcBM / 2) + r;
+        if (r < kTcBM / 2 && g < p.M) {
+#pragma unroll 8
+            for (int i = 0; i < 32; ++i) {
+                const int j = j0 + i;
+                if (j < p.n) {
+                    const float gate = xch[r * kTcXchStride + i], up = xch[(r + kTcBM / 2) * kTcXchStride + i];
+                    p.yb[(long long)j * p.ldy + g] = __float2bfloat16_rn(silu_tc(gate) * up);
+                }
+            }
+        }
+    } else {
+        const int m = tile * kTcBM + r;
+        const int total = p.nq_cols + 2 * p.nkv_cols;
+        if (m < total) {
+            const bool rot = m < p.nq_cols + p.nkv_cols;
+            const int hd = p.head_dim, half = hd >> 1;
+            const int ih = (m < p.nq_cols ? m : m - p.nq_cols) % hd;
+            int pair = 0, partner = r;
+            bool first = true;
+            if (rot) {
+                if (p.rope_layout == DS_ROPE_HALF_SPLIT) {
+                    first = ih < half;
+                    pair = first ? ih : ih - half;
+                    partner = first ? r + half : r - half;
+                } else {
+                    first = (ih & 1) == 0;
+                    pair = ih >> 1;
+                    partner = r ^ 1;
+                }
+            }
+            for (int i = 0; i < 32; ++i) {
+                const int j = j0 + i;
+                if (j >= p.n) break;
+                float out = xch[r * kTcXchStride + i];
+                const int row = s_row[i];
+                if (rot) {
+                    const int pos = s_row[32 + i];
+                    float c = 1.0f, sn = 0.0f;
+                    if (pos >= 0 && pos < p.rope_rows) {
+                        c = p.rope_cos[(long long)pos * half + pair];
+                        sn = p.rope_sin[(long long)pos * half + pair];
+                    }
+                    const float o = xch[partner * kTcXchStride + i];
+                    out = first ? out * c - o * sn : o * sn + out * c;
+                }
+                if (m < p.nq_cols) {
+                    p.y[(long long)j * p.ldy + m] = out;
+                } else if (row >= 0) {
+                    const int kv = m - p.nq_cols;
+                    if (kv < p.nkv_cols)
+                        store_as(p.k_cache, (long long)row * p.nkv_cols + kv, p.kv_dtype, out);
+                    else
+                        store_as(p.v_cache, (long long)row * p.nkv_cols + kv - p.nkv_cols, p.kv_dtype, out);
+                }
+            }
+        }
+    }
+    named_sync(1, kTcEpiThreads);
+    }
+}
+
+template <int A_MN, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the swizzled stages
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int stages = p.stages;
+    const int b_bytes = p.n_pad * kTcBK * 2;
+    const int stage_bytes = kTcABytes + b_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
+    uint64_t *empty = full + kTcMaxStages;
+    uint64_t *acc_full = empty + kTcMaxStages;   // [2]
+    uint64_t *acc_empty = acc_full + 2;          // [2]
+    uint64_t *mma_done = acc_empty + 2;          // [1]
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(mma_done + 1);
+    int *s_flags = reinterpret_cast<int *>(s_tmem + 1);  // [0] abort, [1] last-arriver broadcast
+    int *s_row = s_flags + 2;                             // [64]
+    int *s_ok = s_row + 64;                               // [2][4]
+    float *xch = reinterpret_cast<float *>(s_ok + 8);     // [128][33]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KB = (p.K + kTcBK - 1) / kTcBK;
+    const int T = p.m_tiles;
+    const long long W = (long long)T * KB;
+    const int G = gridDim.x;
+    const long long u0 = W * blockIdx.x / G, u1 = W * (blockIdx.x + 1) / G;
+    volatile int *abort_flag = s_flags;
+    const uint32_t tmem_cols = (uint32_t)p.tmem_cols;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(mma_done, 1);
+        s_flags[0] = 0;
+        s_flags[1] = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    allow_dependent_launch();
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            // prologue: the first stages' weight boxes go out before the
+            // previous kernel's output is awaited
+            long long u = u0;
+            int pre = (int)std::min<long long>(stages, u1 - u0);
+            auto issue_a = [&](int s, long long unit) {
+                const int tile = (int)(unit / KB), kb = (int)(unit - (long long)tile * KB);
+                unsigned char *sa = smem + (size_t)s * stage_bytes;
+                if (A_MN) {
+                    if (EPI == TC_SILU) {
+                        tma_box_g2s(sa, &p.ta0, tile * (kTcBM / 2), kb * kTcBK, &full[s], pol);
+                        tma_box_g2s(sa + kTcABytes / 2, &p.ta1, tile * (kTcBM / 2), kb * kTcBK, &full[s], pol);
+                    } else {
+                        tma_box_g2s(sa, &p.ta0, tile * kTcBM, kb * kTcBK, &full[s], pol);
+                        tma_box_g2s(sa + kTcABytes / 2, &p.ta0, tile * kTcBM + kTcBM / 2, kb * kTcBK, &full[s], pol);
+                    }
+                } else {
+                    tma_box_g2s(sa, &p.ta0, kb * kTcBK, tile * kTcBM, &full[s], pol);
+                }
+            };
+            auto issue_b = [&](int s, long long unit) {
+                const int tile = (int)(unit / KB), kb = (int)(unit - (long long)tile * KB);
+                (void)tile;
+                tma_box_g2s_nohint(smem + (size_t)s * stage_bytes + kTcABytes, &p.tb, kb * kTcBK, 0, &full[s]);
+            };
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
+                issue_a(i, u0 + i);
+            }
+            grid_dependency_wait();
+            for (int i = 0; i < pre; ++i) issue_b(i, u0 + i);
+            uint32_t fill = (uint32_t)pre;
+            bool ok = true;
+            for (u = u0 + pre; u < u1; ++u, ++fill) {
+                const int s = fill % stages;
+                const uint32_t use = fill / stages;
+                if (!tc_wait(&empty[s], (use - 1) & 1, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+                issue_a(s, u);
+                issue_b(s, u);
+            }
+            // every copy issued has landed before the CTA may exit
+            const uint32_t first = fill > (uint32_t)stages ? fill - stages : 0;
+            for (uint32_t f = first; f < fill; ++f) {
+                int dummy = 0;
+                if (!mbar_wait(&full[f % stages], (f / stages) & 1, ok ? p.err : &dummy)) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            grid_dependency_wait();
+            const uint32_t idesc = tc_idesc(A_MN, p.n_pad);
+            uint32_t fill = 0;
+            int seg_i = 0;
+            long long u = u0;
+            TcSeg sg;
+            bool ok = true;
+            while (ok && tc_next_seg(u, u1, KB, sg)) {
+                const int buf = seg_i & 1;
+                if (seg_i >= 2 && !tc_wait(&acc_empty[buf], ((seg_i >> 1) - 1) & 1, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * p.n_pad);
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++fill) {
+                    const int s = fill % stages;
+                    if (!tc_wait(&full[s], (fill / stages) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+                    const uint32_t sb = sa + kTcABytes;
+#pragma unroll
+                    for (int k = 0; k < kTcBK / 16; ++k) {
+                        const uint64_t ad = A_MN ? smem_desc(sa + k * 2048, kTcABytes / 2, 1024)
+                                                 : smem_desc(sa + k * 32, 16, 1024);
+                        const uint64_t bd = smem_desc(sb + k * 32, 16, 1024);
+                        tc_mma(d_tmem, ad, bd, idesc, (kb > sg.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[s]);
+                }
+                if (!ok) break;
+                tc_commit(&acc_full[buf]);
+                ++seg_i;
+            }
+            // nothing of ours may still be running on the tensor cores at exit
+            tc_commit(mma_done);
+            int dummy = 0;
+            mbar_wait(mma_done, 0, ok ? p.err : &dummy);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        grid_dependency_wait();
+        const int q = warp & 3;
+        const int r = q * 32 + lane;  // accumulator lane = feature row of the tile
+        const int et = threadIdx.x - 64;
+        long long u = u0;
+        int seg_i = 0;
+        TcSeg sg;
+        const int n_chunks = p.n_pad / 32;
+        while (tc_next_seg(u, u1, KB, sg)) {
+            const int buf = seg_i & 1;
+            // the four warps agree on whether the accumulator arrived, so none
+            // of them can be left alone at a named barrier
+            bool ok = __all_sync(0xffffffffu, tc_wait(&acc_full[buf], (seg_i >> 1) & 1, abort_flag, p.err));
+            if (lane == 0) s_ok[(seg_i & 1) * 4 + q] = ok ? 1 : 0;
+            named_sync(1, kTcEpiThreads);
+            ok = s_ok[(seg_i & 1) * 4 + 0] && s_ok[(seg_i & 1) * 4 + 1] && s_ok[(seg_i & 1) * 4 + 2] &&
+                 s_ok[(seg_i & 1) * 4 + 3];
+            tc_fence_after();
+            const bool whole = sg.kb0 == 0 && sg.kb1 == KB;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.n_pad);
+            if (!ok) break;
+            if (whole) {
+                for (int c = 0; c < n_chunks; ++c) {
+                    float v[32];
+                    tmem_ld32(tbase + c * 32, v);
+                    if (c == n_chunks - 1) {  // the buffer may be reused once every lane has read it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                    }
+                    tc_epilogue_chunk<EPI>(p, sg.tile, c, v, xch, s_row, r);
+                }
+            } else {
+                // partial accumulator to this (CTA, tile) slot, feature-fastest
+                float *slot = p.partials + ((size_t)blockIdx.x + sg.tile) * kTcBM * p.n_pad;
+                for (int c = 0; c < n_chunks; ++c) {
+                    float v[32];
+                    tmem_ld32(tbase + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) slot[(size_t)(c * 32 + i) * kTcBM + r] = v[i];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                // contributors of this tile: the CTAs holding its first and last unit
+                const long long tu0 = (long long)sg.tile * KB, tu1 = tu0 + KB - 1;
+                const int c_first = (int)(((tu0 + 1) * G - 1) / W);
+                const int c_last = (int)(((tu1 + 1) * G - 1) / W);
+                __threadfence();
+                named_sync(1, kTcEpiThreads);
+                if (et == 0) {
+                    const int prev = atomicAdd(p.counters + sg.tile, 1);
+                    const bool last = prev == c_last - c_first;
+                    if (last) p.counters[sg.tile] = 0;  // ready for the next launch
+                    s_flags[1] = last ? 1 : 0;
+                }
+                named_sync(1, kTcEpiThreads);
+                if (s_flags[1]) {
+                    __threadfence();
+                    for (int c = 0; c < n_chunks; ++c) {
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                        for (int cc = c_first; cc <= c_last; ++cc) {
+                            const float *src = p.partials + ((size_t)cc + sg.tile) * kTcBM * p.n_pad;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] += __ldcg(src + (size_t)(c * 32 + i) * kTcBM + r);
+                        }
+                        tc_epilogue_chunk<EPI>(p, sg.tile, c, v, xch, s_row, r);
+                    }
+                }
+                named_sync(1, kTcEpiThreads);
+            }
+            ++seg_i;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, tmem_cols);
+}
+
+// ---------------------------------------------------------------- host
+// The MMA's N: the vector count rounded up to whole 32-column chunks of the
+// accumulator (the epilogue reads 32 columns at a time).
+int tc_n_pad(int n) { return std::max(32, (n + 31) / 32 * 32); }
+
+int tc_stages(int n_pad) {
+    const size_t stage = (size_t)kTcABytes + (size_t)n_pad * kTcBK * 2;
+    const size_t fixed = 1024 + 256 + 72 * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
+    int s = (int)((kTcSmemLimit - fixed) / stage);
+    return std::min(s, kTcMaxStages);
+}
+
+size_t tc_smem_bytes(int n_pad, int stages) {
+    const size_t stage = (size_t)kTcABytes + (size_t)n_pad * kTcBK * 2;
+    return 1024 + (size_t)stages * stage + 256 + 72 * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
+}
+
+int tc_m_tiles(int M, int epi) { return epi == TC_SILU ? (M + kTcBM / 2 - 1) / (kTcBM / 2) : (M + kTcBM - 1) / kTcBM; }
+
+int tc_grid(int m_tiles, int K) {
+    const long long W = (long long)m_tiles * ((K + kTcBK - 1) / kTcBK);
+    return (int)std::min<long long>(sm_count(), W);
+}
+
+size_t tc_partial_floats(int m_tiles, int n_pad) {
+    return (size_t)(sm_count() + m_tiles) * kTcBM * n_pad;
+}
+
+bool tc_make_maps(TcArgs &a, const void *A0, const void *A1, long long a_row_stride, const void *X) {
+    if (a.a_mn) {
+        // [K][M] (M contiguous): boxes of 64 features x 64 rows
+        if (!encode_tiled_2d(&a.ta0, A0, DS_BF16, a.M, a.K, a_row_stride, 64, kTcBK, true)) return false;
+        if (A1 && !encode_tiled_2d(&a.ta1, A1, DS_BF16, a.M, a.K, a_row_stride, 64, kTcBK, true)) return false;
+    } else {
+        // [M][K] (K contiguous): boxes of 64 columns x 128 rows
+        if (!encode_tiled_2d(&a.ta0, A0, DS_BF16, a.K, a.M, a_row_stride, kTcBK, kTcBM, true)) return false;
+    }
+    return encode_tiled_2d(&a.tb, X, DS_BF16, a.K, a.n, (long long)a.K * 2, kTcBK, a.n_pad, true);
+}
+
+template <int A_MN, int EPI>
+static cudaError_t launch_tc_t(const TcArgs &a, int grid, cudaStream_t stream, bool pdl) {
+    const size_t smem = tc_smem_bytes(a.n_pad, a.stages);
+    if (smem > kTcSmemLimit) return cudaErrorInvalidValue;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kTcSmemLimit);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    return launch_ex(tc_gemm_kernel<A_MN, EPI>, dim3(grid), dim3(kTcThreads), smem, stream, pdl, a);
+}
+
+cudaError_t launch_tc_gemm(const TcArgs &a, int grid, cudaStream_t stream, bool pdl) {
+    if (a.n_pad < 32 || a.n_pad > 256 || a.n_pad % 32 || a.stages < 2 || a.stages > kTcMaxStages) return cudaErrorInvalidValue;
+    if (a.a_mn) {
+        switch (a.epi) {
+            case TC_STORE: return launch_tc_t<1, TC_STORE>(a, grid, stream, pdl);
+            case TC_ADD: return launch_tc_t<1, TC_ADD>(a, grid, stream, pdl);
+            case TC_SILU: return launch_tc_t<1, TC_SILU>(a, grid, stream, pdl);
+            case TC_QKV: return launch_tc_t<1, TC_QKV>(a, grid, stream, pdl);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    if (a.epi == TC_STORE) return launch_tc_t<0, TC_STORE>(a, grid, stream, pdl);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t prepare_tc_kernels() {
+    const void *fns[] = {(const void *)tc_gemm_kernel<1, TC_STORE>, (const void *)tc_gemm_kernel<1, TC_ADD>,
+                         (const void *)tc_gemm_kernel<1, TC_SILU>, (const void *)tc_gemm_kernel<1, TC_QKV>,
+                         (const void *)tc_gemm_kernel<0, TC_STORE>};
+    for (const void *f : fns) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemLimit);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace ds
+
+// =====================================================================
+// C ABI
+// =====================================================================
+using namespace ds;
+
+namespace {
+
+size_t tc_ws_bytes(int64_t n, int64_t M, int64_t K, int epi) {
+    const int n_pad = tc_n_pad((int)n);
+    const int T = tc_m_tiles((int)M, epi);
+    (void)K;
+    return kWsHeader + align_up((size_t)T * 4, 256) + tc_partial_floats(T, n_pad) * 4;
+}
+
+int tc_check(const void *A, int64_t a_len, const void *X, int64_t x_len, int64_t n, int64_t rows, int64_t cols,
+             const float *Y, int64_t y_len, int64_t y_need, int64_t K) {
+    if (n < 1 || rows < 1 || cols < 1) return DS_EMPTY_DIMENSION;
+    if (rows > DS_MAX_DIM || cols > DS_MAX_DIM) return DS_DIMENSION_TOO_LARGE;
+    if (n > 256) return DS_DIMENSION_TOO_LARGE;
+    if (a_len != rows * cols) return DS_GEMV_A_LENGTH_MISMATCH;
+    if (x_len != n * K) return DS_GEMV_X_LENGTH_MISMATCH;
+    if (y_len != y_need) return DS_A_LENGTH_MISMATCH;
+    if (!A || !X || !Y) return DS_BAD_ARGUMENT;
+    if (((uintptr_t)A | (uintptr_t)X) & 15) return DS_BAD_ARGUMENT;
+    if ((cols * 2) % 16) return DS_BAD_ARGUMENT;  // row strides of both operands: whole 16-byte units
+    if ((K * 2) % 16) return DS_BAD_ARGUMENT;
+    return DS_OK;
+}
+
+int tc_run(const void *A, const void *X, int64_t n, int64_t M, int64_t K, int a_mn, long long a_row_stride, float *Y,
+           void *ws, size_t ws_bytes, cudaStream_t s) {
+    TcArgs a = {};
+    a.a_mn = a_mn;
+    a.M = (int)M;
+    a.K = (int)K;
+    a.n = (int)n;
+    a.n_pad = tc_n_pad((int)n);
+    a.epi = TC_STORE;
+    a.m_tiles = tc_m_tiles(a.M, a.epi);
+    a.stages = tc_stages(a.n_pad);
+    a.tmem_cols = 32;
+    while (a.tmem_cols < 2 * a.n_pad) a.tmem_cols *= 2;
+    a.y = Y;
+    a.ldy = (int)M;
+    if (!ws || ws_bytes < tc_ws_bytes(n, M, K, a.epi)) return DS_WORKSPACE_TOO_SMALL;
+    char *w = static_cast<char *>(ws);
+    a.err = reinterpret_cast<int *>(w);
+    a.counters = reinterpret_cast<int *>(w + kWsHeader);
+    a.partials = reinterpret_cast<float *>(w + kWsHeader + align_up((size_t)a.m_tiles * 4, 256));
+    if (!tc_make_maps(a, A, nullptr, a_row_stride, X)) return DS_CUDA_ERROR;
+    const int grid = tc_grid(a.m_tiles, a.K);
+    return launch_tc_gemm(a, grid, s, false) == cudaSuccess ? DS_OK : DS_CUDA_ERROR;
+}
+
+}  // namespace
+
+extern "C" DS_API size_t ds_gemm_workspace_bytes(int64_t n, int64_t rows, int64_t cols) {
+    if (n < 1 || n > 256 || rows < 1 || cols < 1) return 0;
+    // the larger of the two orientations' needs
+    return std::max(tc_ws_bytes(n, cols, rows, TC_STORE), tc_ws_bytes(n, rows, cols, TC_STORE));
+}
+
+extern "C" DS_API int ds_gemm_transposed(const void *A, int64_t a_len, const void *X, int64_t x_len, int64_t n,
+                                         int64_t rows, int64_t cols, float *Y, int64_t y_len, void *workspace,
+                                         size_t workspace_bytes, ds_stream_t stream) {
+    int st = tc_check(A, a_len, X, x_len, n, rows, cols, Y, y_len, n * cols, rows);
+    if (st != DS_OK) return st;
+    return tc_run(A, X, n, cols, rows, 1, cols * 2, Y, workspace, workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" DS_API int ds_gemm(const void *W, int64_t w_len, const void *X, int64_t x_len, int64_t n, int64_t rows,
+                              int64_t cols, float *Y, int64_t y_len, void *workspace, size_t workspace_bytes,
+                              ds_stream_t stream) {
+    int st = tc_check(W, w_len, X, x_len, n, rows, cols, Y, y_len, n * rows, cols);
+    if (st != DS_OK) return st;
+    return tc_run(W, X, n, rows, cols, 0, cols * 2, Y, workspace, workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
+}

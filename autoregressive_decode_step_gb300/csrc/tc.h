@@ -1,0 +1,56 @@
+// Internal interface of the tensor-core (tcgen05) batched projections.
+#pragma once
+
+#include "internal.h"
+
+#include <cuda_bf16.h>
+
+namespace ds {
+
+// Encode a 2-D tensor map over a row-major matrix of `rows` rows of `cols`
+// elements (dtype DS_F32 / DS_BF16) with rows `row_stride` bytes apart, boxes
+// of box_cols x box_rows elements, 128-byte swizzled or not.  False if the
+// driver refuses.
+bool encode_tiled_2d(CUtensorMap *map, const void *base, int dtype, long long cols, long long rows,
+                     long long row_stride, int box_cols, int box_rows, bool swizzle128);
+
+// Fused epilogues of the batched projection kernel.
+enum { TC_STORE = 0, TC_ADD = 1, TC_SILU = 2, TC_QKV = 3 };
+
+struct TcArgs {
+    CUtensorMap ta0;  // weights: [K][M] boxes {64 features, 64 rows} (a_mn) or [M][K] boxes {64, 128}
+    CUtensorMap ta1;  // TC_SILU: the up columns' map (ta0 holds the gate columns)
+    CUtensorMap tb;   // activations [n][K] bf16, boxes {64, n_pad}
+    int a_mn;         // 1: weights [K][M], M contiguous; 0: [M][K], K contiguous
+    int M, K, n, n_pad;
+    int epi, m_tiles, stages, tmem_cols;
+    float *y;             // TC_STORE / TC_ADD: y[s * ldy + m]; TC_QKV: q [n][ldy]
+    __nv_bfloat16 *yb;    // TC_SILU: silu(gate) * up as bf16, yb[s * ldy + g]
+    int ldy;
+    // TC_QKV: RoPE on the q and k columns, K/V written at each sequence's pos
+    const int *pos;
+    const int *block_table;
+    int max_blocks, block_tokens;
+    long long cache_rows;
+    const float *rope_cos, *rope_sin;
+    int rope_rows;
+    int nq_cols, nkv_cols, head_dim, rope_layout;
+    void *k_cache, *v_cache;
+    int kv_dtype;
+    // split tiles: partial accumulators and arrival counters (zero between launches)
+    float *partials;
+    int *counters;
+    int *err;
+};
+
+int tc_n_pad(int n);
+int tc_stages(int n_pad);
+int tc_m_tiles(int M, int epi);
+int tc_grid(int m_tiles, int K);
+size_t tc_partial_floats(int m_tiles, int n_pad);
+// Encode a.ta0 (and a.ta1 from A1 when set) and a.tb.
+bool tc_make_maps(TcArgs &a, const void *A0, const void *A1, long long a_row_stride, const void *X);
+cudaError_t launch_tc_gemm(const TcArgs &a, int grid, cudaStream_t stream, bool pdl);
+cudaError_t prepare_tc_kernels();
+
+}  // namespace ds

@@ -160,6 +160,39 @@ DS_API int ds_gemv(const void *W, int64_t w_len, int w_dtype, const float *x, in
                    int64_t rows, int64_t cols, float *y, int64_t y_len, ds_stream_t stream);
 
 /* ---------------------------------------------------------------------
+ * Batched projections (tensor cores)
+ *
+ * When one step decodes n sequences ("Inside the engine", section 4:
+ * batched decode, one token per sequence per step) each projection applies
+ * the same matrix to n activation vectors: a skinny GEMM, run on the tcgen05
+ * tensor cores with bf16 operands and fp32 accumulation.  n is 1..256.
+ * ------------------------------------------------------------------- */
+
+/* Workspace bytes ds_gemm_transposed / ds_gemm need for n vectors and a
+ * rows x cols matrix (either orientation); 0 for an unsupported shape. */
+DS_API size_t ds_gemm_workspace_bytes(int64_t n, int64_t rows, int64_t cols);
+
+/* Y[s][j] = sum_i A[i * cols + j] * X[s * rows + i] for s < n, j < cols:
+ * ds_gemv_transposed's y = A^T x ("LLM inference kernels", "A parallel path
+ * for one frozen kernel's known-slow shape") for the n rows of X at once.
+ *   A: bf16 rows*cols (a_len, else 569); X: bf16 n*rows (x_len, else 570);
+ *   Y: fp32 n*cols (y_len, else 562).  rows and cols multiples of 8, A and X
+ *   16-byte aligned (577).  561 / 564 for an empty / oversized dimension
+ *   (n > 256 included).  workspace: ds_gemm_workspace_bytes(n, rows, cols)
+ *   bytes, zeroed before first use. */
+DS_API int ds_gemm_transposed(const void *A, int64_t a_len, const void *X, int64_t x_len, int64_t n,
+                              int64_t rows, int64_t cols, float *Y, int64_t y_len, void *workspace,
+                              size_t workspace_bytes, ds_stream_t stream);
+
+/* Y[s][r] = sum_c W[r * cols + c] * X[s * cols + c] for s < n, r < rows: the
+ * untransposed form of the output head (ds_gemv) for n vectors.
+ *   W: bf16 rows*cols (569); X: bf16 n*cols (570); Y: fp32 n*rows (562);
+ *   cols a multiple of 8; other checks as ds_gemm_transposed. */
+DS_API int ds_gemm(const void *W, int64_t w_len, const void *X, int64_t x_len, int64_t n, int64_t rows,
+                   int64_t cols, float *Y, int64_t y_len, void *workspace, size_t workspace_bytes,
+                   ds_stream_t stream);
+
+/* ---------------------------------------------------------------------
  * Decode glue
  * ------------------------------------------------------------------- */
 

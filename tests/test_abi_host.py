@@ -146,3 +146,27 @@ def test_model_config_validation(abi):
     out = ctypes.c_void_p()
     m = mc(C.TOY)
     assert abi.lib.ds_model_create(ctypes.byref(m), None, None, 0, ctypes.byref(out)) == abi.DS_BAD_ARGUMENT
+
+
+def test_batched_projection_refusals(abi):
+    L = abi.lib
+    f = L.ds_gemm_transposed
+    # rows 64, cols 128, n 4
+    assert f(FAKE, 64 * 128, FAKE, 4 * 64, 0, 64, 128, FAKE, 0, FAKE, 1 << 24, None) == abi.DS_EMPTY_DIMENSION
+    assert f(FAKE, 64 * 128, FAKE, 257 * 64, 257, 64, 128, FAKE, 257 * 128, FAKE, 1 << 24, None) == \
+        abi.DS_DIMENSION_TOO_LARGE
+    assert f(FAKE, 64 * 127, FAKE, 4 * 64, 4, 64, 128, FAKE, 4 * 128, FAKE, 1 << 24, None) == \
+        abi.DS_GEMV_A_LENGTH_MISMATCH
+    assert f(FAKE, 64 * 128, FAKE, 4 * 63, 4, 64, 128, FAKE, 4 * 128, FAKE, 1 << 24, None) == \
+        abi.DS_GEMV_X_LENGTH_MISMATCH
+    assert f(FAKE, 64 * 128, FAKE, 4 * 64, 4, 64, 128, FAKE, 4 * 127, FAKE, 1 << 24, None) == \
+        abi.DS_A_LENGTH_MISMATCH
+    # cols not a whole number of 16-byte units of bf16
+    assert f(FAKE, 64 * 100, FAKE, 4 * 64, 4, 64, 100, FAKE, 4 * 100, FAKE, 1 << 24, None) == abi.DS_BAD_ARGUMENT
+    g = L.ds_gemm
+    assert g(FAKE, 1000 * 512, FAKE, 5 * 512, 5, 1000, 512, FAKE, 5 * 999, FAKE, 1 << 24, None) == \
+        abi.DS_A_LENGTH_MISMATCH
+    assert g(FAKE, 1000 * 512, FAKE, 5 * 1000, 5, 1000, 512, FAKE, 5 * 1000, FAKE, 1 << 24, None) == \
+        abi.DS_GEMV_X_LENGTH_MISMATCH
+    assert L.ds_gemm_workspace_bytes(0, 64, 64) == 0
+    assert L.ds_gemm_workspace_bytes(257, 64, 64) == 0
