@@ -242,8 +242,22 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const __grid_co
             A = fmaf(a, sm[sp * GQ + j], A);
             A2 = fmaf(a2, sm[sp * GQ + j2], A2);
         }
-        p.out[((long long)seq * p.n_qh + g * GQ + j) * hd + idx % hd] = A / sM[GQ + j];
-        if (two) p.out[((long long)seq * p.n_qh + g * GQ + j2) * hd + idx2 % hd] = A2 / sM[GQ + j2];
+        const long long o1 = ((long long)seq * p.n_qh + g * GQ + j) * hd + idx % hd;
+        const long long o2 = ((long long)seq * p.n_qh + g * GQ + j2) * hd + idx2 % hd;
+        const float r1 = A / sM[GQ + j], r2 = A2 / sM[GQ + j2];
+        p.out[o1] = r1;
+        if (two) p.out[o2] = r2;
+        if (p.out_bf16) {  // hi + lo pair: r = hi + lo to 16 significant bits
+            __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(p.out_bf16);
+            const __nv_bfloat16 h1 = __float2bfloat16_rn(r1);
+            ob[o1] = h1;
+            if (p.out_bf16_lo) ob[o1 + p.out_bf16_lo] = __float2bfloat16_rn(r1 - __bfloat162float(h1));
+            if (two) {
+                const __nv_bfloat16 h2 = __float2bfloat16_rn(r2);
+                ob[o2] = h2;
+                if (p.out_bf16_lo) ob[o2 + p.out_bf16_lo] = __float2bfloat16_rn(r2 - __bfloat162float(h2));
+            }
+        }
     }
 }
 

@@ -93,6 +93,44 @@ __global__ void kv_append_kernel(void *cache, int dtype, long long cache_len, co
         store_as(cache, cache_len + i, dtype, nv[i]);
 }
 
+// h[s][:] = x[s][:] * (mean(x[s]^2) + eps)^-1/2 * w, square sum in fp32
+// ("The forward pass end to end", "The code": rmsnorm), one CTA per row: the
+// normalised input of a batched projection, written for the tensor cores as
+// the bf16 pair hi (at h) + lo (lo_off elements further; 0: hi only).
+__global__ void rmsnorm_rows_bf16_kernel(const float *x, const float *w, float eps, __nv_bfloat16 *h, int d,
+                                         long long lo_off) {
+    __shared__ float red[32];
+    __shared__ float s_scale;
+    allow_dependent_launch();
+    grid_dependency_wait();
+    const float *xr = x + (long long)blockIdx.x * d;
+    float ss = 0.0f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.0f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+        s_scale = 1.0f / sqrtf(tot / (float)d + eps);
+    }
+    __syncthreads();
+    const float sc = s_scale;
+    __nv_bfloat16 *hr = h + (long long)blockIdx.x * d;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        const float v = xr[i] * sc * w[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        hr[i] = hi;
+        if (lo_off) hr[i + lo_off] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    }
+}
+
+cudaError_t launch_rmsnorm_rows_bf16(const float *x, const float *w, float eps, void *h, long long lo_off,
+                                     int n_rows, int d, cudaStream_t stream, bool pdl) {
+    return launch_ex(rmsnorm_rows_bf16_kernel, dim3(n_rows), dim3(256), 0, stream, pdl, x, w, eps,
+                     static_cast<__nv_bfloat16 *>(h), d, lo_off);
+}
+
 // x[s][:] = emb[tokens[s]][:] widened to fp32; a token outside [0, vocab)
 // is clamped and flagged.  grid.y = sequence.
 template <typename WT>

@@ -8,8 +8,12 @@
 // goes on the MMA's M side (128 output features per tile) and the n <= 256
 // activation rows on its N side, so one weight byte is fetched once for all n
 // sequences and the accumulator (128 lanes x n columns of fp32) lives in
-// tensor memory.  Operands are bf16 (activations are rounded to bf16 when
-// they are written for this kernel), accumulation fp32.
+// tensor memory.  Operands are bf16, accumulation fp32.  Inside the decode
+// step an fp32 activation v reaches this kernel as a bf16 pair (hi, lo) with
+// hi + lo = v to 16 significant bits; both rows are multiplied into the same
+// accumulator (two MMAs per k-step), so the product is that of the fp32
+// activation, not of a bf16 rounding of it.  The path is bound by the weight
+// stream, so the second MMA costs nothing measurable.
 //
 // Roles (192 threads, one CTA per SM):
 //   warp 0, one thread: TMA producer.  Per 64-row k-block it loads the weight
@@ -210,7 +214,16 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
                 const int j = j0 + i;
                 if (j < p.n) {
                     const float gate = xch[r * kTcXchStride + i], up = xch[(r + kTcBM / 2) * kTcXchStride + i];
-                    p.yb[(long long)j * p.ldy + g] = __float2bfloat16_rn(silu_tc(gate) * up);
+                    const float f = silu_tc(gate) * up;
+                    const long long o = (long long)j * p.ldy + g;
+                    if (p.yb_lo) {
+                        __nv_bfloat16 hi, lo;
+                        split_bf16(f, hi, lo);
+                        p.yb[o] = hi;
+                        p.yb[o + p.yb_lo] = lo;
+                    } else {
+                        p.yb[o] = __float2bfloat16_rn(f);
+                    }
                 }
             }
         }
@@ -272,8 +285,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int stages = p.stages;
-    const int b_bytes = p.n_pad * kTcBK * 2;
-    const int stage_bytes = kTcABytes + b_bytes;
+    const int b_bytes = p.n_pad * kTcBK * 2;  // one activation tile (the hi part when split)
+    const int stage_bytes = kTcABytes + b_bytes * (p.split ? 2 : 1);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
     uint64_t *empty = full + kTcMaxStages;
     uint64_t *acc_full = empty + kTcMaxStages;   // [2]
@@ -344,7 +357,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             auto issue_b = [&](int s, long long unit) {
                 const int tile = (int)(unit / KB), kb = (int)(unit - (long long)tile * KB);
                 (void)tile;
-                tma_box_g2s_nohint(smem + (size_t)s * stage_bytes + kTcABytes, &p.tb, kb * kTcBK, 0, &full[s]);
+                unsigned char *sb = smem + (size_t)s * stage_bytes + kTcABytes;
+                tma_box_g2s_nohint(sb, &p.tb, kb * kTcBK, 0, &full[s]);
+                if (p.split) tma_box_g2s_nohint(sb + b_bytes, &p.tb, kb * kTcBK, p.b_lo_row, &full[s]);
             };
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
@@ -405,6 +420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                                                  : smem_desc(sa + k * 32, 16, 1024);
                         const uint64_t bd = smem_desc(sb + k * 32, 16, 1024);
                         tc_mma(d_tmem, ad, bd, idesc, (kb > sg.kb0 || k > 0) ? 1u : 0u);
+                        if (p.split) tc_mma(d_tmem, ad, smem_desc(sb + b_bytes + k * 32, 16, 1024), idesc, 1u);
                     }
                     tc_commit(&empty[s]);
                 }
@@ -507,15 +523,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 // accumulator (the epilogue reads 32 columns at a time).
 int tc_n_pad(int n) { return std::max(32, (n + 31) / 32 * 32); }
 
-int tc_stages(int n_pad) {
-    const size_t stage = (size_t)kTcABytes + (size_t)n_pad * kTcBK * 2;
+int tc_stages(int n_pad, int split) {
+    const size_t stage = (size_t)kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
     const size_t fixed = 1024 + 256 + 72 * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
     int s = (int)((kTcSmemLimit - fixed) / stage);
     return std::min(s, kTcMaxStages);
 }
 
-size_t tc_smem_bytes(int n_pad, int stages) {
-    const size_t stage = (size_t)kTcABytes + (size_t)n_pad * kTcBK * 2;
+size_t tc_smem_bytes(int n_pad, int split, int stages) {
+    const size_t stage = (size_t)kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
     return 1024 + (size_t)stages * stage + 256 + 72 * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
 }
 
@@ -539,25 +555,26 @@ bool tc_make_maps(TcArgs &a, const void *A0, const void *A1, long long a_row_str
         // [M][K] (K contiguous): boxes of 64 columns x 128 rows
         if (!encode_tiled_2d(&a.ta0, A0, DS_BF16, a.K, a.M, a_row_stride, kTcBK, kTcBM, true)) return false;
     }
-    return encode_tiled_2d(&a.tb, X, DS_BF16, a.K, a.n, (long long)a.K * 2, kTcBK, a.n_pad, true);
+    // split: hi rows [0, n) then lo rows [b_lo_row, b_lo_row + n)
+    const long long x_rows = a.split ? (long long)a.b_lo_row + a.n : a.n;
+    return encode_tiled_2d(&a.tb, X, DS_BF16, a.K, x_rows, (long long)a.K * 2, kTcBK, a.n_pad, true);
 }
 
 template <int A_MN, int EPI>
 static cudaError_t launch_tc_t(const TcArgs &a, int grid, cudaStream_t stream, bool pdl) {
-    const size_t smem = tc_smem_bytes(a.n_pad, a.stages);
+    const size_t smem = tc_smem_bytes(a.n_pad, a.split, a.stages);
     if (smem > kTcSmemLimit) return cudaErrorInvalidValue;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kTcSmemLimit);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
     return launch_ex(tc_gemm_kernel<A_MN, EPI>, dim3(grid), dim3(kTcThreads), smem, stream, pdl, a);
 }
 
+static bool g_tc_ready = false;
+
 cudaError_t launch_tc_gemm(const TcArgs &a, int grid, cudaStream_t stream, bool pdl) {
     if (a.n_pad < 32 || a.n_pad > 256 || a.n_pad % 32 || a.stages < 2 || a.stages > kTcMaxStages) return cudaErrorInvalidValue;
+    if (!g_tc_ready) {
+        cudaError_t e = prepare_tc_kernels();
+        if (e != cudaSuccess) return e;
+    }
     if (a.a_mn) {
         switch (a.epi) {
             case TC_STORE: return launch_tc_t<1, TC_STORE>(a, grid, stream, pdl);
@@ -579,6 +596,7 @@ cudaError_t prepare_tc_kernels() {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemLimit);
         if (e != cudaSuccess) return e;
     }
+    g_tc_ready = true;
     return cudaSuccess;
 }
 
@@ -623,7 +641,7 @@ int tc_run(const void *A, const void *X, int64_t n, int64_t M, int64_t K, int a_
     a.n_pad = tc_n_pad((int)n);
     a.epi = TC_STORE;
     a.m_tiles = tc_m_tiles(a.M, a.epi);
-    a.stages = tc_stages(a.n_pad);
+    a.stages = tc_stages(a.n_pad, 0);
     a.tmem_cols = 32;
     while (a.tmem_cols < 2 * a.n_pad) a.tmem_cols *= 2;
     a.y = Y;

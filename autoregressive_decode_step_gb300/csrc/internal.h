@@ -141,6 +141,8 @@ struct AttnArgs {
     int n_qh, n_kvh, hd;
     float scale;
     float *out;           // [n_seqs][n_qh * hd]
+    void *out_bf16;       // optional bf16 pair of out (the batched o projection's input): hi here,
+    long long out_bf16_lo; // lo this many elements further (0: hi only)
     float *partials;
     int *counters;        // n_seqs * n_kvh ints, zero between launches
     int *err;
@@ -155,6 +157,8 @@ cudaError_t launch_embed(const void *emb, int w_dtype, int vocab, int d, const i
                          float *x, int *err, int n_seqs, cudaStream_t stream, bool pdl);
 cudaError_t launch_rope_table(float *cos_t, float *sin_t, int rows, int head_dim, double base,
                               cudaStream_t stream);
+cudaError_t launch_rmsnorm_rows_bf16(const float *x, const float *w, float eps, void *h, long long lo_off,
+                                     int n_rows, int d, cudaStream_t stream, bool pdl);
 
 // ------------------------------------------------------------------ picking
 struct ArgmaxArgs {

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.h"
 
 namespace ds {
 cudaError_t prepare_kernels();
@@ -61,6 +62,12 @@ struct ds_model {
     // tagged activation words and partials of the step kernel
     unsigned long long *st_x, *st_q, *st_kv, *st_f, *st_ss, *st_part, *st_att;
     size_t st_part_stride;
+    // the batched step (max_seqs > 1): projections on the tensor cores
+    bool batched;
+    int b_splits;
+    void *h_bf, *att_bf, *f_bf;  // projection inputs as bf16 pairs: [2][max_seqs][d | nq | ff], hi then lo
+    int *b_am_counters;          // argmax arrival counters, one per sequence
+    std::vector<ds::TcArgs> tc;  // per layer: q|k|v, o, gate|up, down; then the head
 };
 
 struct ds_step_graph {
@@ -75,7 +82,8 @@ using namespace ds;
 struct Layout {
     size_t x, q, att, f, logits, rope_cos, rope_sin, g_counters, g_partials, a_counters, a_partials, am_val,
         am_idx, am_counter, step_layers, step_bar, phase_times, trace, st_x, st_q, st_kv, st_f, st_ss, st_part,
-        st_att, total;
+        st_att, h_bf, att_bf, f_bf, tc_counters, tc_partials, b_am_counters, total;
+    int b_splits, tc_tiles;
     size_t st_part_stride;
     int grid_qkv, grid_o, grid_gu, grid_d, grid_head, nb_qkv, nb_o, nb_gu, nb_d, attn_splits;
     bool step_ok;
@@ -104,7 +112,13 @@ int validate(const ds_model_config *c) {
     if (gemv_t_band_cols(es) % c->head_dim) return DS_BAD_ARGUMENT;
     if (!gemv_n_streamable(nullptr, c->vocab, c->d, es)) return DS_BAD_ARGUMENT;
     if (!(c->eps >= 0.0f) || !(c->rope_base > 0.0)) return DS_BAD_ARGUMENT;
-    if (c->max_seqs != 1) return DS_BAD_ARGUMENT;  // batch-1 path
+    if (c->max_seqs > 256) return DS_DIMENSION_TOO_LARGE;
+    if (c->max_seqs > 1) {
+        // the batched step runs its projections on bf16 tensor cores, with
+        // whole heads in every 128-feature tile
+        if (c->w_dtype != DS_BF16) return DS_BAD_DTYPE;
+        if (128 % c->head_dim) return DS_BAD_ARGUMENT;
+    }
     return DS_OK;
 }
 
@@ -140,6 +154,15 @@ Layout make_layout(const ds_model_config *c) {
         L.step_ok = L.step_stages >= 2;
     }
     L.n_phase_times = 5 * c->n_layer + 4;
+    // the batched step: attention splits of about 256 positions at the
+    // largest context; tensor-core tiles of the largest projection
+    const bool batched = S > 1;
+    L.b_splits = batched ? (int)std::min<long long>(kStMaxSplits, std::max<long long>(1, (c->max_ctx + 255) / 256)) : 0;
+    if (batched) {
+        const int nqkv = nq + 2 * nkv;
+        L.tc_tiles = std::max(std::max(tc_m_tiles(nqkv, TC_QKV), tc_m_tiles(c->d, TC_ADD)),
+                              std::max(tc_m_tiles(c->ff, TC_SILU), tc_m_tiles(c->vocab, TC_STORE)));
+    }
     size_t partial = 0;
     partial = std::max(partial, gemv_t_partial_floats(L.grid_qkv, L.nb_qkv, es));
     partial = std::max(partial, gemv_t_partial_floats(L.grid_o, L.nb_o, es));
@@ -160,9 +183,12 @@ Layout make_layout(const ds_model_config *c) {
     L.g_partials = carve(off, partial * 4);
     L.a_counters = carve(off, (size_t)S * c->n_kvh * 4);
     L.a_partials = carve(off, attention_partial_floats(S, c->n_qh, c->n_kvh, c->head_dim,
-                                                       std::max(L.attn_splits, L.step_splits)) * 4);
-    L.am_val = carve(off, (size_t)std::max(L.grid_head, L.step_grid) * 4);
-    L.am_idx = carve(off, (size_t)std::max(L.grid_head, L.step_grid) * 4);
+                                                       std::max(std::max(L.attn_splits, L.step_splits), L.b_splits)) *
+                                  4);
+    const size_t am_slots = std::max((size_t)std::max(L.grid_head, L.step_grid),
+                                     (size_t)S * argmax_blocks_per_row(c->vocab));
+    L.am_val = carve(off, am_slots * 4);
+    L.am_idx = carve(off, am_slots * 4);
     L.am_counter = carve(off, 4);
     L.step_layers = carve(off, (size_t)std::max(c->n_layer, 1) * step_layer_bytes());
     L.step_bar = carve(off, 32);  // arrival count (u64), epoch (u64), abort flag
@@ -179,6 +205,14 @@ Layout make_layout(const ds_model_config *c) {
         L.st_part_stride = (size_t)(L.step_grid + max_bands) * bc;
         L.st_part = carve(off, 4 * L.st_part_stride * 8);
         L.st_att = carve(off, (size_t)c->n_kvh * L.step_splits * gq * (c->head_dim + 2) * 8);
+    }
+    if (batched) {
+        L.h_bf = carve(off, (size_t)2 * S * c->d * 2);
+        L.att_bf = carve(off, (size_t)2 * S * nq * 2);
+        L.f_bf = carve(off, (size_t)2 * S * c->ff * 2);
+        L.tc_counters = carve(off, (size_t)L.tc_tiles * 4);
+        L.tc_partials = carve(off, tc_partial_floats(L.tc_tiles, tc_n_pad(S)) * 4);
+        L.b_am_counters = carve(off, (size_t)S * 4);
     }
     L.total = off;
     return L;
@@ -533,6 +567,74 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
     m->st_att = reinterpret_cast<unsigned long long *>(ws + L.st_att);
     m->st_part_stride = L.st_part_stride;
 
+    m->batched = cfg->max_seqs > 1;
+    m->b_splits = L.b_splits;
+    if (m->batched) {
+        m->h_bf = ws + L.h_bf;
+        m->att_bf = ws + L.att_bf;
+        m->f_bf = ws + L.f_bf;
+        m->b_am_counters = reinterpret_cast<int *>(ws + L.b_am_counters);
+        const int S = cfg->max_seqs, es = 2;
+        const int nq = cfg->n_qh * cfg->head_dim, nkv = cfg->n_kvh * cfg->head_dim, nqkv = nq + 2 * nkv;
+        auto mk = [&](int epi, int a_mn, const void *A0, const void *A1, long long stride, int M, int K, void *X,
+                      TcArgs &a) {
+            a = TcArgs{};
+            a.a_mn = a_mn;
+            a.M = M;
+            a.K = K;
+            a.n = S;
+            a.n_pad = tc_n_pad(S);
+            a.split = 1;  // fp32 activations as bf16 hi + lo rows, S rows apart
+            a.b_lo_row = S;
+            a.epi = epi;
+            a.m_tiles = tc_m_tiles(M, epi);
+            a.stages = tc_stages(a.n_pad, 1);
+            a.tmem_cols = 32;
+            while (a.tmem_cols < 2 * a.n_pad) a.tmem_cols *= 2;
+            a.partials = reinterpret_cast<float *>(ws + L.tc_partials);
+            a.counters = reinterpret_cast<int *>(ws + L.tc_counters);
+            a.err = m->err;
+            return tc_make_maps(a, A0, A1, stride, X);
+        };
+        m->tc.resize((size_t)4 * cfg->n_layer + 1);
+        bool ok = true;
+        for (int l = 0; l < cfg->n_layer && ok; ++l) {
+            TcArgs &q = m->tc[4 * l + 0];
+            ok = ok && mk(TC_QKV, 1, m->wqkv[l], nullptr, (long long)nqkv * es, nqkv, cfg->d, m->h_bf, q);
+            q.y = m->q;
+            q.ldy = nq;
+            q.rope_cos = m->rope_cos;
+            q.rope_sin = m->rope_sin;
+            q.rope_rows = cfg->max_ctx;
+            q.nq_cols = nq;
+            q.nkv_cols = nkv;
+            q.head_dim = cfg->head_dim;
+            q.rope_layout = cfg->rope_layout;
+            q.kv_dtype = cfg->kv_dtype;
+            TcArgs &o = m->tc[4 * l + 1];
+            ok = ok && mk(TC_ADD, 1, m->wo[l], nullptr, (long long)cfg->d * es, cfg->d, nq, m->att_bf, o);
+            o.y = m->x;
+            o.ldy = cfg->d;
+            TcArgs &gu = m->tc[4 * l + 2];
+            ok = ok && mk(TC_SILU, 1, m->wgu[l], static_cast<const char *>(m->wgu[l]) + (size_t)cfg->ff * es,
+                          (long long)2 * cfg->ff * es, cfg->ff, cfg->d, m->h_bf, gu);
+            gu.yb = static_cast<__nv_bfloat16 *>(m->f_bf);
+            gu.yb_lo = (long long)S * cfg->ff;
+            gu.ldy = cfg->ff;
+            TcArgs &dn = m->tc[4 * l + 3];
+            ok = ok && mk(TC_ADD, 1, m->wd[l], nullptr, (long long)cfg->d * es, cfg->d, cfg->ff, m->f_bf, dn);
+            dn.y = m->x;
+            dn.ldy = cfg->d;
+        }
+        TcArgs &hd = m->tc[(size_t)4 * cfg->n_layer];
+        ok = ok && mk(TC_STORE, 0, m->out, nullptr, (long long)cfg->d * es, cfg->vocab, cfg->d, m->h_bf, hd);
+        hd.ldy = cfg->vocab;
+        if (!ok || prepare_tc_kernels() != cudaSuccess) {
+            delete m;
+            return DS_CUDA_ERROR;
+        }
+    }
+
     std::vector<unsigned char> layer_img((size_t)std::max(cfg->n_layer, 1) * step_layer_bytes(), 0);
     for (int l = 0; l < cfg->n_layer; ++l)
         step_layer_fill(layer_img.data() + (size_t)l * step_layer_bytes(), &m->maps[5 * l], w->n1[l], w->n2[l]);
@@ -638,15 +740,134 @@ int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t 
     return DS_OK;
 }
 
+// One batched step for n sequences ("Inside the engine", section 4: batched
+// decode, one token per sequence per step).  Activations stay fp32; each
+// projection input is handed to the tensor cores as a bf16 pair hi + lo.  Per
+// layer RMSNorm rows ->
+// q|k|v on the tensor cores (RoPE + K/V write at each sequence's position in
+// the epilogue) -> split-context attention over each sequence's blocks (fp32
+// and bf16 outputs) -> o on the tensor cores (+ residual) -> RMSNorm rows ->
+// gate|up (SiLU-gate to bf16) -> down (+ residual); final RMSNorm rows ->
+// head -> per-row greedy argmax or sampler.  Every launch may begin while its
+// predecessor drains (programmatic dependent launch).
+int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n,
+                     const ds_sampling *sampling, const float *u, int32_t *next_ids, float *logits_out, unsigned flags,
+                     cudaStream_t s) {
+    const ds_model_config &c = m->cfg;
+    const bool greedy = sampling == nullptr || !(sampling->temperature > 0.0f);
+    const bool advance = (flags & DS_STEP_ADVANCE) != 0;
+    float *logits = logits_out ? logits_out : m->logits;
+    const bool pdl = true;
+#define DS_TRYB(expr)                               \
+    do {                                            \
+        if ((expr) != cudaSuccess) return DS_CUDA_ERROR; \
+    } while (0)
+    auto gemm = [&](TcArgs a) { return launch_tc_gemm(a, tc_grid(a.m_tiles, a.K), s, pdl); };
+    const long long h_lo = (long long)c.max_seqs * c.d;  // hi rows, then lo rows
+    DS_TRYB(launch_embed(m->emb, c.w_dtype, c.vocab, c.d, tokens, m->x, m->err, n, s, pdl));
+    for (int l = 0; l < c.n_layer; ++l) {
+        DS_TRYB(launch_rmsnorm_rows_bf16(m->x, m->n1[l], c.eps, m->h_bf, h_lo, n, c.d, s, pdl));
+        TcArgs a = m->tc[4 * l + 0];
+        a.n = n;
+        a.pos = pos;
+        a.block_table = kv->block_table;
+        a.max_blocks = kv->max_blocks;
+        a.block_tokens = kv->block_tokens;
+        a.cache_rows = kv->rows;
+        a.k_cache = kv->k[l];
+        a.v_cache = kv->v[l];
+        DS_TRYB(gemm(a));
+        AttnArgs at = {};
+        at.q = m->q;
+        at.k_cache = kv->k[l];
+        at.v_cache = kv->v[l];
+        at.kv_dtype = c.kv_dtype;
+        at.cache_rows = kv->rows;
+        at.block_table = kv->block_table;
+        at.max_blocks = kv->max_blocks;
+        at.block_tokens = kv->block_tokens;
+        at.seq_lens = nullptr;
+        at.pos = pos;
+        at.n_qh = c.n_qh;
+        at.n_kvh = c.n_kvh;
+        at.hd = c.head_dim;
+        at.scale = 1.0f / sqrtf((float)c.head_dim);
+        at.out = m->att;
+        at.out_bf16 = m->att_bf;
+        at.out_bf16_lo = (long long)c.max_seqs * c.n_qh * c.head_dim;
+        at.partials = m->a_partials;
+        at.counters = m->a_counters;
+        at.err = m->err;
+        at.n_splits = m->b_splits;
+        DS_TRYB(launch_attention(at, n, s, pdl));
+        a = m->tc[4 * l + 1];
+        a.n = n;
+        DS_TRYB(gemm(a));
+        DS_TRYB(launch_rmsnorm_rows_bf16(m->x, m->n2[l], c.eps, m->h_bf, h_lo, n, c.d, s, pdl));
+        a = m->tc[4 * l + 2];
+        a.n = n;
+        DS_TRYB(gemm(a));
+        a = m->tc[4 * l + 3];
+        a.n = n;
+        DS_TRYB(gemm(a));
+    }
+    DS_TRYB(launch_rmsnorm_rows_bf16(m->x, m->final_norm, c.eps, m->h_bf, h_lo, n, c.d, s, pdl));
+    TcArgs hd = m->tc[(size_t)4 * c.n_layer];
+    hd.n = n;
+    hd.y = logits;
+    DS_TRYB(gemm(hd));
+    if (greedy) {
+        ArgmaxArgs am = {};
+        am.logits = logits;
+        am.n_rows = n;
+        am.n = c.vocab;
+        am.ids = next_ids;
+        am.max_logit = nullptr;
+        am.part_val = m->am_val;
+        am.part_idx = m->am_idx;
+        am.counters = m->b_am_counters;
+        am.tokens_adv = advance ? tokens : nullptr;
+        am.pos_adv = advance ? pos : nullptr;
+        am.err = m->err;
+        am.blocks_per_row = argmax_blocks_per_row(c.vocab);
+        DS_TRYB(launch_argmax(am, s, pdl));
+    } else {
+        SampleArgs sa = {};
+        sa.logits = logits;
+        sa.n_rows = n;
+        sa.n = c.vocab;
+        sa.temperature = sampling->temperature;
+        sa.top_k = sampling->top_k;
+        sa.top_p = sampling->top_p;
+        sa.u = u;
+        sa.ids = next_ids;
+        sa.tokens_adv = advance ? tokens : nullptr;
+        sa.pos_adv = advance ? pos : nullptr;
+        sa.err = m->err;
+        DS_TRYB(launch_sample(sa, s, pdl));
+    }
+#undef DS_TRYB
+    return DS_OK;
+}
+
+// The step for this model: the batched path, the persistent step kernel
+// (batch 1) or the per-kernel launch sequence.
+int dispatch_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
+                  const ds_sampling *sampling, const float *u, int32_t *next_ids, float *logits_out, unsigned flags,
+                  cudaStream_t s) {
+    if (m->batched) return run_step_batched(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s);
+    if (m->step_ok && n_seqs == 1)
+        return run_step_fused(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s);
+    return run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s, nullptr);
+}
+
 extern "C" DS_API int ds_decode_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
                                      const ds_sampling *sampling, const float *u, int32_t *next_ids,
                                      float *logits_out, unsigned flags, ds_stream_t stream) {
     int st = check_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids);
     if (st != DS_OK) return st;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (m->step_ok && n_seqs == 1)
-        return run_step_fused(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s);
-    return run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s, nullptr);
+    return dispatch_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" DS_API int ds_model_phase_times(ds_model *m, uint64_t *ns_out, int cap, int *n_out, ds_stream_t stream) {
@@ -671,9 +892,7 @@ extern "C" DS_API int ds_step_graph_create(ds_model *m, const ds_kv_cache *kv, i
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!s) return DS_BAD_ARGUMENT;  // the legacy stream cannot be captured
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return DS_CUDA_ERROR;
-    st = (m->step_ok && n_seqs == 1)
-             ? run_step_fused(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s)
-             : run_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s, nullptr);
+    st = dispatch_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(s, &graph);
     if (st != DS_OK || e != cudaSuccess) {
@@ -716,6 +935,7 @@ extern "C" DS_API int ds_decode_step_profile(ds_model *m, const ds_kv_cache *kv,
                                              float *ms_out, int32_t *kinds_out, int cap, int *n_out,
                                              ds_stream_t stream) {
     if (reps < 1 || !ms_out || !kinds_out || !n_out || cap < 1) return DS_BAD_ARGUMENT;
+    if (m && m->batched) return DS_BAD_ARGUMENT;  // per-kernel timing covers the batch-1 launch sequence
     int st = check_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids);
     if (st != DS_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -749,6 +969,7 @@ extern "C" DS_API int ds_decode_kernel_time(ds_model *m, const ds_kv_cache *kv, 
                                             int kind, int reps, float *us_per_launch, ds_stream_t stream) {
     if (reps < 1 || !us_per_launch || kind < 0 || kind >= DS_KIND_COUNT || kind == DS_KIND_SAMPLE)
         return DS_BAD_ARGUMENT;
+    if (m && m->batched) return DS_BAD_ARGUMENT;
     int st = check_step(m, kv, tokens, pos, 1, nullptr, nullptr, m ? m->am_idx : nullptr);
     if (st != DS_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

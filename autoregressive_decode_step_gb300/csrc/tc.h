@@ -20,12 +20,15 @@ enum { TC_STORE = 0, TC_ADD = 1, TC_SILU = 2, TC_QKV = 3 };
 struct TcArgs {
     CUtensorMap ta0;  // weights: [K][M] boxes {64 features, 64 rows} (a_mn) or [M][K] boxes {64, 128}
     CUtensorMap ta1;  // TC_SILU: the up columns' map (ta0 holds the gate columns)
-    CUtensorMap tb;   // activations [n][K] bf16, boxes {64, n_pad}
+    CUtensorMap tb;   // activations [n][K] bf16, boxes {64, n_pad}; split: [2][rows][K], hi rows then lo rows
     int a_mn;         // 1: weights [K][M], M contiguous; 0: [M][K], K contiguous
     int M, K, n, n_pad;
+    int split;        // 1: each activation is hi + lo, two bf16 rows b_lo_row apart; both are multiplied
+    int b_lo_row;
     int epi, m_tiles, stages, tmem_cols;
     float *y;             // TC_STORE / TC_ADD: y[s * ldy + m]; TC_QKV: q [n][ldy]
-    __nv_bfloat16 *yb;    // TC_SILU: silu(gate) * up as bf16, yb[s * ldy + g]
+    __nv_bfloat16 *yb;    // TC_SILU: silu(gate) * up as bf16, yb[s * ldy + g] (hi part when yb_lo > 0)
+    long long yb_lo;      // TC_SILU: elements from the hi part to the lo part (0: hi only)
     int ldy;
     // TC_QKV: RoPE on the q and k columns, K/V written at each sequence's pos
     const int *pos;
@@ -44,13 +47,19 @@ struct TcArgs {
 };
 
 int tc_n_pad(int n);
-int tc_stages(int n_pad);
+int tc_stages(int n_pad, int split);
 int tc_m_tiles(int M, int epi);
 int tc_grid(int m_tiles, int K);
 size_t tc_partial_floats(int m_tiles, int n_pad);
 // Encode a.ta0 (and a.ta1 from A1 when set) and a.tb.
 bool tc_make_maps(TcArgs &a, const void *A0, const void *A1, long long a_row_stride, const void *X);
 cudaError_t launch_tc_gemm(const TcArgs &a, int grid, cudaStream_t stream, bool pdl);
+// The bf16 pair (hi, lo) with hi + lo = v to 16 significant bits: the form in
+// which a batched projection takes an fp32 activation.
+__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
+    hi = __float2bfloat16_rn(v);
+    lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
 cudaError_t prepare_tc_kernels();
 
 }  // namespace ds

@@ -159,3 +159,17 @@ def logits_with_ties(n, n_ties=3, seed=0, device="cpu"):
     idx = torch.randperm(n, generator=g)[:n_ties].sort().values
     l[idx] = float(l.max()) + 1.0
     return l.to(device), idx.tolist()
+
+
+def context_lengths(n_seqs, lo, hi, seed=0):
+    """n_seqs context lengths uniform in [lo, hi] (the batched workload's mix)."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, (n_seqs,), generator=g, dtype=torch.int64).tolist()
+
+
+def paged_block_table(n_seqs, max_blocks, seed=0):
+    """int32 [n_seqs, max_blocks]: a seeded permutation of the pool's
+    n_seqs * max_blocks physical blocks, so consecutive blocks of a sequence
+    are scattered over the pool."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randperm(n_seqs * max_blocks, generator=g).to(torch.int32).view(n_seqs, max_blocks)

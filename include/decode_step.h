@@ -318,7 +318,11 @@ typedef struct {
     int32_t tied;        /* 1: the output head is the embedding table */
     int32_t w_dtype;     /* DS_F32 or DS_BF16, for emb, out and projections */
     int32_t kv_dtype;    /* DS_F32 or DS_BF16 */
-    int32_t max_seqs;    /* largest n_seqs a step will be given */
+    int32_t max_seqs;    /* largest n_seqs a step will be given, 1..256.  Above 1 every step
+                          * runs the batched path: the projections as GEMMs over the batch on
+                          * the tcgen05 tensor cores ("Inside the engine", section 4: batched
+                          * decode), which needs bf16 weights (else 572) and a head_dim that
+                          * divides 128 (else 577). */
     int32_t max_ctx;     /* largest position + 1 a step will see */
 } ds_model_config;
 
@@ -385,7 +389,12 @@ DS_API void *ds_model_workspace(ds_model *model);
 /* One decode step for n_seqs sequences: for each sequence s, token
  * tokens[s] at position pos[s] ("The forward pass end to end", "What a
  * forward step does"; "LLM inference kernels", "How this composes into a
- * decode step"): embed; per layer RMSNorm -> fused q|k|v projection -> RoPE on
+ * decode step").  A model with max_seqs 1 runs the step as one persistent
+ * kernel; a model with max_seqs > 1 runs the batched path (one launch per
+ * operation, projections on the tensor cores, each fp32 activation handed to
+ * them as a bf16 pair hi + lo, 16 significant bits), every sequence at its own
+ * position in its own blocks of the K/V cache.  The step: embed; per layer
+ * RMSNorm -> fused q|k|v projection -> RoPE on
  * q and k with the K/V write at pos ("Inside the engine", section 1: qkPrep)
  * -> attention over positions 0..pos -> output projection + residual ->
  * RMSNorm -> fused gate|up projection with SiLU-gate -> down projection +

@@ -1,0 +1,168 @@
+"""The batched decode step — projections on the tensor cores, K/V in a paged
+pool, one token per sequence — through the C ABI against the oracle's decode
+step, sequence by sequence.  Both sides receive the same synthetic prefilled
+pool and the same (teacher-forced) tokens."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from autoregressive_decode_step_gb300 import configs as C
+from autoregressive_decode_step_gb300 import synth
+from tests.gpu_util import BF16_TOL, TIE_GAP, host, rel_err, top2_gap
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from autoregressive_decode_step_gb300 import model
+    return model
+
+
+class Pair:
+    """A batched GPU model and the oracle over the same weights and the same
+    synthetic paged pool."""
+
+    def __init__(self, M, cfg, n_seqs, ctx, n_steps, block_tokens, seed):
+        self.cfg, self.n, self.ctx = cfg, n_seqs, list(ctx)
+        W = synth.model_weights(cfg, seed=seed, device="cuda")
+        st = synth.weights_to_numpy(W)
+        cap = max(ctx) + n_steps + 1
+        mb = (cap + block_tokens - 1) // block_tokens
+        n_blocks = n_seqs * mb
+        table = synth.paged_block_table(n_seqs, mb, seed=seed + 1)
+        self.g = M.DecodeModel(cfg, W, capacity=cap, block_tokens=block_tokens, block_table=table.cuda(),
+                               n_blocks=n_blocks, max_seqs=n_seqs)
+        self.o = O.Model(dict(cfg, block_tokens=block_tokens, max_blocks=mb, block_table=table.numpy(),
+                              n_blocks=n_blocks, n_seqs=n_seqs), st)
+        ks, vs = synth.synthetic_kv(cfg, n_blocks * block_tokens, seed=seed + 2, device="cuda")
+        for l in range(cfg["n_layer"]):
+            self.g.k_cache[l].copy_(ks[l])
+            self.g.v_cache[l].copy_(vs[l])
+            self.o.k[l][:] = host(ks[l]).ravel()
+            self.o.v[l][:] = host(vs[l]).ravel()
+        del W, ks, vs
+        self.t = 0
+
+    def step(self, tokens, sampling=None, u=None):
+        """One batched step at positions ctx[s] + t; returns (gpu logits,
+        oracle logits) as [n, vocab] arrays."""
+        pos = [c + self.t for c in self.ctx]
+        self.g.set_state(tokens, pos)
+        if u is not None:
+            self.g.u[:self.n].copy_(torch.as_tensor(u))
+        self.g.step(n_seqs=self.n, sampling=sampling)
+        got = host(self.g.logits[:self.n])
+        ref = np.stack([self.o.step(tokens[s], pos[s], seq=s) for s in range(self.n)])
+        self.t += 1
+        return got, ref
+
+
+def check_logits_and_ids(p, got, ref):
+    worst = 0.0
+    compared = 0
+    ids = host(p.g.next_ids[:p.n])
+    for s in range(p.n):
+        e = rel_err(got[s], ref[s])
+        worst = max(worst, e)
+        assert e <= BF16_TOL, (s, e)
+        if top2_gap(ref[s]) > TIE_GAP:
+            assert int(ids[s]) == O.argmax(ref[s].astype(np.float32))[0], s
+            compared += 1
+    return worst, compared
+
+
+def test_batched_tiny_shape_all_sequences(M):
+    """The tiny decoder's shape with bf16 weights and K/V, 64 sequences at
+    contexts 1..60 in a paged pool of 4-position blocks, 3 steps."""
+    cfg = dict(C.TOY, w_dtype=C.BF16, kv_dtype=C.BF16)
+    ctx = synth.context_lengths(64, 1, 60, seed=3)
+    p = Pair(M, cfg, 64, ctx, 3, block_tokens=4, seed=5)
+    toks = synth.prompt_ids(cfg, 64 * 3, seed=6)
+    compared = 0
+    for t in range(3):
+        got, ref = p.step(toks[64 * t:64 * (t + 1)])
+        _, c = check_logits_and_ids(p, got, ref)
+        compared += c
+    assert compared >= 150
+    assert p.g.error_word() == 0
+
+
+def test_batched_llama8b_shape_two_layers_paged(M):
+    """8B widths (q|k|v 4096 x 6144, gate|up 4096 x 28672, down 14336 x 4096,
+    head 128,256 x 4096), 2 layers, 16 sequences at contexts 1..300 in a
+    paged pool of 16-position blocks, 2 steps; K/V written at each position
+    checked against the oracle's cache."""
+    cfg = dict(C.LLAMA3_8B, n_layer=2)
+    ctx = synth.context_lengths(16, 1, 300, seed=7)
+    p = Pair(M, cfg, 16, ctx, 2, block_tokens=16, seed=8)
+    toks = synth.prompt_ids(cfg, 32, seed=9)
+    for t in range(2):
+        got, ref = p.step(toks[16 * t:16 * (t + 1)])
+        worst, compared = check_logits_and_ids(p, got, ref)
+        assert compared >= 10
+    # the K/V rows this step wrote, sequence 3, both layers
+    row_len = cfg["n_kvh"] * cfg["head_dim"]
+    table = host(p.g.block_table)
+    for s in (0, 3, 15):
+        pos = ctx[s] + 1
+        row = int(table[s][pos // 16]) * 16 + pos % 16
+        for l in range(2):
+            kg = O.bf16_bits_to_f64(host(p.g.k_cache[l][row]))
+            ko = O.bf16_bits_to_f64(p.o.k[l][row * row_len:(row + 1) * row_len])
+            assert rel_err(kg, ko) <= BF16_TOL
+    assert p.g.error_word() == 0
+
+
+def test_batched_qwen_shape_per_row_sampling(M):
+    """Tied Qwen3-0.6B widths, 1 layer, 8 sequences, per-row sampling at
+    temperature 0.8 / top_k 50 / top_p 0.95 with one seeded draw per row: the
+    GPU's id equals the oracle sampler's on the oracle's logits wherever the
+    draw is not within 1e-3 of a CDF boundary."""
+    cfg = dict(C.QWEN3_0_6B, n_layer=1)
+    ctx = synth.context_lengths(8, 1, 100, seed=10)
+    p = Pair(M, cfg, 8, ctx, 2, block_tokens=16, seed=11)
+    toks = synth.prompt_ids(cfg, 16, seed=12)
+    u = synth.uniform_draws(16, seed=13)
+    compared = 0
+    for t in range(2):
+        uu = u[8 * t:8 * (t + 1)]
+        got, ref = p.step(toks[8 * t:8 * (t + 1)], sampling=(0.8, 50, 0.95), u=uu)
+        ids = host(p.g.next_ids[:8])
+        for s in range(8):
+            assert rel_err(got[s], ref[s]) <= BF16_TOL
+            want, margin = O.sample(ref[s].astype(np.float32), 0.8, 50, 0.95, float(uu[s]))
+            if margin >= 1e-3:
+                assert int(ids[s]) == want, s
+                compared += 1
+    assert compared >= 8
+
+
+def test_batched_graph_replay_equals_eager_and_is_bit_stable(M):
+    cfg = dict(C.LLAMA3_8B, n_layer=1, vocab=4096)
+    ctx = synth.context_lengths(32, 1, 64, seed=14)
+    runs = []
+    for mode in ("eager", "graph", "eager"):
+        p = Pair(M, cfg, 32, ctx, 4, block_tokens=16, seed=15)
+        p.g.set_state(synth.prompt_ids(cfg, 32, seed=16), ctx)
+        ids = []
+        if mode == "graph":
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                replay = p.g.graph(n_seqs=32, advance=True, write_logits=True, stream=s)
+                for _ in range(4):
+                    replay(s)
+                    s.synchronize()
+                    ids.append(host(p.g.next_ids[:32]).copy())
+        else:
+            for _ in range(4):
+                p.g.step(n_seqs=32, advance=True)
+                ids.append(host(p.g.next_ids[:32]).copy())
+        assert host(p.g.pos[:32]).tolist() == [c + 4 for c in ctx]
+        runs.append((np.stack(ids), host(p.g.logits[:32]).copy()))
+    for r in runs[1:]:
+        np.testing.assert_array_equal(r[0], runs[0][0])
+        np.testing.assert_array_equal(r[1], runs[0][1])
