@@ -13,6 +13,8 @@
 // the workspace.  The last CTA of a (sequence, KV head) — an atomic counter,
 // never a wait — merges the splits in split order, so the result does not
 // depend on which CTA finishes first.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -306,8 +308,9 @@ extern "C" DS_API size_t ds_attention_workspace_bytes(int n_seqs, int n_qh, int 
                                                       int64_t max_ctx) {
     if (n_seqs < 1 || n_kvh < 1 || n_qh < n_kvh || head_dim < 1 || max_ctx < 1) return 0;
     const int splits = attention_splits(n_seqs, n_kvh, max_ctx);
-    return kWsHeader + align_up((size_t)n_seqs * n_kvh * 4, 256) +
-           attention_partial_floats(n_seqs, n_qh, n_kvh, head_dim, splits) * 4;
+    const size_t partial = std::max(attention_partial_floats(n_seqs, n_qh, n_kvh, head_dim, splits),
+                                    paged_attention_partial_floats(n_seqs, n_qh));
+    return kWsHeader + align_up((size_t)n_seqs * n_kvh * 4, 256) + partial * 4;
 }
 
 extern "C" DS_API int ds_gqa_decode_attn(const float *q, const void *k_cache, const void *v_cache,
@@ -338,6 +341,28 @@ extern "C" DS_API int ds_gqa_decode_attn(const float *q, const void *k_cache, co
     if (!workspace || workspace_bytes < need) return DS_WORKSPACE_TOO_SMALL;
     if ((uintptr_t)workspace & 255) return DS_BAD_ARGUMENT;
     char *ws = static_cast<char *>(workspace);
+    if (paged_attention_supported(n_qh, n_kvh, head_dim, block_tokens, n_seqs, kv_dtype)) {
+        // whole 16-position blocks streamed through shared memory, work split evenly over the SMs
+        PagedAttnArgs pa = {};
+        pa.q = q;
+        pa.k_cache = k_cache;
+        pa.v_cache = v_cache;
+        pa.kv_dtype = kv_dtype;
+        pa.cache_rows = cache_rows;
+        pa.block_table = block_table;
+        pa.max_blocks = max_blocks_per_seq;
+        pa.seq_lens = seq_lens;
+        pa.n_seqs = n_seqs;
+        pa.n_qh = n_qh;
+        pa.n_kvh = n_kvh;
+        pa.scale = scale;
+        pa.out = out;
+        pa.err = reinterpret_cast<int *>(ws);
+        pa.counters = reinterpret_cast<int *>(ws + kWsHeader);
+        pa.partials = reinterpret_cast<float *>(ws + kWsHeader + align_up((size_t)n_seqs * n_kvh * 4, 256));
+        cudaError_t e = launch_paged_attention(pa, reinterpret_cast<cudaStream_t>(stream), false);
+        return e == cudaSuccess ? DS_OK : DS_CUDA_ERROR;
+    }
     AttnArgs a = {};
     a.q = q;
     a.k_cache = k_cache;

@@ -148,6 +148,33 @@ struct AttnArgs {
     int *err;
     int n_splits;
 };
+// Paged flash-decoding over whole cache blocks (head_dim 128, 16-position
+// blocks, 2 or 4 query heads per KV head, at most 8 KV heads).
+struct PagedAttnArgs {
+    const float *q;        // [n_seqs][n_qh * 128]
+    const void *k_cache;   // rows of n_kvh * 128 elements of kv_dtype
+    const void *v_cache;
+    int kv_dtype;
+    long long cache_rows;
+    const int *block_table;  // [n_seqs][max_blocks] or nullptr (contiguous slots)
+    int max_blocks;
+    const int *seq_lens;   // [n_seqs] or nullptr (then n_ctx = pos[s] + 1)
+    const int *pos;
+    int n_seqs, n_qh, n_kvh;
+    float scale;
+    float *out;            // [n_seqs][n_qh * 128]
+    void *out_bf16;        // optional bf16 pair of out: hi here, lo out_bf16_lo elements further
+    long long out_bf16_lo;
+    float *partials;       // paged_attention_partial_floats(n_seqs, n_qh)
+    int *counters;         // n_seqs * n_kvh ints, zero between launches
+    int *err;
+    int stages;            // set by the launcher
+};
+bool paged_attention_supported(int n_qh, int n_kvh, int hd, int block_tokens, int n_seqs, int kv_dtype);
+size_t paged_attention_partial_floats(int n_seqs, int n_qh);
+cudaError_t launch_paged_attention(const PagedAttnArgs &a, cudaStream_t stream, bool pdl);
+cudaError_t prepare_paged_attention();
+
 int attention_splits(int n_seqs, int n_kvh, long long max_ctx);
 size_t attention_partial_floats(int n_seqs, int n_qh, int n_kvh, int hd, int n_splits);
 cudaError_t launch_attention(const AttnArgs &a, int n_seqs, cudaStream_t stream, bool pdl);

@@ -182,9 +182,10 @@ Layout make_layout(const ds_model_config *c) {
     L.g_counters = carve(off, (size_t)max_bands * 4);
     L.g_partials = carve(off, partial * 4);
     L.a_counters = carve(off, (size_t)S * c->n_kvh * 4);
-    L.a_partials = carve(off, attention_partial_floats(S, c->n_qh, c->n_kvh, c->head_dim,
-                                                       std::max(std::max(L.attn_splits, L.step_splits), L.b_splits)) *
-                                  4);
+    size_t a_part = attention_partial_floats(S, c->n_qh, c->n_kvh, c->head_dim,
+                                             std::max(std::max(L.attn_splits, L.step_splits), L.b_splits));
+    if (batched) a_part = std::max(a_part, paged_attention_partial_floats(S, c->n_qh));
+    L.a_partials = carve(off, a_part * 4);
     const size_t am_slots = std::max((size_t)std::max(L.grid_head, L.step_grid),
                                      (size_t)S * argmax_blocks_per_row(c->vocab));
     L.am_val = carve(off, am_slots * 4);
@@ -629,7 +630,7 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
         TcArgs &hd = m->tc[(size_t)4 * cfg->n_layer];
         ok = ok && mk(TC_STORE, 0, m->out, nullptr, (long long)cfg->d * es, cfg->vocab, cfg->d, m->h_bf, hd);
         hd.ldy = cfg->vocab;
-        if (!ok || prepare_tc_kernels() != cudaSuccess) {
+        if (!ok || prepare_tc_kernels() != cudaSuccess || prepare_paged_attention() != cudaSuccess) {
             delete m;
             return DS_CUDA_ERROR;
         }
@@ -777,29 +778,53 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
         a.k_cache = kv->k[l];
         a.v_cache = kv->v[l];
         DS_TRYB(gemm(a));
-        AttnArgs at = {};
-        at.q = m->q;
-        at.k_cache = kv->k[l];
-        at.v_cache = kv->v[l];
-        at.kv_dtype = c.kv_dtype;
-        at.cache_rows = kv->rows;
-        at.block_table = kv->block_table;
-        at.max_blocks = kv->max_blocks;
-        at.block_tokens = kv->block_tokens;
-        at.seq_lens = nullptr;
-        at.pos = pos;
-        at.n_qh = c.n_qh;
-        at.n_kvh = c.n_kvh;
-        at.hd = c.head_dim;
-        at.scale = 1.0f / sqrtf((float)c.head_dim);
-        at.out = m->att;
-        at.out_bf16 = m->att_bf;
-        at.out_bf16_lo = (long long)c.max_seqs * c.n_qh * c.head_dim;
-        at.partials = m->a_partials;
-        at.counters = m->a_counters;
-        at.err = m->err;
-        at.n_splits = m->b_splits;
-        DS_TRYB(launch_attention(at, n, s, pdl));
+        if (paged_attention_supported(c.n_qh, c.n_kvh, c.head_dim, kv->block_tokens, n, c.kv_dtype)) {
+            PagedAttnArgs pa = {};
+            pa.q = m->q;
+            pa.k_cache = kv->k[l];
+            pa.v_cache = kv->v[l];
+            pa.kv_dtype = c.kv_dtype;
+            pa.cache_rows = kv->rows;
+            pa.block_table = kv->block_table;
+            pa.max_blocks = kv->max_blocks;
+            pa.seq_lens = nullptr;
+            pa.pos = pos;
+            pa.n_seqs = n;
+            pa.n_qh = c.n_qh;
+            pa.n_kvh = c.n_kvh;
+            pa.scale = 1.0f / sqrtf((float)c.head_dim);
+            pa.out = m->att;
+            pa.out_bf16 = m->att_bf;
+            pa.out_bf16_lo = (long long)c.max_seqs * c.n_qh * c.head_dim;
+            pa.partials = m->a_partials;
+            pa.counters = m->a_counters;
+            pa.err = m->err;
+            DS_TRYB(launch_paged_attention(pa, s, pdl));
+        } else {
+            AttnArgs at = {};
+            at.q = m->q;
+            at.k_cache = kv->k[l];
+            at.v_cache = kv->v[l];
+            at.kv_dtype = c.kv_dtype;
+            at.cache_rows = kv->rows;
+            at.block_table = kv->block_table;
+            at.max_blocks = kv->max_blocks;
+            at.block_tokens = kv->block_tokens;
+            at.seq_lens = nullptr;
+            at.pos = pos;
+            at.n_qh = c.n_qh;
+            at.n_kvh = c.n_kvh;
+            at.hd = c.head_dim;
+            at.scale = 1.0f / sqrtf((float)c.head_dim);
+            at.out = m->att;
+            at.out_bf16 = m->att_bf;
+            at.out_bf16_lo = (long long)c.max_seqs * c.n_qh * c.head_dim;
+            at.partials = m->a_partials;
+            at.counters = m->a_counters;
+            at.err = m->err;
+            at.n_splits = m->b_splits;
+            DS_TRYB(launch_attention(at, n, s, pdl));
+        }
         a = m->tc[4 * l + 1];
         a.n = n;
         DS_TRYB(gemm(a));

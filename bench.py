@@ -37,6 +37,12 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--ctx", type=int, default=1024, help="prefilled context before the first timed step")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-batched", action="store_true", help="skip the batched (64-sequence) decode measurement")
+    p.add_argument("--batched-only", action="store_true",
+                   help="time only the batched (64-sequence) decode (a profiling case; the line's batch-1 keys are "
+                        "then absent)")
+    p.add_argument("--batched-steps", type=int, default=None,
+                   help="timed steps of the batched decode (default: the workload's 128)")
     p.add_argument("--layers", type=int, default=None,
                    help="decoder layers (default: the model's 32); fewer layers make a small profiling case, "
                         "not a benchmark number")
@@ -279,6 +285,98 @@ def profile_summary_traffic(kernel_src_sha):
     return traffic if sha == kernel_src_sha else None
 
 
+def run_batched(cfg, W, dev, rank, clocks_cls, bus, warmup=3, steps=None):
+    """Batched continuous decode on the same 8B-shaped weights: 64 sequences,
+    contexts uniform in [128, 4096] (a synthetic prefilled paged pool of
+    16-position blocks), one token per sequence per step, per-row sampling at
+    temperature 0.8 / top_k 50 / top_p 0.95 with seeded draws, 128 steps
+    replayed from a captured graph (tokens and positions advance on the
+    device; each step's 64 draws are copied into place before it)."""
+    import torch
+
+    from autoregressive_decode_step_gb300 import configs as C
+    from autoregressive_decode_step_gb300 import synth
+    from autoregressive_decode_step_gb300.model import DecodeModel
+
+    B = C.BATCHED_8B
+    n, bt = B["n_seqs"], B["block_tokens"]
+    steps = steps or B["steps"]
+    ctx = synth.context_lengths(n, B["ctx_lo"], B["ctx_hi"], seed=rank)
+    # a compact pool: sequence s owns ceil((ctx + steps + warm-up + 1) / bt)
+    # blocks, scattered over the pool by a seeded permutation
+    need = [(c + steps + warmup + 1 + bt - 1) // bt for c in ctx]
+    max_blocks = max(need)
+    n_blocks = sum(need)
+    perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(rank + 1)).to(torch.int32)
+    table = torch.zeros(n, max_blocks, dtype=torch.int32)
+    at = 0
+    for s_, k in enumerate(need):
+        table[s_, :k] = perm[at:at + k]
+        at += k
+    model = DecodeModel(cfg, W, capacity=max_blocks * bt, device=dev, block_tokens=bt,
+                        block_table=table.to(dev), n_blocks=n_blocks, max_seqs=n)
+    ks, vs = synth.synthetic_kv(cfg, n_blocks * bt, seed=rank + 2, device=dev)
+    for l in range(cfg["n_layer"]):
+        model.k_cache[l].copy_(ks[l])
+        model.v_cache[l].copy_(vs[l])
+    del ks, vs
+    toks = synth.prompt_ids(cfg, n, seed=rank + 3)
+    U = synth.uniform_draws((warmup + steps) * n, seed=rank + 4).view(warmup + steps, n).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    sampling = (B["temperature"], B["top_k"], B["top_p"])
+    with torch.cuda.stream(stream):
+        replay = model.graph(n_seqs=n, sampling=sampling, advance=True, write_logits=False, stream=stream)
+    model.set_state(toks, ctx)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            model.u[:n].copy_(U[i], non_blocking=True)
+            replay(stream)
+    stream.synchronize()
+    pos0 = [c + warmup for c in ctx]
+    clocks = clocks_cls(bus)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            model.u[:n].copy_(U[warmup + i], non_blocking=True)
+            replay(stream)
+        e1.record(stream)
+    e1.synchronize()
+    t_wall1 = time.perf_counter()
+    ms = e0.elapsed_time(e1)
+    time.sleep(0.2)
+    clocks.stop()
+    err = model.error_word()
+    if err:
+        raise RuntimeError("device error word %d during the batched timed region" % err)
+    assert model.pos[:n].cpu().tolist() == [p + steps for p in pos0]
+    kvb = C.kv_bytes_per_token(cfg)
+    alg = sum(C.weight_bytes_per_step(cfg) + sum(p + i + 1 for p in pos0) * kvb for i in range(steps)) / steps
+    step_ms = ms / steps
+    peak, kind = peaks()
+    achieved = alg / (step_ms / 1e3) / 1e9
+    out = {"workload": "llama3-8b-shape, %d sequences, contexts uniform in [%d, %d] (mean %.0f), paged K/V pool of "
+                       "%d-position blocks (%d blocks), sampling T=%.1f top_k=%d top_p=%.2f with seeded draws, %d steps"
+                       % (n, B["ctx_lo"], B["ctx_hi"], sum(ctx) / n, bt, n_blocks, sampling[0], sampling[1],
+                          sampling[2], steps),
+           "value": n * steps / (ms / 1e3), "unit": "tokens/s (all sequences)", "ms_per_step": step_ms,
+           "steps": steps, "warmup": warmup,
+           "hbm_roofline_step": {"achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                                 "algorithmic_bytes_per_step": alg,
+                                 "algorithmic_bytes": "every weight byte once + K/V of every attended position of "
+                                                      "every sequence", "peak_source": kind},
+           "gpu_launches_per_step": 7 * cfg["n_layer"] + 4,
+           "clocks": clocks.summary(t_wall0, t_wall1)}
+    del model
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -296,6 +394,16 @@ def run_ours(args, rank, world, local):
     K, Wm = args.steps, args.warmup
     cap = args.ctx + max(Wm, K) + 8
     W = synth.model_weights(cfg, seed=0, device=dev)
+    if args.batched_only:
+        props = torch.cuda.get_device_properties(dev)
+        bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), getattr(props, "pci_bus_id", 0),
+                                    getattr(props, "pci_device_id", 0))
+        line = {"metric": METRIC, "n_gpus": world, "data": "synthetic",
+                "batched": run_batched(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus,
+                                       steps=args.batched_steps)}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
     model = DecodeModel(cfg, W, capacity=cap, device=dev, block_tokens=16)
     if args.kv_fill == "prefill":
         prompt = synth.prompt_ids(cfg, args.ctx, seed=rank)
@@ -416,7 +524,12 @@ def run_ours(args, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
             "gpu_launches": K,
             "clocks": clocks.summary(t_wall0, t_wall1)}
-    del W, model
+    del model
+    torch.cuda.empty_cache()
+    if args.layers is None and not args.no_batched:
+        line["batched"] = run_batched(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus,
+                                      steps=args.batched_steps)
+    del W
     torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         per_tok, threads, desc, parts = oracle_token_time(C.LLAMA3_8B, args.ctx, reps=3)

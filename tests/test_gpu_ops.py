@@ -185,6 +185,18 @@ def test_attention_8b_heads_bf16(A, lens, paged):
     _attn_case(A, 32, 8, 128, lens, torch.bfloat16, 16, paged, seed=len(lens) * 100 + lens[0])
 
 
+def test_attention_many_sequences_paged_pool(A):
+    """64 sequences, contexts 1..600, 16-position blocks scattered over the
+    pool: the whole-block streaming kernel with its even split of blocks over
+    the SMs and the per-sequence merge."""
+    lens = synth.context_lengths(64, 1, 600, seed=21)
+    _attn_case(A, 32, 8, 128, lens, torch.bfloat16, 16, True, seed=22)
+
+
+def test_attention_fp32_cache_two_heads_per_group(A):
+    _attn_case(A, 16, 8, 128, [5, 300, 1, 64, 17, 33], torch.float32, 16, True, seed=23)
+
+
 @pytest.mark.parametrize("n_qh,n_kvh,hd", [(4, 2, 4), (16, 8, 128), (8, 8, 64), (8, 1, 32)])
 def test_attention_fp32_shapes(A, n_qh, n_kvh, hd):
     _attn_case(A, n_qh, n_kvh, hd, [1, 29, 64], torch.float32, 4, False, seed=hd)
