@@ -105,7 +105,19 @@ __global__ void rmsnorm_rows_bf16_kernel(const float *x, const float *w, float e
     grid_dependency_wait();
     const float *xr = x + (long long)blockIdx.x * d;
     float ss = 0.0f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+    if ((d & 3) == 0) {  // 16-byte loads, several in flight per thread
+        const float4 *x4 = reinterpret_cast<const float4 *>(xr);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+            const float4 v = x4[i];
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            ss = fmaf(v.z, v.z, ss);
+            ss = fmaf(v.w, v.w, ss);
+        }
+    } else {
+        for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+    }
     ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
@@ -117,6 +129,7 @@ __global__ void rmsnorm_rows_bf16_kernel(const float *x, const float *w, float e
     __syncthreads();
     const float sc = s_scale;
     __nv_bfloat16 *hr = h + (long long)blockIdx.x * d;
+#pragma unroll 4
     for (int i = threadIdx.x; i < d; i += blockDim.x) {
         const float v = xr[i] * sc * w[i];
         const __nv_bfloat16 hi = __float2bfloat16_rn(v);

@@ -173,13 +173,20 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
     if constexpr (EPI == TC_STORE || EPI == TC_ADD) {
         const int m = tile * kTcBM + r;
         if (m < p.M) {
+            float *col = p.y + (long long)j0 * p.ldy + m;
+            const int nj = min(32, p.n - j0);
+            if constexpr (EPI == TC_ADD) {
+                // every residual load of the chunk goes out before the first store
+                float old[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int j = j0 + i;
-                if (j < p.n) {
-                    float *dst = p.y + (long long)j * p.ldy + m;
-                    *dst = EPI == TC_ADD ? *dst + v[i] : v[i];
-                }
+                for (int i = 0; i < 32; ++i) old[i] = i < nj ? __ldcg(col + (long long)i * p.ldy) : 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < nj) col[(long long)i * p.ldy] = old[i] + v[i];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < nj) col[(long long)i * p.ldy] = v[i];
             }
         }
         return;
@@ -247,20 +254,30 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
                     partner = r ^ 1;
                 }
             }
+            const int nj = min(32, p.n - j0);
+            // the chunk's rotation angles, loaded together before any use
+            float cs[32], sn[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                cs[i] = 1.0f;
+                sn[i] = 0.0f;
+                if (rot && i < nj) {
+                    const int pos = s_row[32 + i];
+                    if (pos >= 0 && pos < p.rope_rows) {
+                        cs[i] = __ldg(p.rope_cos + (long long)pos * half + pair);
+                        sn[i] = __ldg(p.rope_sin + (long long)pos * half + pair);
+                    }
+                }
+            }
+#pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int j = j0 + i;
-                if (j >= p.n) break;
+                if (i >= nj) break;
                 float out = xch[r * kTcXchStride + i];
                 const int row = s_row[i];
                 if (rot) {
-                    const int pos = s_row[32 + i];
-                    float c = 1.0f, sn = 0.0f;
-                    if (pos >= 0 && pos < p.rope_rows) {
-                        c = p.rope_cos[(long long)pos * half + pair];
-                        sn = p.rope_sin[(long long)pos * half + pair];
-                    }
                     const float o = xch[partner * kTcXchStride + i];
-                    out = first ? out * c - o * sn : o * sn + out * c;
+                    out = first ? out * cs[i] - o * sn[i] : o * sn[i] + out * cs[i];
                 }
                 if (m < p.nq_cols) {
                     p.y[(long long)j * p.ldy + m] = out;
