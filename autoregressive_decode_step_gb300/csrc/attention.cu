@@ -360,6 +360,7 @@ extern "C" DS_API int ds_gqa_decode_attn(const float *q, const void *k_cache, co
         pa.err = reinterpret_cast<int *>(ws);
         pa.counters = reinterpret_cast<int *>(ws + kWsHeader);
         pa.partials = reinterpret_cast<float *>(ws + kWsHeader + align_up((size_t)n_seqs * n_kvh * 4, 256));
+        if (kv_dtype == DS_BF16 && !paged_attention_maps(pa)) return DS_CUDA_ERROR;
         cudaError_t e = launch_paged_attention(pa, reinterpret_cast<cudaStream_t>(stream), false);
         return e == cudaSuccess ? DS_OK : DS_CUDA_ERROR;
     }

@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.h"
 
 namespace ds {
 
@@ -56,6 +57,88 @@ __device__ __forceinline__ void fold(float (&v)[2 * N], float (&out)[N], int dis
     }
 }
 
+// After a CTA has written its record for (sequence s, KV head g) into slot
+// CTA + s: count the arrival; the last of the CTAs that covered the sequence
+// (those holding its units f0 .. f1) merges the records in CTA order,
+// out = sum_c w_c acc_c / sum_c w_c l_c with w_c = exp(m_c - max m), and
+// writes the output rows (fp32, and the bf16 pair hi + lo when asked).
+template <int GQ>
+__device__ void pa_finish_sequence(const PagedAttnArgs &p, int s, int g, long long f0, long long f1, int Ge,
+                                   long long T) {
+    const int lane = threadIdx.x & 31;
+    const int rec = kPaHd + 2;
+    const int c_first = (int)(((f0 + 1) * Ge - 1) / T), c_last = (int)(((f1 + 1) * Ge - 1) / T);
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        int *ctr = p.counters + (size_t)s * p.n_kvh + g;
+        last = atomicAdd(ctr, 1) == c_last - c_first;
+        if (last) *ctr = 0;  // ready for the next launch
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    for (int j = 0; j < GQ; ++j) {
+        const int h = g * GQ + j;
+        float M = -INFINITY;
+        for (int c = c_first; c <= c_last; ++c)
+            M = fmaxf(M, __ldcg(p.partials + ((size_t)c + s) * p.n_qh * rec + (size_t)h * rec));
+        float L = 0.0f, A[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int c = c_first; c <= c_last; ++c) {
+            const float *rr = p.partials + ((size_t)c + s) * p.n_qh * rec + (size_t)h * rec;
+            const float mc = __ldcg(rr);
+            const float w = mc == -INFINITY ? 0.0f : expf(mc - M);
+            L = fmaf(__ldcg(rr + 1), w, L);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) A[e] = fmaf(__ldcg(rr + 2 + lane * 4 + e), w, A[e]);
+        }
+        const long long o = ((long long)s * p.n_qh + h) * kPaHd + lane * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float r1 = A[e] / L;
+            p.out[o + e] = r1;
+            if (p.out_bf16) {
+                __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(p.out_bf16);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(r1);
+                ob[o + e] = hi;
+                if (p.out_bf16_lo) ob[o + e + p.out_bf16_lo] = __float2bfloat16_rn(r1 - __bfloat162float(hi));
+            }
+        }
+    }
+}
+
+// The flattened block list of a launch: every CTA reads the sequence lengths
+// (seq_lens, else pos + 1, clamped to the cache and flagged when outside it)
+// and forms the prefix sums of their block counts.  Warp 0 does the scan.
+__device__ void pa_block_list(const PagedAttnArgs &p, PaSeqs &sq) {
+    const int lane = threadIdx.x & 31;
+    const int cap = p.max_blocks * kPaBt;
+    int carry = 0;
+    for (int s0 = 0; s0 < p.n_seqs; s0 += 32) {
+        const int s = s0 + lane;
+        int n_ctx = 0, nb = 0;
+        if (s < p.n_seqs) {
+            n_ctx = p.seq_lens ? p.seq_lens[s] : p.pos[s] + 1;
+            if (n_ctx < 1 || n_ctx > cap) {
+                if (blockIdx.x == 0) flag_error(p.err, DS_ERR_POSITION);
+                n_ctx = min(max(n_ctx, 1), cap);
+            }
+            nb = (n_ctx + kPaBt - 1) / kPaBt;
+            sq.n_ctx[s] = n_ctx;
+        }
+        int incl = nb;  // inclusive scan over the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (s < p.n_seqs) sq.first[s] = carry + incl - nb;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) sq.first[p.n_seqs] = carry;
+}
+
 template <typename KT, int GQ>
 __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_kernel(const __grid_constant__ PagedAttnArgs p) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -81,33 +164,8 @@ __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_kernel
 
     // every thread block derives the flattened block list from the lengths
     if (warp == 0) {
-        const int cap = p.max_blocks * kPaBt;
-        int carry = 0;
-        for (int s0 = 0; s0 < p.n_seqs; s0 += 32) {
-            const int s = s0 + lane;
-            int n_ctx = 0, nb = 0;
-            if (s < p.n_seqs) {
-                n_ctx = p.seq_lens ? p.seq_lens[s] : p.pos[s] + 1;
-                if (n_ctx < 1 || n_ctx > cap) {
-                    if (blockIdx.x == 0) flag_error(p.err, DS_ERR_POSITION);
-                    n_ctx = min(max(n_ctx, 1), cap);
-                }
-                nb = (n_ctx + kPaBt - 1) / kPaBt;
-                sq.n_ctx[s] = n_ctx;
-            }
-            int incl = nb;  // inclusive scan over the warp
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (s < p.n_seqs) sq.first[s] = carry + incl - nb;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) {
-            sq.first[p.n_seqs] = carry;
-            s_abort = 0;
-        }
+        pa_block_list(p, sq);
+        if (lane == 0) s_abort = 0;
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -353,49 +411,307 @@ __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_kernel
                 for (int e = 0; e < 8; ++e) rr[2 + sl * 8 + e] = acc[j][e];
             }
         }
-        // the CTAs holding this sequence's first and last block
-        const long long f0 = sq.first[s], f1 = sq.first[s + 1] - 1;
-        const int c_first = (int)(((f0 + 1) * Ge - 1) / T), c_last = (int)(((f1 + 1) * Ge - 1) / T);
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            int *ctr = p.counters + (size_t)s * n_kvh + g;
-            last = atomicAdd(ctr, 1) == c_last - c_first;
-            if (last) *ctr = 0;  // ready for the next launch
+        pa_finish_sequence<GQ>(p, s, g, sq.first[s], sq.first[s + 1] - 1, Ge, T);
+    }
+}
+
+
+// ------------------------------------------------------------------ tensor-core variant (bf16 caches)
+// The same work split and merge, with the two products of a block on the
+// tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulators):
+//   scores   S^T[16 positions][8] = K[16 x 128] . Q^T[128 x 8]
+//   output   O^T[128][8]         += V^T[128 x 16] . P^T[16 x 8]
+// The 8 columns hold the GQ query heads twice: their bf16 "hi" parts and,
+// GQ columns further, the "lo" remainders (hi + lo = the fp32 value to 16
+// significant bits), so q and the softmax weights P keep fp32-like precision
+// and a column pair is summed after each product.  K and V arrive per head as
+// two 64-dim x 16-position boxes with 128-byte swizzling, which ldmatrix
+// reads without bank conflicts (.trans for V^T).
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 lo_elem, __nv_bfloat16 hi_elem) {
+    return (uint32_t)__bfloat16_as_ushort(lo_elem) | ((uint32_t)__bfloat16_as_ushort(hi_elem) << 16);
+}
+// Byte offset, within a stage, of dims d..d+7 of position pos of head g: two
+// 2 KB boxes per head (dims 0-63, 64-127), rows of 128 bytes whose 16-byte
+// chunks are swizzled by the row index.
+__device__ __forceinline__ uint32_t pa_swz(int g, int pos, int d) {
+    const int half = d >> 6, c = (d & 63) >> 3;
+    return (uint32_t)(g * 4096 + half * 2048 + pos * 128 + ((c ^ (pos & 7)) << 4));
+}
+
+template <int GQ>
+__global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_tc_kernel(const __grid_constant__ PagedAttnArgs p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int n_kvh = p.n_kvh;
+    const int stage_bytes = n_kvh * 4096;  // 16 positions x n_kvh heads x 128 dims of bf16
+    const int stages = p.stages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
+    uint64_t *empty = full + 16;
+    __nv_bfloat16 *ptab_all = reinterpret_cast<__nv_bfloat16 *>(empty + 16);  // per warp [8 columns][16 positions]
+    __shared__ PaSeqs sq;
+    __shared__ int s_abort_raw;
+    volatile int &s_abort = s_abort_raw;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x;
+
+    allow_dependent_launch();
+    grid_dependency_wait();
+    if (warp == 0) {
+        pa_block_list(p, sq);
+        if (lane == 0) s_abort = 0;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], n_kvh);
         }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-            __threadfence();
-            // merge in CTA order: out = sum_c w_c acc_c / sum_c w_c l_c, w_c = exp(m_c - max m)
-            for (int j = 0; j < GQ; ++j) {
-                const int h = g * GQ + j;
-                float M = -INFINITY;
-                for (int c = c_first; c <= c_last; ++c)
-                    M = fmaxf(M, __ldcg(p.partials + ((size_t)c + s) * p.n_qh * rec + (size_t)h * rec));
-                float L = 0.0f, A[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                for (int c = c_first; c <= c_last; ++c) {
-                    const float *rr = p.partials + ((size_t)c + s) * p.n_qh * rec + (size_t)h * rec;
-                    const float mc = __ldcg(rr);
-                    const float w = mc == -INFINITY ? 0.0f : expf(mc - M);
-                    L = fmaf(__ldcg(rr + 1), w, L);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) A[e] = fmaf(__ldcg(rr + 2 + lane * 4 + e), w, A[e]);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    const long long T = sq.first[p.n_seqs];
+    const int Ge = (int)min((long long)G, T);
+    const bool in = (int)blockIdx.x < Ge;
+    const long long u0 = in ? T * blockIdx.x / Ge : 0, u1 = in ? T * (blockIdx.x + 1) / Ge : 0;
+    auto seq_of = [&](long long u) {
+        int lo = 0, hi = p.n_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sq.first[mid] <= u) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    };
+
+    if (warp == n_kvh) {
+        // ------------------------------------------------ producer
+        if (lane == 0 && u0 < u1) {
+            const uint64_t pol = policy_evict_first();
+            uint32_t fill = 0;
+            int s = seq_of(u0);
+            for (long long u = u0; u < u1; ++u) {
+                while (u >= sq.first[s + 1]) ++s;
+                const int b = (int)(u - sq.first[s]);
+                const long long blk = p.block_table ? (long long)__ldg(p.block_table + (long long)s * p.max_blocks + b)
+                                                    : (long long)s * p.max_blocks + b;
+                const bool ok = blk >= 0 && (blk + 1) * kPaBt <= p.cache_rows;
+                if (!ok) flag_error(p.err, DS_ERR_POSITION);
+                const int row0 = ok ? (int)(blk * kPaBt) : 0;
+                for (int kv = 0; kv < 2; ++kv, ++fill) {
+                    const int st = fill % stages;
+                    const uint32_t use = fill / stages;
+                    if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, p.err)) {
+                        s_abort = 1;
+                        goto drain;
+                    }
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)stage_bytes);
+                    const CUtensorMap *map = kv ? &p.tv : &p.tk;
+                    unsigned char *dst = smem + (size_t)st * stage_bytes;
+                    for (int g = 0; g < n_kvh; ++g)
+                        for (int h = 0; h < 2; ++h)
+                            tma_box_g2s(dst + g * 4096 + h * 2048, map, g * kPaHd + h * 64, row0, &full[st], pol);
                 }
-                const long long o = ((long long)s * p.n_qh + h) * kPaHd + lane * 4;
+            }
+        drain:
+            const uint32_t first = fill > (uint32_t)stages ? fill - stages : 0;
+            for (uint32_t f = first; f < fill; ++f)
+                if (!mbar_wait(&full[f % stages], (f / stages) & 1, p.err)) break;
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumers: warp g = KV head g
+    constexpr int NC = 2 * GQ;          // columns in use: GQ hi, then GQ lo
+    constexpr int PD = GQ / 2;          // lane distance between a hi column and its lo column
+    const int g = warp;
+    const int q4 = lane & 3, r8 = lane >> 2;
+    // columns of this lane in the C fragments: 2 q4, 2 q4 + 1
+    const bool use_lane = 2 * q4 < NC;           // lanes past the used columns hold padding
+    const int hA = (2 * q4) % GQ, hB = hA + 1;   // heads of the lane's two columns
+    const bool lo_part = 2 * q4 >= GQ && use_lane;
+    __nv_bfloat16 *ptab = ptab_all + warp * 8 * kPaBt;
+    const uint32_t st_base = smem_u32(smem);
+    const float scale = p.scale;
+    const int rec = kPaHd + 2;
+    uint32_t fill = 0;
+    int s = u0 < u1 ? seq_of(u0) : 0;
+    long long u = u0;
+    while (u < u1) {
+        while (u >= sq.first[s + 1]) ++s;
+        const long long seg_end = min(u1, (long long)sq.first[s + 1]);
+        const int n_ctx = sq.n_ctx[s];
+        // Q^T fragments: column n = r8 (head n hi, head n - GQ lo, else 0), dims 16 t + 2 q4 + {0, 1} (+ 8)
+        uint32_t qb[8][2];
+        {
+            const int n = r8;
+            const int head = n < GQ ? n : n - GQ;
+            const bool have = n < NC;
+            const float *qr = p.q + ((long long)s * p.n_qh + g * GQ + (have ? head : 0)) * kPaHd;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float r1 = A[e] / L;
-                    p.out[o + e] = r1;
-                    if (p.out_bf16) {
-                        __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(p.out_bf16);
-                        const __nv_bfloat16 hi = __float2bfloat16_rn(r1);
-                        ob[o + e] = hi;
-                        if (p.out_bf16_lo) ob[o + e + p.out_bf16_lo] = __float2bfloat16_rn(r1 - __bfloat162float(hi));
+            for (int t = 0; t < 8; ++t) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int d = 16 * t + 2 * q4 + 8 * k;
+                    const float2 v = have ? __ldg(reinterpret_cast<const float2 *>(qr + d)) : make_float2(0.f, 0.f);
+                    const __nv_bfloat16 h0 = __float2bfloat16_rn(v.x), h1 = __float2bfloat16_rn(v.y);
+                    if (n < GQ) {
+                        qb[t][k] = pack_bf16(h0, h1);
+                    } else {
+                        qb[t][k] = pack_bf16(__float2bfloat16_rn(v.x - __bfloat162float(h0)),
+                                             __float2bfloat16_rn(v.y - __bfloat162float(h1)));
                     }
                 }
             }
         }
+        float acc[8][4];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[t][e] = 0.0f;
+        float mA = -INFINITY, mB = -INFINITY, lA = 0.0f, lB = 0.0f;
+        for (; u < seg_end; ++u) {
+            const int b = (int)(u - sq.first[s]);
+            const int valid = min(kPaBt, n_ctx - b * kPaBt);
+            // ---- scores: S^T[pos][col] over the 8 dim slices
+            int st = fill % stages;
+            bool ok = !s_abort && mbar_wait(&full[st], (fill / stages) & 1, p.err);
+            if (!ok) s_abort = 1;
+            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            {
+                const uint32_t base = st_base + (uint32_t)(st * stage_bytes);
+                const int pos = (lane & 7) + 8 * ((lane >> 3) & 1), dsub = 8 * (lane >> 4);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    uint32_t a[4];
+                    ldsm_x4(a, base + pa_swz(g, pos, 16 * t + dsub));
+                    mma_bf16_16816(c, a, qb[t][0], qb[t][1]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            ++fill;
+            // hi + lo columns; rows r8 and r8 + 8 are positions
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[e] += __shfl_xor_sync(0xffffffffu, c[e], PD);
+            const bool in0 = r8 < valid, in1 = r8 + 8 < valid;
+            float sA0 = in0 ? c[0] * scale : -INFINITY, sB0 = in0 ? c[1] * scale : -INFINITY;
+            float sA1 = in1 ? c[2] * scale : -INFINITY, sB1 = in1 ? c[3] * scale : -INFINITY;
+            float bA = fmaxf(sA0, sA1), bB = fmaxf(sB0, sB1);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, o));
+                bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, o));
+            }
+            const float nA = fmaxf(mA, bA), nB = fmaxf(mB, bB);
+            const float cA = mA == -INFINITY ? 0.0f : expf(mA - nA), cB = mB == -INFINITY ? 0.0f : expf(mB - nB);
+            mA = nA;
+            mB = nB;
+            const float pA0 = in0 ? expf(sA0 - nA) : 0.0f, pB0 = in0 ? expf(sB0 - nB) : 0.0f;
+            const float pA1 = in1 ? expf(sA1 - nA) : 0.0f, pB1 = in1 ? expf(sB1 - nB) : 0.0f;
+            float sumA = pA0 + pA1, sumB = pB0 + pB1;
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                sumA += __shfl_xor_sync(0xffffffffu, sumA, o);
+                sumB += __shfl_xor_sync(0xffffffffu, sumB, o);
+            }
+            lA = lA * cA + sumA;
+            lB = lB * cB + sumB;
+            // P^T table [column][position]: hi parts in columns hA, hB; lo parts GQ further
+            if (use_lane) {
+                const float pv[4] = {pA0, pB0, pA1, pB1};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = (e & 1) ? hB : hA, pos = r8 + 8 * (e >> 1);
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(pv[e]);
+                    const __nv_bfloat16 w = lo_part ? __float2bfloat16_rn(pv[e] - __bfloat162float(hi)) : hi;
+                    ptab[(col + (lo_part ? GQ : 0)) * kPaBt + pos] = w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ptab[(2 * q4 + (e & 1)) * kPaBt + r8 + 8 * (e >> 1)] = __float2bfloat16_rn(0.0f);
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                acc[t][0] *= cA;
+                acc[t][1] *= cB;
+                acc[t][2] *= cA;
+                acc[t][3] *= cB;
+            }
+            __syncwarp();
+            // ---- output: O^T[dims][col] += V^T . P^T
+            const uint32_t pb0 = *reinterpret_cast<const uint32_t *>(ptab + r8 * kPaBt + 2 * q4);
+            const uint32_t pb1 = *reinterpret_cast<const uint32_t *>(ptab + r8 * kPaBt + 2 * q4 + 8);
+            st = fill % stages;
+            ok = !s_abort && mbar_wait(&full[st], (fill / stages) & 1, p.err);
+            if (!ok) s_abort = 1;
+            {
+                const uint32_t base = st_base + (uint32_t)(st * stage_bytes);
+                const int pos = (lane & 7) + 8 * (lane >> 4), dsub = 8 * ((lane >> 3) & 1);
+                // rows past the context may hold anything: their weights are 0, but 0 x NaN is not
+                const bool row_ok = pos < valid;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    uint32_t a[4];
+                    ldsm_x4_trans(a, base + pa_swz(g, pos, 16 * t + dsub));
+                    if (valid < kPaBt) {
+                        // zero the elements that came from rows past the context: a[e] holds
+                        // positions 2 q4 + {0,1} (a0, a1) and 2 q4 + 8 + {0,1} (a2, a3)
+                        const int p0 = 2 * q4, p1 = 2 * q4 + 8;
+                        const uint32_t m0 = (p0 < valid ? 0xffffu : 0u) | (p0 + 1 < valid ? 0xffff0000u : 0u);
+                        const uint32_t m1 = (p1 < valid ? 0xffffu : 0u) | (p1 + 1 < valid ? 0xffff0000u : 0u);
+                        a[0] &= m0;
+                        a[1] &= m0;
+                        a[2] &= m1;
+                        a[3] &= m1;
+                    }
+                    mma_bf16_16816(acc[t], a, pb0, pb1);
+                }
+                (void)row_ok;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            ++fill;
+        }
+        // hi + lo columns of the output; the hi lanes write the record
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[t][e] += __shfl_xor_sync(0xffffffffu, acc[t][e], PD);
+        float *slot = p.partials + ((size_t)blockIdx.x + s) * p.n_qh * rec;
+        if (use_lane && !lo_part) {
+            float *rA = slot + (size_t)(g * GQ + hA) * rec, *rB = slot + (size_t)(g * GQ + hB) * rec;
+            if (r8 == 0) {
+                rA[0] = mA;
+                rA[1] = lA;
+                rB[0] = mB;
+                rB[1] = lB;
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                rA[2 + 16 * t + r8] = acc[t][0];
+                rB[2 + 16 * t + r8] = acc[t][1];
+                rA[2 + 16 * t + r8 + 8] = acc[t][2];
+                rB[2 + 16 * t + r8 + 8] = acc[t][3];
+            }
+        }
+        pa_finish_sequence<GQ>(p, s, g, sq.first[s], sq.first[s + 1] - 1, Ge, T);
     }
 }
 
@@ -412,6 +728,22 @@ size_t paged_attention_partial_floats(int n_seqs, int n_qh) {
     return (size_t)(sm_count() + n_seqs) * n_qh * (kPaHd + 2);
 }
 
+bool paged_attention_maps(PagedAttnArgs &a) {
+    return encode_tiled_2d(&a.tk, a.k_cache, DS_BF16, (long long)a.n_kvh * kPaHd, a.cache_rows,
+                           (long long)a.n_kvh * kPaHd * 2, 64, kPaBt, true) &&
+           encode_tiled_2d(&a.tv, a.v_cache, DS_BF16, (long long)a.n_kvh * kPaHd, a.cache_rows,
+                           (long long)a.n_kvh * kPaHd * 2, 64, kPaBt, true);
+}
+
+template <int GQ>
+static cudaError_t launch_pa_tc(PagedAttnArgs a, cudaStream_t stream, bool pdl) {
+    const int stage_bytes = a.n_kvh * 4096;
+    a.stages = std::min(16, kPaRingBytes / stage_bytes);
+    const size_t smem = 1024 + (size_t)a.stages * stage_bytes + 256 + (size_t)a.n_kvh * 8 * kPaBt * 2;
+    if (smem > kPaSmemLimit) return cudaErrorInvalidValue;
+    return launch_ex(paged_attention_tc_kernel<GQ>, dim3(sm_count()), dim3(a.n_kvh * 32 + 32), smem, stream, pdl, a);
+}
+
 template <typename KT, int GQ>
 static cudaError_t launch_pa(PagedAttnArgs a, cudaStream_t stream, bool pdl) {
     const int es = sizeof(KT);
@@ -425,8 +757,7 @@ static cudaError_t launch_pa(PagedAttnArgs a, cudaStream_t stream, bool pdl) {
 static bool g_pa_ready = false;
 
 cudaError_t prepare_paged_attention() {
-    const void *fns[] = {(const void *)paged_attention_kernel<__nv_bfloat16, 2>,
-                         (const void *)paged_attention_kernel<__nv_bfloat16, 4>,
+    const void *fns[] = {(const void *)paged_attention_tc_kernel<2>, (const void *)paged_attention_tc_kernel<4>,
                          (const void *)paged_attention_kernel<float, 2>, (const void *)paged_attention_kernel<float, 4>};
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPaSmemLimit);
@@ -442,10 +773,10 @@ cudaError_t launch_paged_attention(const PagedAttnArgs &a, cudaStream_t stream, 
         if (e != cudaSuccess) return e;
     }
     const int gq = a.n_qh / a.n_kvh;
-    if (a.kv_dtype == DS_BF16) {
+    if (a.kv_dtype == DS_BF16) {  // a.tk / a.tv encoded by paged_attention_maps
         switch (gq) {
-            case 2: return launch_pa<__nv_bfloat16, 2>(a, stream, pdl);
-            case 4: return launch_pa<__nv_bfloat16, 4>(a, stream, pdl);
+            case 2: return launch_pa_tc<2>(a, stream, pdl);
+            case 4: return launch_pa_tc<4>(a, stream, pdl);
         }
     } else {
         switch (gq) {

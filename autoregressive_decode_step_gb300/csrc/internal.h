@@ -151,6 +151,7 @@ struct AttnArgs {
 // Paged flash-decoding over whole cache blocks (head_dim 128, 16-position
 // blocks, 2 or 4 query heads per KV head, at most 8 KV heads).
 struct PagedAttnArgs {
+    CUtensorMap tk, tv;    // bf16 caches: 2-D maps {n_kvh * 128, cache_rows}, boxes {64, 16}, 128-byte swizzle
     const float *q;        // [n_seqs][n_qh * 128]
     const void *k_cache;   // rows of n_kvh * 128 elements of kv_dtype
     const void *v_cache;
@@ -171,6 +172,8 @@ struct PagedAttnArgs {
     int stages;            // set by the launcher
 };
 bool paged_attention_supported(int n_qh, int n_kvh, int hd, int block_tokens, int n_seqs, int kv_dtype);
+// Encode a.tk / a.tv for bf16 caches (the tensor-core variant); false if the driver refuses.
+bool paged_attention_maps(PagedAttnArgs &a);
 size_t paged_attention_partial_floats(int n_seqs, int n_qh);
 cudaError_t launch_paged_attention(const PagedAttnArgs &a, cudaStream_t stream, bool pdl);
 cudaError_t prepare_paged_attention();

@@ -68,6 +68,11 @@ struct ds_model {
     void *h_bf, *att_bf, *f_bf;  // projection inputs as bf16 pairs: [2][max_seqs][d | nq | ff], hi then lo
     int *b_am_counters;          // argmax arrival counters, one per sequence
     std::vector<ds::TcArgs> tc;  // per layer: q|k|v, o, gate|up, down; then the head
+    // tensor maps of the K/V buffers for the paged attention, per layer, and
+    // the cache they were encoded for (re-encoded when a step passes another)
+    std::vector<CUtensorMap> pa_maps;
+    std::vector<const void *> pa_k, pa_v;
+    std::vector<long long> pa_rows;
 };
 
 struct ds_step_graph {
@@ -780,6 +785,29 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
         DS_TRYB(gemm(a));
         if (paged_attention_supported(c.n_qh, c.n_kvh, c.head_dim, kv->block_tokens, n, c.kv_dtype)) {
             PagedAttnArgs pa = {};
+            if (c.kv_dtype == DS_BF16) {
+                if (m->pa_maps.empty()) {
+                    m->pa_maps.resize((size_t)2 * c.n_layer);
+                    m->pa_k.assign(c.n_layer, nullptr);
+                    m->pa_v.assign(c.n_layer, nullptr);
+                    m->pa_rows.assign(c.n_layer, -1);
+                }
+                if (m->pa_k[l] != kv->k[l] || m->pa_v[l] != kv->v[l] || m->pa_rows[l] != kv->rows) {
+                    PagedAttnArgs enc = {};
+                    enc.k_cache = kv->k[l];
+                    enc.v_cache = kv->v[l];
+                    enc.n_kvh = c.n_kvh;
+                    enc.cache_rows = kv->rows;
+                    if (!paged_attention_maps(enc)) return DS_CUDA_ERROR;
+                    m->pa_maps[2 * l] = enc.tk;
+                    m->pa_maps[2 * l + 1] = enc.tv;
+                    m->pa_k[l] = kv->k[l];
+                    m->pa_v[l] = kv->v[l];
+                    m->pa_rows[l] = kv->rows;
+                }
+                pa.tk = m->pa_maps[2 * l];
+                pa.tv = m->pa_maps[2 * l + 1];
+            }
             pa.q = m->q;
             pa.k_cache = kv->k[l];
             pa.v_cache = kv->v[l];
