@@ -524,9 +524,18 @@ __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_tc_ker
                     mbar_arrive_expect_tx(&full[st], (uint32_t)stage_bytes);
                     const CUtensorMap *map = kv ? &p.tv : &p.tk;
                     unsigned char *dst = smem + (size_t)st * stage_bytes;
-                    for (int g = 0; g < n_kvh; ++g)
-                        for (int h = 0; h < 2; ++h)
-                            tma_box_g2s(dst + g * 4096 + h * 2048, map, g * kPaHd + h * 64, row0, &full[st], pol);
+                    if (p.box3d) {  // the whole block in one box: [head half][16 positions][64 dims]
+                        asm volatile(
+                            "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                            " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+                            "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row0), "r"(0), "r"(smem_u32(&full[st])),
+                            "l"(pol)
+                            : "memory");
+                    } else {
+                        for (int g = 0; g < n_kvh; ++g)
+                            for (int h = 0; h < 2; ++h)
+                                tma_box_g2s(dst + g * 4096 + h * 2048, map, g * kPaHd + h * 64, row0, &full[st], pol);
+                    }
                 }
             }
         drain:
@@ -729,10 +738,22 @@ size_t paged_attention_partial_floats(int n_seqs, int n_qh) {
 }
 
 bool paged_attention_maps(PagedAttnArgs &a) {
-    return encode_tiled_2d(&a.tk, a.k_cache, DS_BF16, (long long)a.n_kvh * kPaHd, a.cache_rows,
-                           (long long)a.n_kvh * kPaHd * 2, 64, kPaBt, true) &&
-           encode_tiled_2d(&a.tv, a.v_cache, DS_BF16, (long long)a.n_kvh * kPaHd, a.cache_rows,
-                           (long long)a.n_kvh * kPaHd * 2, 64, kPaBt, true);
+    // one box per block: dims {64 dims, positions, head halves}, the halves 128 bytes apart
+    const long long row_bytes = (long long)a.n_kvh * kPaHd * 2;
+    const long long dims[3] = {64, a.cache_rows, 2LL * a.n_kvh};
+    const long long strides[2] = {row_bytes, 128};
+    const int box[3] = {64, kPaBt, 2 * a.n_kvh};
+    if (encode_tiled_3d(&a.tk, a.k_cache, DS_BF16, dims, strides, box, true) &&
+        encode_tiled_3d(&a.tv, a.v_cache, DS_BF16, dims, strides, box, true)) {
+        a.box3d = 1;
+        return true;
+    }
+    // else sixteen 2-D boxes per block
+    a.box3d = 0;
+    return encode_tiled_2d(&a.tk, a.k_cache, DS_BF16, (long long)a.n_kvh * kPaHd, a.cache_rows, row_bytes, 64, kPaBt,
+                           true) &&
+           encode_tiled_2d(&a.tv, a.v_cache, DS_BF16, (long long)a.n_kvh * kPaHd, a.cache_rows, row_bytes, 64, kPaBt,
+                           true);
 }
 
 template <int GQ>

@@ -404,6 +404,20 @@ bool encode_tiled_2d(CUtensorMap *m, const void *base, int dtype, long long cols
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tiled_3d(CUtensorMap *m, const void *base, int dtype, const long long dims[3], const long long strides[2],
+                     const int box[3], bool swizzle128) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t d[3] = {(cuuint64_t)dims[0], (cuuint64_t)dims[1], (cuuint64_t)dims[2]};
+    const cuuint64_t st[2] = {(cuuint64_t)strides[0], (cuuint64_t)strides[1]};
+    const cuuint32_t bx[3] = {(cuuint32_t)box[0], (cuuint32_t)box[1], (cuuint32_t)box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = dtype == DS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return fn(m, dt, 3, const_cast<void *>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool gemv_t_make_maps(GemvTArgs &a, int dtype) {
     const int es = dtype == DS_BF16 ? 2 : 4;
     const int band_cols = gemv_t_band_cols(es);

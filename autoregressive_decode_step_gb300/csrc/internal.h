@@ -151,7 +151,9 @@ struct AttnArgs {
 // Paged flash-decoding over whole cache blocks (head_dim 128, 16-position
 // blocks, 2 or 4 query heads per KV head, at most 8 KV heads).
 struct PagedAttnArgs {
-    CUtensorMap tk, tv;    // bf16 caches: 2-D maps {n_kvh * 128, cache_rows}, boxes {64, 16}, 128-byte swizzle
+    CUtensorMap tk, tv;    // bf16 caches, 128-byte swizzle: 3-D maps {64, cache_rows, 2 n_kvh} with one box per
+                           // block (box3d), else 2-D maps {n_kvh * 128, cache_rows} with boxes {64, 16}
+    int box3d;
     const float *q;        // [n_seqs][n_qh * 128]
     const void *k_cache;   // rows of n_kvh * 128 elements of kv_dtype
     const void *v_cache;

@@ -71,6 +71,7 @@ struct ds_model {
     // tensor maps of the K/V buffers for the paged attention, per layer, and
     // the cache they were encoded for (re-encoded when a step passes another)
     std::vector<CUtensorMap> pa_maps;
+    std::vector<int> pa_box3d;
     std::vector<const void *> pa_k, pa_v;
     std::vector<long long> pa_rows;
 };
@@ -791,6 +792,7 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
                     m->pa_k.assign(c.n_layer, nullptr);
                     m->pa_v.assign(c.n_layer, nullptr);
                     m->pa_rows.assign(c.n_layer, -1);
+                    m->pa_box3d.assign(c.n_layer, 0);
                 }
                 if (m->pa_k[l] != kv->k[l] || m->pa_v[l] != kv->v[l] || m->pa_rows[l] != kv->rows) {
                     PagedAttnArgs enc = {};
@@ -801,12 +803,14 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
                     if (!paged_attention_maps(enc)) return DS_CUDA_ERROR;
                     m->pa_maps[2 * l] = enc.tk;
                     m->pa_maps[2 * l + 1] = enc.tv;
+                    m->pa_box3d[l] = enc.box3d;
                     m->pa_k[l] = kv->k[l];
                     m->pa_v[l] = kv->v[l];
                     m->pa_rows[l] = kv->rows;
                 }
                 pa.tk = m->pa_maps[2 * l];
                 pa.tv = m->pa_maps[2 * l + 1];
+                pa.box3d = m->pa_box3d[l];
             }
             pa.q = m->q;
             pa.k_cache = kv->k[l];

@@ -14,6 +14,10 @@ namespace ds {
 bool encode_tiled_2d(CUtensorMap *map, const void *base, int dtype, long long cols, long long rows,
                      long long row_stride, int box_cols, int box_rows, bool swizzle128);
 
+// The same for a 3-D map: dims[0] innermost, strides in bytes of dims 1 and 2.
+bool encode_tiled_3d(CUtensorMap *map, const void *base, int dtype, const long long dims[3], const long long strides[2],
+                     const int box[3], bool swizzle128);
+
 // Fused epilogues of the batched projection kernel.
 enum { TC_STORE = 0, TC_ADD = 1, TC_SILU = 2, TC_QKV = 3 };
 
