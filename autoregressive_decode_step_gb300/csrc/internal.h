@@ -259,7 +259,10 @@ struct StepParams {
     float *am_val;
     int *am_idx;
     int *am_counter;
-    unsigned long long *epoch;  // launches completed (tags derive from it)
+    unsigned long long *epoch;  // steps completed (tags derive from it)
+    int n_steps;                // greedy steps this launch decodes (tokens hand over on the device)
+    int *ids_out;               // optional: the id picked at every step [n_steps]
+    unsigned long long *tokt;   // tagged word: a step's pick, read by the next step's embed
     int *err;
     int *abort_flag;
     unsigned long long *phase_times;  // optional: globaltimer at every phase start, then at the end

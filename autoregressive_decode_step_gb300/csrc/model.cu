@@ -198,7 +198,7 @@ Layout make_layout(const ds_model_config *c) {
     L.am_idx = carve(off, am_slots * 4);
     L.am_counter = carve(off, 4);
     L.step_layers = carve(off, (size_t)std::max(c->n_layer, 1) * step_layer_bytes());
-    L.step_bar = carve(off, 32);  // arrival count (u64), epoch (u64), abort flag
+    L.step_bar = carve(off, 32);  // arrival count (u64), epoch (u64), abort flag (int, + pad), handed-over token (u64)
     L.phase_times = carve(off, (size_t)L.n_phase_times * 8);
     L.trace = carve(off, (size_t)L.n_phase_times * L.step_grid * 5 * 8);
     if (L.step_ok) {
@@ -664,7 +664,7 @@ extern "C" DS_API void *ds_model_workspace(ds_model *m) { return m ? m->ws : nul
 // One step through the persistent step kernel (and the sampler after it).
 int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
                    const ds_sampling *sampling, const float *u, int32_t *next_ids, float *logits_out, unsigned flags,
-                   cudaStream_t s) {
+                   cudaStream_t s, int n_steps = 1, int32_t *ids_out = nullptr) {
     const ds_model_config &c = m->cfg;
     const bool greedy = sampling == nullptr || !(sampling->temperature > 0.0f);
     const bool advance = (flags & DS_STEP_ADVANCE) != 0;
@@ -712,10 +712,13 @@ int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t 
     p.am_idx = m->am_idx;
     p.am_counter = m->am_counter;
     p.epoch = reinterpret_cast<unsigned long long *>(m->step_bar) + 1;
+    p.n_steps = n_steps;
+    p.ids_out = ids_out;
+    p.tokt = reinterpret_cast<unsigned long long *>(m->step_bar) + 3;
     p.err = m->err;
     p.abort_flag = m->step_abort;
-    p.phase_times = (flags & (DS_STEP_PHASE_TIMES | DS_STEP_TRACE)) ? m->phase_times : nullptr;
-    p.trace = (flags & DS_STEP_TRACE) ? m->trace : nullptr;
+    p.phase_times = (n_steps == 1 && (flags & (DS_STEP_PHASE_TIMES | DS_STEP_TRACE))) ? m->phase_times : nullptr;
+    p.trace = (n_steps == 1 && (flags & DS_STEP_TRACE)) ? m->trace : nullptr;
     p.nb_qkv = m->nb_qkv;
     p.nb_o = m->nb_o;
     p.nb_gu = m->nb_gu;
@@ -925,6 +928,17 @@ extern "C" DS_API int ds_decode_step(ds_model *m, const ds_kv_cache *kv, int32_t
     if (st != DS_OK) return st;
     return dispatch_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" DS_API int ds_decode_steps(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos,
+                                      int n_steps, int32_t *ids_out, int32_t *next_ids, unsigned flags,
+                                      ds_stream_t stream) {
+    if (n_steps < 1) return DS_EMPTY_DIMENSION;
+    int st = check_step(m, kv, tokens, pos, 1, nullptr, nullptr, next_ids);
+    if (st != DS_OK) return st;
+    if (!m->step_ok || m->batched) return DS_BAD_ARGUMENT;  // the persistent batch-1 kernel only
+    return run_step_fused(m, kv, tokens, pos, 1, nullptr, nullptr, next_ids, nullptr, flags & DS_STEP_ADVANCE,
+                          reinterpret_cast<cudaStream_t>(stream), n_steps, ids_out);
 }
 
 extern "C" DS_API int ds_model_phase_times(ds_model *m, uint64_t *ns_out, int cap, int *n_out, ds_stream_t stream) {

@@ -239,18 +239,24 @@ __device__ __forceinline__ void issue_stage(const StageDesc &d, unsigned char *d
 template <int ES>
 __device__ void produce_all(const Ring &r, const StepParams &p) {
     const uint64_t pol = policy_evict_first();
-    StageCursor fc;
-    cursor_begin<ES>(fc, p);
     uint32_t fill = 0;
-    StageDesc d;
-    while (cursor_desc<ES>(fc, p, d)) {
-        const int s = fill % r.stages;
-        const uint32_t use = fill / r.stages;
-        if (use > 0 && !st_wait(&r.empty[s], (use - 1) & 1, p)) break;
-        mbar_arrive_expect_tx(&r.full[s], d.bytes);
-        issue_stage(d, r.base + (size_t)s * kStStageBytes, &r.full[s], pol);
-        cursor_advance<ES>(fc, p);
-        ++fill;
+    bool ok = true;
+    for (int step = 0; step < p.n_steps && ok; ++step) {  // weights do not depend on the token
+        StageCursor fc;
+        cursor_begin<ES>(fc, p);
+        StageDesc d;
+        while (cursor_desc<ES>(fc, p, d)) {
+            const int s = fill % r.stages;
+            const uint32_t use = fill / r.stages;
+            if (use > 0 && !st_wait(&r.empty[s], (use - 1) & 1, p)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(&r.full[s], d.bytes);
+            issue_stage(d, r.base + (size_t)s * kStStageBytes, &r.full[s], pol);
+            cursor_advance<ES>(fc, p);
+            ++fill;
+        }
     }
     const uint32_t first = fill > (uint32_t)r.stages ? fill - r.stages : 0;
     for (uint32_t f = first; f < fill; ++f)
@@ -774,6 +780,21 @@ __device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *
     };
     int tb = t0 + warp * RUN;
     if (tb < tc) load_run(tb);  // K/V requests go out before q is polled
+    // the current position's k and v (handed over by the q|k|v phase), read by
+    // the last warp: requested now, their arrival checked after the cached run
+    const bool cur_warp = has_cur && warp == kStConsumerWarps - 1;
+    u64 cw[8];
+    const u64 *ca[8];
+    {
+        const u64 *kt = p.kvt + (size_t)g * hd + d0, *vt = p.kvt + p.nkv_cols + (size_t)g * hd + d0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            ca[e] = cur_warp && active ? kt + e : nullptr;
+            ca[4 + e] = cur_warp && active ? vt + e : nullptr;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cw[e] = ca[e] ? ld_tag(ca[e]) : 0ull;
+    }
     {   // the group's q rows, polled once by the whole CTA into shared memory
         const u64 *qg = p.qt + (size_t)g * GQ * hd;
         for (int i0 = 0; i0 < GQ * hd; i0 += 2 * kStConsumers) {
@@ -838,22 +859,12 @@ __device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *
         tb += kStConsumerWarps * RUN;
         if (tb < tc) load_run(tb);
     }
-    if (has_cur && warp == kStConsumerWarps - 1) {  // the current position
-        const u64 *kt = p.kvt + (size_t)g * hd + d0, *vt = p.kvt + p.nkv_cols + (size_t)g * hd + d0;
-        u64 w[8];
-        const u64 *a[8];
+    if (cur_warp) {  // the current position
+        tag_fix_at<8>(cw, ca, q_tag, p);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            a[e] = active ? kt + e : nullptr;
-            a[4 + e] = active ? vt + e : nullptr;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = a[e] ? ld_tag(a[e]) : 0ull;
-        tag_fix_at<8>(w, a, q_tag, p);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            kf[0][e] = active ? tag_f(w[e]) : 0.0f;
-            vf[0][e] = active ? tag_f(w[4 + e]) : 0.0f;
+            kf[0][e] = active ? tag_f(cw[e]) : 0.0f;
+            vf[0][e] = active ? tag_f(cw[4 + e]) : 0.0f;
         }
         update(1);
     }
@@ -954,10 +965,40 @@ __device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, uint
     named_sync(1, kStConsumers);
 }
 
+// The best (value, index) of the 256 consumer threads' candidates under
+// ranks_above, left in every thread: a shuffle tree per warp, then over the
+// eight warps' winners (sv/si: 8 entries of shared scratch).
+__device__ void block_best(float &bv, int &bi, float *sv, int *si) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ranks_above(ov, oi, bv, bi)) {
+            bv = ov;
+            bi = oi;
+        }
+    }
+    if (lane == 0) {
+        sv[warp] = bv;
+        si[warp] = bi;
+    }
+    named_sync(1, kStConsumers);
+    bv = sv[0];
+    bi = si[0];
+    for (int w = 1; w < kStConsumerWarps; ++w)
+        if (ranks_above(sv[w], si[w], bv, bi)) {
+            bv = sv[w];
+            bi = si[w];
+        }
+    named_sync(1, kStConsumers);
+}
+
 // The head phase: logits of this CTA's rows, then (once every CTA has
 // finished) the greedy pick and the launch's epoch advance.
 template <typename T>
-__device__ void consume_gn(const Ring &r, uint32_t &fill, uint32_t in_tag, float *scratch, const StepParams &p) {
+__device__ void consume_gn(const Ring &r, uint32_t &fill, uint32_t in_tag, float *scratch, const StepParams &p,
+                           int step, int phase) {
     constexpr int LE = 16 / sizeof(T);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int G = gridDim.x;
@@ -970,6 +1011,7 @@ __device__ void consume_gn(const Ring &r, uint32_t &fill, uint32_t in_tag, float
     int *besti = reinterpret_cast<int *>(bestv + 256);   // [256]
     float *xs = bestv + 512;                             // [cols]
     float *rowpart = xs + cols;                          // [rows of this CTA][parts]
+    trace_point(p, phase, 0);
 
     for (int i0 = 0; i0 < cols; i0 += 8 * kStConsumers) {
         u64 v[8];
@@ -988,6 +1030,7 @@ __device__ void consume_gn(const Ring &r, uint32_t &fill, uint32_t in_tag, float
     }
     named_sync(1, kStConsumers);
     const float scale = scale_from_sst(p, cols, in_tag, bestv);
+    trace_point(p, phase, 1);
 
     const int chunks = (int)(row_bytes / 16);
     for (int rr = r0; rr < r1; rr += rps) {
@@ -1034,6 +1077,7 @@ __device__ void consume_gn(const Ring &r, uint32_t &fill, uint32_t in_tag, float
         ++fill;
     }
     named_sync(1, kStConsumers);
+    trace_point(p, phase, 2);
 
     float bv = -INFINITY;
     int bi = INT_MAX;
@@ -1047,42 +1091,55 @@ __device__ void consume_gn(const Ring &r, uint32_t &fill, uint32_t in_tag, float
             bi = r0 + q;
         }
     }
-    bestv[t] = bv;
-    besti[t] = bi;
-    named_sync(1, kStConsumers);
+    // this CTA's best row: a tree over the 256 consumer threads (ranks_above is
+    // a total order, so any tree gives the first index of the maximum)
+    block_best(bv, bi, bestv, besti);
+    __shared__ int s_last;
     if (t == 0) {
-        bv = bestv[0];
-        bi = besti[0];
-        for (int j = 1; j < kStConsumers; ++j)
-            if (ranks_above(bestv[j], besti[j], bv, bi)) {
-                bv = bestv[j];
-                bi = besti[j];
-            }
         p.am_val[blockIdx.x] = bv;
         p.am_idx[blockIdx.x] = bi;
+        trace_point(p, phase, 3);
         __threadfence();
-        if (atomicAdd(p.am_counter, 1) == G - 1) {  // every CTA is done with the step
-            __threadfence();
-            if (p.greedy) {
-                bv = ldcg(&p.am_val[0]);
-                bi = __ldcg(&p.am_idx[0]);
-                for (int j = 1; j < G; ++j) {
-                    const float v = ldcg(&p.am_val[j]);
-                    const int ix = __ldcg(&p.am_idx[j]);
-                    if (ranks_above(v, ix, bv, bi)) {
-                        bv = v;
-                        bi = ix;
-                    }
-                }
-                p.next_ids[0] = bi;
-                if (p.advance) {
-                    p.tokens[0] = bi;
-                    p.pos[0] += 1;
-                }
+        const int last = atomicAdd(p.am_counter, 1) == G - 1;  // every CTA is done with the step
+        if (last) *p.am_counter = 0;
+        s_last = last;
+    }
+    named_sync(1, kStConsumers);
+    const bool last = s_last != 0;
+    named_sync(1, kStConsumers);
+    if (!last) return;
+    __threadfence();
+    // the step's pick: every CTA's best, read in parallel
+    bv = -INFINITY;
+    bi = INT_MAX;
+    if (p.greedy) {
+        for (int j = t; j < G; j += kStConsumers) {
+            const float v = ldcg(&p.am_val[j]);
+            const int ix = __ldcg(&p.am_idx[j]);
+            if (ranks_above(v, ix, bv, bi)) {
+                bv = v;
+                bi = ix;
             }
-            *p.am_counter = 0;
-            // every CTA read this launch's epoch at its start: advance it
-            asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(p.epoch) : "memory");
+        }
+        block_best(bv, bi, bestv, besti);
+    }
+    if (t == 0) {
+        if (p.greedy) {
+            p.next_ids[0] = bi;
+            if (p.ids_out) p.ids_out[step] = bi;
+            if (p.advance) {
+                p.tokens[0] = bi;
+                p.pos[0] += 1;
+            }
+        }
+        if (step + 1 < p.n_steps) {
+            // the next step's embed waits for this word; the counter reset above
+            // is visible before it is
+            __threadfence();
+            st_tag(p.tokt, __int_as_float(bi), in_tag);
+        } else {
+            // every CTA read the epoch at its start: advance it past this launch's steps
+            asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p.epoch), "l"((u64)p.n_steps) : "memory");
         }
     }
 }
@@ -1135,13 +1192,29 @@ __global__ void __launch_bounds__(kStThreads, 1) step_kernel(const __grid_consta
         named_sync(1, kStConsumers);
     }
     const int cap = p.max_blocks * p.block_tokens;
+    const int pos0 = cx.pos;
+    const uint32_t epoch0 = cx.seq.base >> 10;
+    uint32_t fill = 0;
+    for (int step = 0; step < p.n_steps; ++step) {
+    cx.seq.base = ((epoch0 + (uint32_t)step) & 0x3FFFFFu) << 10;
+    cx.pos = pos0 + step;
     cx.pos_ok = cx.pos >= 0 && cx.pos < p.rope_rows && cx.pos < cap;
     if (!cx.pos_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_error(p.err, DS_ERR_POSITION);
     cx.n_ctx = min(max(cx.pos + 1, 1), cap);
+    if (step > 0) {  // the previous step's pick, handed over as a tagged word
+        __shared__ int s_next;
+        if (threadIdx.x == 0) {
+            const Seq prev{((epoch0 + (uint32_t)step - 1u) & 0x3FFFFFu) << 10};
+            s_next = __float_as_int(ld_wait(p.tokt, prev(5 * p.n_layer), p));
+        }
+        named_sync(1, kStConsumers);
+        tok = s_next;
+        named_sync(1, kStConsumers);
+    }
 
     int phase = 0;
-    uint32_t fill = 0;
     mark_phase(p, phase);
+    trace_point(p, 0, 0);
     {   // embed (phase id 0): x = E[token]; every CTA writes a slice
         if (tok < 0 || tok >= p.vocab) {
             if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(p.err, DS_ERR_TOKEN_RANGE);
@@ -1161,6 +1234,7 @@ __global__ void __launch_bounds__(kStThreads, 1) step_kernel(const __grid_consta
             if (threadIdx.x == 0) st_tag(p.sst + b, ss, tag);
         }
     }
+    trace_point(p, 0, 3);
     for (int l = 0; l < p.n_layer; ++l) {
         const StepLayer &L = p.layers[l];
         const int ph = ph_qkv(l);
@@ -1182,8 +1256,9 @@ __global__ void __launch_bounds__(kStThreads, 1) step_kernel(const __grid_consta
                                              cx.seq(ph + 2), l, ph + 4, cx, scratch, p, phase - 1);
     }
     mark_phase(p, phase);
-    consume_gn<T>(r, fill, cx.seq(5 * p.n_layer), scratch, p);
+    consume_gn<T>(r, fill, cx.seq(5 * p.n_layer), scratch, p, step, phase - 1);
     mark_phase(p, phase);
+    }
 }
 
 // ---------------------------------------------------------------- host

@@ -116,6 +116,14 @@ class DecodeModel:
                                          abi.ptr(self.logits) if write_logits else None, flags,
                                          abi.stream_handle(stream)), "ds_decode_step")
 
+    def steps(self, n_steps, ids_out=None, advance=True, stream=None):
+        """n_steps greedy steps of sequence 0 in one launch (ds_decode_steps);
+        ids_out: optional device int32 tensor receiving every step's pick."""
+        flags = abi.DS_STEP_ADVANCE if advance else 0
+        abi.check(abi.lib.ds_decode_steps(self._h, ctypes.byref(self._kv), abi.ptr(self.tokens), abi.ptr(self.pos),
+                                          n_steps, abi.ptr(ids_out), abi.ptr(self.next_ids), flags,
+                                          abi.stream_handle(stream)), "ds_decode_steps")
+
     def graph(self, n_seqs=1, sampling=None, advance=True, write_logits=False, stream=None):
         """A captured step (created once per argument set); returns a
         callable that replays it on `stream`."""

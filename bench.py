@@ -43,6 +43,9 @@ def parse():
                         "then absent)")
     p.add_argument("--batched-steps", type=int, default=None,
                    help="timed steps of the batched decode (default: the workload's 128)")
+    p.add_argument("--chunk", type=int, default=32,
+                   help="greedy steps per kernel launch in the timed region (the picks hand over on the device); "
+                        "1 = one captured-graph replay per step")
     p.add_argument("--layers", type=int, default=None,
                    help="decoder layers (default: the model's 32); fewer layers make a small profiling case, "
                         "not a benchmark number")
@@ -439,12 +442,22 @@ def run_ours(args, rank, world, local):
     time.sleep(0.3)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    chunks = []
+    if args.chunk > 1:  # K steps as launches of up to `chunk` steps each
+        left = K
+        while left > 0:
+            chunks.append(min(args.chunk, left))
+            left -= chunks[-1]
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     e0.record(stream)
-    for _ in range(K):
-        replay(stream)
+    if chunks:
+        for n in chunks:
+            model.steps(n, stream=stream)
+    else:
+        for _ in range(K):
+            replay(stream)
     e1.record(stream)
     e1.synchronize()
     torch.cuda.synchronize()
@@ -496,18 +509,20 @@ def run_ours(args, rank, world, local):
     per_step = {k: sum(acc[k]) / n_pt for k in names}
     per_launch = {k: per_step[k] / (1 if k in ("embed", "head") else cfg["n_layer"]) for k in names}
 
-    # the dominant (and only) kernel of a greedy step is the persistent step
-    # kernel: one launch per step, so its mean launch duration is the
-    # CUDA-event time of the K replays / K
+    # the dominant (and only) kernel of the timed region is the persistent
+    # step kernel: launches = chunks (or one per step), so its mean launch
+    # duration is the CUDA-event time over the launches
     peak, peak_kind = peaks()
+    n_launch = len(chunks) if chunks else K
     step_bytes = [C.step_bytes(cfg, args.ctx + i + 1) for i in range(K)]
-    alg_bytes = sum(step_bytes) / K
-    launch_us = ms * 1000.0 / K
+    alg_bytes = sum(step_bytes) / n_launch
+    launch_us = ms * 1000.0 / n_launch
     achieved = alg_bytes / (launch_us / 1e6) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": profile_summary_traffic(kernel_source_sha()) if args.layers is None else None,
-                "kernel": "step_kernel: persistent cooperative decode step (all layers + head + argmax), "
-                          "one launch per token",
+                "kernel": "step_kernel: persistent cooperative decode step (all layers + head + argmax); "
+                          + ("%d greedy steps per launch, picks handed over on the device" % args.chunk
+                             if chunks else "one launch per token"),
                 "peak_source": peak_kind + " (MEASURED_PEAKS hbm_gbs copy)" if peak_kind == "measured" else peak_kind,
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "algorithmic_bytes": "every weight byte once + K/V of every attended position",
@@ -522,7 +537,7 @@ def run_ours(args, rank, world, local):
             "per_op_us_per_launch": per_launch, "per_op_us_per_step": per_step,
             "per_op_source": "device phase timestamps inside the step kernel, mean of %d steps" % n_pt,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
-            "gpu_launches": K,
+            "gpu_launches": n_launch,
             "clocks": clocks.summary(t_wall0, t_wall1)}
     del model
     torch.cuda.empty_cache()

@@ -410,6 +410,20 @@ DS_API int ds_decode_step(ds_model *model, const ds_kv_cache *kv, int32_t *token
                           int32_t *next_ids, float *logits_out, unsigned flags,
                           ds_stream_t stream);
 
+/* n_steps greedy decode steps of one sequence in ONE kernel launch: step i
+ * decodes tokens[0] at pos[0] + i and feeds its pick to step i + 1 on the
+ * device, so the weight stream runs on from one step's output head into the
+ * next step's first layer without a launch in between ("Inside the engine",
+ * section 4: the decode loop's steps issued back to back on the device).
+ * Each step is a whole ds_decode_step (same result, same K/V writes).
+ *   ids_out: optional device int32 [n_steps], the pick of every step;
+ *   next_ids: device int32 [1], the last pick.  With DS_STEP_ADVANCE,
+ *   tokens[0] and pos[0] end at the last pick and pos[0] + n_steps.
+ * Batch-1 models (max_seqs 1) on the persistent step kernel only (577
+ * otherwise); n_steps >= 1 (561); logits are not written. */
+DS_API int ds_decode_steps(ds_model *model, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_steps,
+                           int32_t *ids_out, int32_t *next_ids, unsigned flags, ds_stream_t stream);
+
 /* Device timestamps (ns, globaltimer) of the last step run with
  * DS_STEP_PHASE_TIMES: [0] start, then the start of every phase in order
  * (per layer: q|k|v, attention, o, gate|up, down), then the head, then the

@@ -225,3 +225,44 @@ def test_sampled_decode_matches_oracle_sampler(M):
             assert int(g.next_ids[0]) == want
             compared += 1
     assert compared >= 3
+
+
+def test_multi_step_launch_equals_single_steps(M):
+    """ds_decode_steps (n greedy steps in one launch, the pick handed to the
+    next step on the device) against n separate single steps: same ids, same
+    final state, same K/V written, bit for bit."""
+    cfg = small_bf16(C.LLAMA3_8B, 2)
+    W = synth.model_weights(cfg, seed=6, device="cuda")
+    prompt = synth.prompt_ids(cfg, 9, seed=6)
+    a = M.DecodeModel(cfg, W, capacity=48, block_tokens=16)
+    b = M.DecodeModel(cfg, W, capacity=48, block_tokens=16)
+    for g in (a, b):
+        g.prefill(prompt)
+        g.set_state([int(g.next_ids[0])], [len(prompt)])
+    ids = torch.zeros(12, dtype=torch.int32, device="cuda")
+    a.steps(12, ids_out=ids)
+    want = []
+    for _ in range(12):
+        b.step(advance=True)
+        want.append(int(b.next_ids[0]))
+    assert host(ids).tolist() == want
+    assert int(a.pos[0]) == int(b.pos[0]) == len(prompt) + 12
+    assert int(a.tokens[0]) == int(b.tokens[0]) == want[-1]
+    for l in range(cfg["n_layer"]):
+        assert torch.equal(a.k_cache[l], b.k_cache[l]) and torch.equal(a.v_cache[l], b.v_cache[l])
+    assert a.error_word() == 0 and b.error_word() == 0
+
+
+def test_multi_step_launch_reproduces_the_page_on_the_tiny_decoder(M):
+    st, W = toy_weights_gpu()
+    g = M.DecodeModel(C.TOY, W, capacity=C.TOY["max_seq"], block_tokens=4)
+    prompt = [3, 14, 15, 9, 2, 6]
+    g.prefill(prompt)
+    first = int(g.next_ids[0])
+    g.set_state([first], [len(prompt)])
+    ids = torch.zeros(9, dtype=torch.int32, device="cuda")
+    g.steps(9, ids_out=ids)
+    o = oracle_model(C.TOY, st, g.capacity)
+    out, _ = O.greedy_generate(o, prompt, 10)
+    assert [first] + host(ids).tolist() == out
+    assert out[:3] == [30, 30, 30]
