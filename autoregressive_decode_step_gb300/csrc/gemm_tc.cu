@@ -302,8 +302,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int stages = p.stages;
+    const int MS = p.msub;
+    const int a_bytes = MS * kTcABytes;        // the tile's weight sub-tiles
     const int b_bytes = p.n_pad * kTcBK * 2;  // one activation tile (the hi part when split)
-    const int stage_bytes = kTcABytes + b_bytes * (p.split ? 2 : 1);
+    const int stage_bytes = a_bytes + b_bytes * (p.split ? 2 : 1);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
     uint64_t *empty = full + kTcMaxStages;
     uint64_t *acc_full = empty + kTcMaxStages;   // [2]
@@ -358,23 +360,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             int pre = (int)std::min<long long>(stages, u1 - u0);
             auto issue_a = [&](int s, long long unit) {
                 const int tile = (int)(unit / KB), kb = (int)(unit - (long long)tile * KB);
-                unsigned char *sa = smem + (size_t)s * stage_bytes;
-                if (A_MN) {
-                    if (EPI == TC_SILU) {
-                        tma_box_g2s(sa, &p.ta0, tile * (kTcBM / 2), kb * kTcBK, &full[s], pol);
-                        tma_box_g2s(sa + kTcABytes / 2, &p.ta1, tile * (kTcBM / 2), kb * kTcBK, &full[s], pol);
+                for (int h = 0; h < MS; ++h) {
+                    const int st = tile * MS + h;  // 128-feature sub-tile
+                    unsigned char *sa = smem + (size_t)s * stage_bytes + h * kTcABytes;
+                    if (A_MN) {
+                        if (EPI == TC_SILU) {
+                            tma_box_g2s(sa, &p.ta0, st * (kTcBM / 2), kb * kTcBK, &full[s], pol);
+                            tma_box_g2s(sa + kTcABytes / 2, &p.ta1, st * (kTcBM / 2), kb * kTcBK, &full[s], pol);
+                        } else {
+                            tma_box_g2s(sa, &p.ta0, st * kTcBM, kb * kTcBK, &full[s], pol);
+                            tma_box_g2s(sa + kTcABytes / 2, &p.ta0, st * kTcBM + kTcBM / 2, kb * kTcBK, &full[s], pol);
+                        }
                     } else {
-                        tma_box_g2s(sa, &p.ta0, tile * kTcBM, kb * kTcBK, &full[s], pol);
-                        tma_box_g2s(sa + kTcABytes / 2, &p.ta0, tile * kTcBM + kTcBM / 2, kb * kTcBK, &full[s], pol);
+                        tma_box_g2s(sa, &p.ta0, kb * kTcBK, st * kTcBM, &full[s], pol);
                     }
-                } else {
-                    tma_box_g2s(sa, &p.ta0, kb * kTcBK, tile * kTcBM, &full[s], pol);
                 }
             };
             auto issue_b = [&](int s, long long unit) {
                 const int tile = (int)(unit / KB), kb = (int)(unit - (long long)tile * KB);
                 (void)tile;
-                unsigned char *sb = smem + (size_t)s * stage_bytes + kTcABytes;
+                unsigned char *sb = smem + (size_t)s * stage_bytes + a_bytes;
                 tma_box_g2s_nohint(sb, &p.tb, kb * kTcBK, 0, &full[s]);
                 if (p.split) tma_box_g2s_nohint(sb + b_bytes, &p.tb, kb * kTcBK, p.b_lo_row, &full[s]);
             };
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(buf * p.n_pad);
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * MS * p.n_pad);
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++fill) {
                     const int s = fill % stages;
                     if (!tc_wait(&full[s], (fill / stages) & 1, abort_flag, p.err)) {
@@ -429,15 +434,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-                    const uint32_t sb = sa + kTcABytes;
+                    const uint32_t sa0 = smem_u32(smem + (size_t)s * stage_bytes);
+                    const uint32_t sb = sa0 + a_bytes;
 #pragma unroll
                     for (int k = 0; k < kTcBK / 16; ++k) {
-                        const uint64_t ad = A_MN ? smem_desc(sa + k * 2048, kTcABytes / 2, 1024)
-                                                 : smem_desc(sa + k * 32, 16, 1024);
                         const uint64_t bd = smem_desc(sb + k * 32, 16, 1024);
-                        tc_mma(d_tmem, ad, bd, idesc, (kb > sg.kb0 || k > 0) ? 1u : 0u);
-                        if (p.split) tc_mma(d_tmem, ad, smem_desc(sb + b_bytes + k * 32, 16, 1024), idesc, 1u);
+                        for (int h = 0; h < MS; ++h) {  // sub-tile h accumulates n_pad columns further
+                            const uint32_t sa = sa0 + h * kTcABytes;
+                            const uint64_t ad = A_MN ? smem_desc(sa + k * 2048, kTcABytes / 2, 1024)
+                                                     : smem_desc(sa + k * 32, 16, 1024);
+                            const uint32_t d = d_tmem + (uint32_t)(h * p.n_pad);
+                            tc_mma(d, ad, bd, idesc, (kb > sg.kb0 || k > 0) ? 1u : 0u);
+                            if (p.split) tc_mma(d, ad, smem_desc(sb + b_bytes + k * 32, 16, 1024), idesc, 1u);
+                        }
                     }
                     tc_commit(&empty[s]);
                 }
@@ -471,28 +480,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                  s_ok[(seg_i & 1) * 4 + 3];
             tc_fence_after();
             const bool whole = sg.kb0 == 0 && sg.kb1 == KB;
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.n_pad);
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * MS * p.n_pad);
+            const size_t sub_floats = (size_t)kTcBM * p.n_pad;
             if (!ok) break;
             if (whole) {
-                for (int c = 0; c < n_chunks; ++c) {
-                    float v[32];
-                    tmem_ld32(tbase + c * 32, v);
-                    if (c == n_chunks - 1) {  // the buffer may be reused once every lane has read it
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                for (int h = 0; h < MS; ++h)
+                    for (int c = 0; c < n_chunks; ++c) {
+                        float v[32];
+                        tmem_ld32(tbase + h * p.n_pad + c * 32, v);
+                        if (h == MS - 1 && c == n_chunks - 1) {  // the buffer may be reused once every lane has read it
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                        }
+                        tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, xch, s_row, r);
                     }
-                    tc_epilogue_chunk<EPI>(p, sg.tile, c, v, xch, s_row, r);
-                }
             } else {
-                // partial accumulator to this (CTA, tile) slot, feature-fastest
-                float *slot = p.partials + ((size_t)blockIdx.x + sg.tile) * kTcBM * p.n_pad;
-                for (int c = 0; c < n_chunks; ++c) {
-                    float v[32];
-                    tmem_ld32(tbase + c * 32, v);
+                // partial accumulators to this (CTA, tile) slot, feature-fastest per sub-tile
+                float *slot = p.partials + ((size_t)blockIdx.x + sg.tile) * MS * sub_floats;
+                for (int h = 0; h < MS; ++h)
+                    for (int c = 0; c < n_chunks; ++c) {
+                        float v[32];
+                        tmem_ld32(tbase + h * p.n_pad + c * 32, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) slot[(size_t)(c * 32 + i) * kTcBM + r] = v[i];
-                }
+                        for (int i = 0; i < 32; ++i) slot[h * sub_floats + (size_t)(c * 32 + i) * kTcBM + r] = v[i];
+                    }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -511,17 +523,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                 named_sync(1, kTcEpiThreads);
                 if (s_flags[1]) {
                     __threadfence();
-                    for (int c = 0; c < n_chunks; ++c) {
-                        float v[32];
+                    for (int h = 0; h < MS; ++h)
+                        for (int c = 0; c < n_chunks; ++c) {
+                            float v[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-                        for (int cc = c_first; cc <= c_last; ++cc) {
-                            const float *src = p.partials + ((size_t)cc + sg.tile) * kTcBM * p.n_pad;
+                            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                            for (int cc = c_first; cc <= c_last; ++cc) {
+                                const float *src =
+                                    p.partials + ((size_t)cc + sg.tile) * MS * sub_floats + h * sub_floats;
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += __ldcg(src + (size_t)(c * 32 + i) * kTcBM + r);
+                                for (int i = 0; i < 32; ++i) v[i] += __ldcg(src + (size_t)(c * 32 + i) * kTcBM + r);
+                            }
+                            tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, xch, s_row, r);
                         }
-                        tc_epilogue_chunk<EPI>(p, sg.tile, c, v, xch, s_row, r);
-                    }
                 }
                 named_sync(1, kTcEpiThreads);
             }
@@ -540,15 +554,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 // accumulator (the epilogue reads 32 columns at a time).
 int tc_n_pad(int n) { return std::max(32, (n + 31) / 32 * 32); }
 
-int tc_stages(int n_pad, int split) {
-    const size_t stage = (size_t)kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
+int tc_stages(int n_pad, int split, int msub) {
+    const size_t stage = (size_t)msub * kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
     const size_t fixed = 1024 + 256 + 72 * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
     int s = (int)((kTcSmemLimit - fixed) / stage);
     return std::min(s, kTcMaxStages);
 }
 
-size_t tc_smem_bytes(int n_pad, int split, int stages) {
-    const size_t stage = (size_t)kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
+size_t tc_smem_bytes(int n_pad, int split, int msub, int stages) {
+    const size_t stage = (size_t)msub * kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
     return 1024 + (size_t)stages * stage + 256 + 72 * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
 }
 
@@ -559,8 +573,8 @@ int tc_grid(int m_tiles, int K) {
     return (int)std::min<long long>(sm_count(), W);
 }
 
-size_t tc_partial_floats(int m_tiles, int n_pad) {
-    return (size_t)(sm_count() + m_tiles) * kTcBM * n_pad;
+size_t tc_partial_floats(int m_tiles, int n_pad, int msub) {
+    return (size_t)(sm_count() + m_tiles) * msub * kTcBM * n_pad;
 }
 
 bool tc_make_maps(TcArgs &a, const void *A0, const void *A1, long long a_row_stride, const void *X) {
@@ -579,7 +593,7 @@ bool tc_make_maps(TcArgs &a, const void *A0, const void *A1, long long a_row_str
 
 template <int A_MN, int EPI>
 static cudaError_t launch_tc_t(const TcArgs &a, int grid, cudaStream_t stream, bool pdl) {
-    const size_t smem = tc_smem_bytes(a.n_pad, a.split, a.stages);
+    const size_t smem = tc_smem_bytes(a.n_pad, a.split, a.msub, a.stages);
     if (smem > kTcSmemLimit) return cudaErrorInvalidValue;
     return launch_ex(tc_gemm_kernel<A_MN, EPI>, dim3(grid), dim3(kTcThreads), smem, stream, pdl, a);
 }
@@ -588,6 +602,7 @@ static bool g_tc_ready = false;
 
 cudaError_t launch_tc_gemm(const TcArgs &a, int grid, cudaStream_t stream, bool pdl) {
     if (a.n_pad < 32 || a.n_pad > 256 || a.n_pad % 32 || a.stages < 2 || a.stages > kTcMaxStages) return cudaErrorInvalidValue;
+    if ((a.msub != 1 && a.msub != 2) || a.tmem_cols < 2 * a.msub * a.n_pad || a.tmem_cols > 512) return cudaErrorInvalidValue;
     if (!g_tc_ready) {
         cudaError_t e = prepare_tc_kernels();
         if (e != cudaSuccess) return e;
@@ -630,7 +645,7 @@ size_t tc_ws_bytes(int64_t n, int64_t M, int64_t K, int epi) {
     const int n_pad = tc_n_pad((int)n);
     const int T = tc_m_tiles((int)M, epi);
     (void)K;
-    return kWsHeader + align_up((size_t)T * 4, 256) + tc_partial_floats(T, n_pad) * 4;
+    return kWsHeader + align_up((size_t)T * 4, 256) + tc_partial_floats(T, n_pad, 1) * 4;
 }
 
 int tc_check(const void *A, int64_t a_len, const void *X, int64_t x_len, int64_t n, int64_t rows, int64_t cols,
@@ -657,8 +672,9 @@ int tc_run(const void *A, const void *X, int64_t n, int64_t M, int64_t K, int a_
     a.n = (int)n;
     a.n_pad = tc_n_pad((int)n);
     a.epi = TC_STORE;
+    a.msub = 1;
     a.m_tiles = tc_m_tiles(a.M, a.epi);
-    a.stages = tc_stages(a.n_pad, 0);
+    a.stages = tc_stages(a.n_pad, 0, 1);
     a.tmem_cols = 32;
     while (a.tmem_cols < 2 * a.n_pad) a.tmem_cols *= 2;
     a.y = Y;

@@ -168,6 +168,8 @@ Layout make_layout(const ds_model_config *c) {
         const int nqkv = nq + 2 * nkv;
         L.tc_tiles = std::max(std::max(tc_m_tiles(nqkv, TC_QKV), tc_m_tiles(c->d, TC_ADD)),
                               std::max(tc_m_tiles(c->ff, TC_SILU), tc_m_tiles(c->vocab, TC_STORE)));
+        // counted in 128-feature sub-tiles: a pairing never needs more partial
+        // space than (SMs + sub-tiles) single sub-tiles
     }
     size_t partial = 0;
     partial = std::max(partial, gemv_t_partial_floats(L.grid_qkv, L.nb_qkv, es));
@@ -218,7 +220,7 @@ Layout make_layout(const ds_model_config *c) {
         L.att_bf = carve(off, (size_t)2 * S * nq * 2);
         L.f_bf = carve(off, (size_t)2 * S * c->ff * 2);
         L.tc_counters = carve(off, (size_t)L.tc_tiles * 4);
-        L.tc_partials = carve(off, tc_partial_floats(L.tc_tiles, tc_n_pad(S)) * 4);
+        L.tc_partials = carve(off, tc_partial_floats(L.tc_tiles, tc_n_pad(S), 2) * 4);
         L.b_am_counters = carve(off, (size_t)S * 4);
     }
     L.total = off;
@@ -583,8 +585,10 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
         m->b_am_counters = reinterpret_cast<int *>(ws + L.b_am_counters);
         const int S = cfg->max_seqs, es = 2;
         const int nq = cfg->n_qh * cfg->head_dim, nkv = cfg->n_kvh * cfg->head_dim, nqkv = nq + 2 * nkv;
+        // pair = 2: two 128-feature sub-tiles per stage share one activation tile
+        // (the large gate|up and head matrices, where tiles are plentiful)
         auto mk = [&](int epi, int a_mn, const void *A0, const void *A1, long long stride, int M, int K, void *X,
-                      TcArgs &a) {
+                      TcArgs &a, int pair) {
             a = TcArgs{};
             a.a_mn = a_mn;
             a.M = M;
@@ -594,10 +598,11 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
             a.split = 1;  // fp32 activations as bf16 hi + lo rows, S rows apart
             a.b_lo_row = S;
             a.epi = epi;
-            a.m_tiles = tc_m_tiles(M, epi);
-            a.stages = tc_stages(a.n_pad, 1);
+            a.msub = (pair == 2 && a.n_pad <= 128) ? 2 : 1;
+            a.m_tiles = (tc_m_tiles(M, epi) + a.msub - 1) / a.msub;
+            a.stages = tc_stages(a.n_pad, 1, a.msub);
             a.tmem_cols = 32;
-            while (a.tmem_cols < 2 * a.n_pad) a.tmem_cols *= 2;
+            while (a.tmem_cols < 2 * a.msub * a.n_pad) a.tmem_cols *= 2;
             a.partials = reinterpret_cast<float *>(ws + L.tc_partials);
             a.counters = reinterpret_cast<int *>(ws + L.tc_counters);
             a.err = m->err;
@@ -607,7 +612,7 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
         bool ok = true;
         for (int l = 0; l < cfg->n_layer && ok; ++l) {
             TcArgs &q = m->tc[4 * l + 0];
-            ok = ok && mk(TC_QKV, 1, m->wqkv[l], nullptr, (long long)nqkv * es, nqkv, cfg->d, m->h_bf, q);
+            ok = ok && mk(TC_QKV, 1, m->wqkv[l], nullptr, (long long)nqkv * es, nqkv, cfg->d, m->h_bf, q, 1);
             q.y = m->q;
             q.ldy = nq;
             q.rope_cos = m->rope_cos;
@@ -619,22 +624,22 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
             q.rope_layout = cfg->rope_layout;
             q.kv_dtype = cfg->kv_dtype;
             TcArgs &o = m->tc[4 * l + 1];
-            ok = ok && mk(TC_ADD, 1, m->wo[l], nullptr, (long long)cfg->d * es, cfg->d, nq, m->att_bf, o);
+            ok = ok && mk(TC_ADD, 1, m->wo[l], nullptr, (long long)cfg->d * es, cfg->d, nq, m->att_bf, o, 1);
             o.y = m->x;
             o.ldy = cfg->d;
             TcArgs &gu = m->tc[4 * l + 2];
             ok = ok && mk(TC_SILU, 1, m->wgu[l], static_cast<const char *>(m->wgu[l]) + (size_t)cfg->ff * es,
-                          (long long)2 * cfg->ff * es, cfg->ff, cfg->d, m->h_bf, gu);
+                          (long long)2 * cfg->ff * es, cfg->ff, cfg->d, m->h_bf, gu, 2);
             gu.yb = static_cast<__nv_bfloat16 *>(m->f_bf);
             gu.yb_lo = (long long)S * cfg->ff;
             gu.ldy = cfg->ff;
             TcArgs &dn = m->tc[4 * l + 3];
-            ok = ok && mk(TC_ADD, 1, m->wd[l], nullptr, (long long)cfg->d * es, cfg->d, cfg->ff, m->f_bf, dn);
+            ok = ok && mk(TC_ADD, 1, m->wd[l], nullptr, (long long)cfg->d * es, cfg->d, cfg->ff, m->f_bf, dn, 1);
             dn.y = m->x;
             dn.ldy = cfg->d;
         }
         TcArgs &hd = m->tc[(size_t)4 * cfg->n_layer];
-        ok = ok && mk(TC_STORE, 0, m->out, nullptr, (long long)cfg->d * es, cfg->vocab, cfg->d, m->h_bf, hd);
+        ok = ok && mk(TC_STORE, 0, m->out, nullptr, (long long)cfg->d * es, cfg->vocab, cfg->d, m->h_bf, hd, 2);
         hd.ldy = cfg->vocab;
         if (!ok || prepare_tc_kernels() != cudaSuccess || prepare_paged_attention() != cudaSuccess) {
             delete m;

@@ -30,6 +30,7 @@ struct TcArgs {
     int split;        // 1: each activation is hi + lo, two bf16 rows b_lo_row apart; both are multiplied
     int b_lo_row;
     int epi, m_tiles, stages, tmem_cols;
+    int msub;         // 128-feature sub-tiles per tile (1 or 2): a tile's sub-tiles share one activation tile
     float *y;             // TC_STORE / TC_ADD: y[s * ldy + m]; TC_QKV: q [n][ldy]
     __nv_bfloat16 *yb;    // TC_SILU: silu(gate) * up as bf16, yb[s * ldy + g] (hi part when yb_lo > 0)
     long long yb_lo;      // TC_SILU: elements from the hi part to the lo part (0: hi only)
@@ -51,10 +52,10 @@ struct TcArgs {
 };
 
 int tc_n_pad(int n);
-int tc_stages(int n_pad, int split);
+int tc_stages(int n_pad, int split, int msub);
 int tc_m_tiles(int M, int epi);
 int tc_grid(int m_tiles, int K);
-size_t tc_partial_floats(int m_tiles, int n_pad);
+size_t tc_partial_floats(int m_tiles, int n_pad, int msub);
 // Encode a.ta0 (and a.ta1 from A1 when set) and a.tb.
 bool tc_make_maps(TcArgs &a, const void *A0, const void *A1, long long a_row_stride, const void *X);
 cudaError_t launch_tc_gemm(const TcArgs &a, int grid, cudaStream_t stream, bool pdl);
