@@ -763,6 +763,11 @@ __device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *
     const KT *vc = static_cast<const KT *>(p.vc[layer]);
 
     float kf[RUN][4], vf[RUN][4];
+    // bf16 caches: a run's rows are fetched packed (two registers per row) one
+    // run ahead and unpacked when their turn comes, so the next run's loads are
+    // in flight during this run's arithmetic
+    constexpr bool PACKED = sizeof(KT) == 2;
+    uint2 rk[PACKED ? RUN : 1], rv[PACKED ? RUN : 1];
     auto load_run = [&](int tb) {
         const int nt = min(RUN, tc - tb);
 #pragma unroll
@@ -774,8 +779,32 @@ __device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *
                 const long long blk = p.block_table ? (long long)__ldcg(p.block_table + b) : (long long)b;
                 off = (blk * p.block_tokens + tt % p.block_tokens) * row_elems + (long long)g * hd + d0;
             }
-            load4<KT>(kc, off, ok, kf[i]);
-            load4<KT>(vc, off, ok, vf[i]);
+            if constexpr (PACKED) {
+                rk[i] = make_uint2(0u, 0u);
+                rv[i] = make_uint2(0u, 0u);
+                if (ok) {
+                    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(rk[i].x), "=r"(rk[i].y) : "l"(kc + off));
+                    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(rv[i].x), "=r"(rv[i].y) : "l"(vc + off));
+                }
+            } else {
+                load4<KT>(kc, off, ok, kf[i]);
+                load4<KT>(vc, off, ok, vf[i]);
+            }
+        }
+    };
+    auto unpack_run = [&]() {
+        if constexpr (PACKED) {
+#pragma unroll
+            for (int i = 0; i < RUN; ++i) {
+                kf[i][0] = __uint_as_float(rk[i].x << 16);
+                kf[i][1] = __uint_as_float(rk[i].x & 0xffff0000u);
+                kf[i][2] = __uint_as_float(rk[i].y << 16);
+                kf[i][3] = __uint_as_float(rk[i].y & 0xffff0000u);
+                vf[i][0] = __uint_as_float(rv[i].x << 16);
+                vf[i][1] = __uint_as_float(rv[i].x & 0xffff0000u);
+                vf[i][2] = __uint_as_float(rv[i].y << 16);
+                vf[i][3] = __uint_as_float(rv[i].y & 0xffff0000u);
+            }
         }
     };
     int tb = t0 + warp * RUN;
@@ -855,9 +884,16 @@ __device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *
         }
     };
     while (tb < tc) {
-        update(min(RUN, tc - tb));
-        tb += kStConsumerWarps * RUN;
-        if (tb < tc) load_run(tb);
+        const int nt = min(RUN, tc - tb), tn = tb + kStConsumerWarps * RUN;
+        if constexpr (PACKED) {
+            unpack_run();
+            if (tn < tc) load_run(tn);  // the next run's loads go out before this run's arithmetic
+            update(nt);
+        } else {
+            update(nt);
+            if (tn < tc) load_run(tn);
+        }
+        tb = tn;
     }
     if (cur_warp) {  // the current position
         tag_fix_at<8>(cw, ca, q_tag, p);

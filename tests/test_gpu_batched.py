@@ -166,3 +166,58 @@ def test_batched_graph_replay_equals_eager_and_is_bit_stable(M):
     for r in runs[1:]:
         np.testing.assert_array_equal(r[0], runs[0][0])
         np.testing.assert_array_equal(r[1], runs[0][1])
+
+
+@pytest.mark.slow
+def test_batched_full_size_in_the_benchmark_configuration(M):
+    """The benchmark's batched workload at full size — 32 layers, 64 sequences
+    at contexts uniform in [128, 4096] in a scattered pool of 16-position
+    blocks, a captured graph with per-row sampling and the state advanced on
+    the device — one step checked against the oracle on three sampled
+    sequences (the oracle recomputes one sequence at a time)."""
+    cfg = C.LLAMA3_8B
+    n = 64
+    ctx = synth.context_lengths(n, 128, 4096, seed=0)
+    need = [(c + 2 + 15) // 16 for c in ctx]
+    mb = max(need)
+    n_blocks = sum(need)
+    perm = synth.paged_block_table(1, n_blocks, seed=1).view(-1)
+    table = torch.zeros(n, mb, dtype=torch.int32)
+    at = 0
+    for s, k in enumerate(need):
+        table[s, :k] = perm[at:at + k]
+        at += k
+    W = synth.model_weights(cfg, seed=0, device="cuda")
+    g = M.DecodeModel(cfg, W, capacity=mb * 16, block_tokens=16, block_table=table.cuda(), n_blocks=n_blocks,
+                      max_seqs=n)
+    ks, vs = synth.synthetic_kv(cfg, n_blocks * 16, seed=2, device="cuda")
+    for l in range(cfg["n_layer"]):
+        g.k_cache[l].copy_(ks[l])
+        g.v_cache[l].copy_(vs[l])
+    toks = synth.prompt_ids(cfg, n, seed=3)
+    u = synth.uniform_draws(n, seed=4)
+    g.set_state(toks, ctx)
+    g.u[:n].copy_(u)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        replay = g.graph(n_seqs=n, sampling=(0.8, 50, 0.95), advance=True, write_logits=True, stream=s)
+        replay(s)
+    s.synchronize()
+    got = host(g.logits[:n])
+    ids = host(g.next_ids[:n])
+    assert host(g.pos[:n]).tolist() == [c + 1 for c in ctx]
+    assert np.isfinite(got).all()
+    st = synth.weights_to_numpy(W)
+    del W
+    o = O.Model(dict(cfg, block_tokens=16, max_blocks=mb, block_table=table.numpy(), n_blocks=n_blocks, n_seqs=n), st)
+    for l in range(cfg["n_layer"]):
+        o.k[l][:] = host(ks[l]).ravel()
+        o.v[l][:] = host(vs[l]).ravel()
+    del ks, vs
+    for sq in (0, 31, 63):
+        ref = o.step(toks[sq], ctx[sq], seq=sq)
+        assert rel_err(got[sq], ref) <= BF16_TOL, sq
+        want, margin = O.sample(ref.astype(np.float32), 0.8, 50, 0.95, float(u[sq]))
+        if margin >= 1e-3:
+            assert int(ids[sq]) == want, sq
+    assert g.error_word() == 0

@@ -266,3 +266,38 @@ def test_multi_step_launch_reproduces_the_page_on_the_tiny_decoder(M):
     out, _ = O.greedy_generate(o, prompt, 10)
     assert [first] + host(ids).tolist() == out
     assert out[:3] == [30, 30, 30]
+
+
+@pytest.mark.slow
+def test_qwen_full_size_step_from_synthetic_context(M):
+    """The Qwen3-0.6B shape at full depth and vocabulary (28 layers, tied
+    151,936 x 1024 head, fp32 K/V), in the captured-graph configuration, one
+    step at position 512 over a synthetic 512-position context."""
+    cfg = C.QWEN3_0_6B
+    n_ctx = 512
+    W = synth.model_weights(cfg, seed=0, device="cuda")
+    g = M.DecodeModel(cfg, W, capacity=n_ctx + 256, block_tokens=16)
+    ks, vs = synth.synthetic_kv(cfg, n_ctx, seed=3, device="cuda")
+    for l in range(cfg["n_layer"]):
+        g.k_cache[l][:n_ctx].copy_(ks[l])
+        g.v_cache[l][:n_ctx].copy_(vs[l])
+    tok = synth.prompt_ids(cfg, 1, seed=5)[0]
+    g.set_state([tok], [n_ctx])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        replay = g.graph(advance=True, write_logits=True, stream=s)
+        replay(s)
+    s.synchronize()
+    got = host(g.logits[0])
+    gid = int(g.next_ids[0])
+    st = synth.weights_to_numpy(W)
+    del W
+    o = oracle_model(cfg, st, g.capacity)
+    for l in range(cfg["n_layer"]):
+        o.k[l][:ks[l].numel()] = host(ks[l]).ravel()
+        o.v[l][:vs[l].numel()] = host(vs[l]).ravel()
+    ref = o.step(tok, n_ctx)
+    assert rel_err(got, ref) <= BF16_TOL
+    if top2_gap(ref) > TIE_GAP:
+        assert gid == O.argmax(ref.astype(np.float32))[0]
+    assert g.error_word() == 0
