@@ -270,6 +270,12 @@ struct StepParams {
     int nb_qkv, nb_o, nb_gu, nb_d;
     int attn_splits;
     int stages;             // ring stages in use
+    // the cached K/V of each CTA's attention item streamed through the ring
+    // (between the q|k|v and o stages of a layer) when kv_tma is set:
+    const CUtensorMap *kv_maps;  // per layer: K map, V map; 2-D {n_kvh * hd, rows}, boxes {hd, block_tokens}
+    int kv_tma;
+    int kv_align;           // attention split boundaries are multiples of this (whole blocks)
+    int kv_stage_pos;       // positions per K/V stage
     int scratch_floats;     // shared scratch after the ring
     void *kc[kStMaxLayers];
     void *vc[kStMaxLayers];

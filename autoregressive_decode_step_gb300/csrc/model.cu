@@ -70,6 +70,13 @@ struct ds_model {
     std::vector<ds::TcArgs> tc;  // per layer: q|k|v, o, gate|up, down; then the head
     // tensor maps of the K/V buffers for the paged attention, per layer, and
     // the cache they were encoded for (re-encoded when a step passes another)
+    // K/V tensor maps of the persistent step kernel (device copy in the
+    // workspace), and the cache they were encoded for
+    CUtensorMap *kv_maps_dev;
+    const void *kv_k0 = nullptr;
+    long long kv_rows_enc = -1;
+    int kv_bt_enc = -1;
+    int kv_tma_cur = 0;
     std::vector<CUtensorMap> pa_maps;
     std::vector<int> pa_box3d;
     std::vector<const void *> pa_k, pa_v;
@@ -88,7 +95,7 @@ using namespace ds;
 struct Layout {
     size_t x, q, att, f, logits, rope_cos, rope_sin, g_counters, g_partials, a_counters, a_partials, am_val,
         am_idx, am_counter, step_layers, step_bar, phase_times, trace, st_x, st_q, st_kv, st_f, st_ss, st_part,
-        st_att, h_bf, att_bf, f_bf, tc_counters, tc_partials, b_am_counters, total;
+        st_att, h_bf, att_bf, f_bf, tc_counters, tc_partials, b_am_counters, kv_maps, total;
     int b_splits, tc_tiles;
     size_t st_part_stride;
     int grid_qkv, grid_o, grid_gu, grid_d, grid_head, nb_qkv, nb_o, nb_gu, nb_d, attn_splits;
@@ -200,6 +207,7 @@ Layout make_layout(const ds_model_config *c) {
     L.am_idx = carve(off, am_slots * 4);
     L.am_counter = carve(off, 4);
     L.step_layers = carve(off, (size_t)std::max(c->n_layer, 1) * step_layer_bytes());
+    L.kv_maps = carve(off, (size_t)2 * std::max(c->n_layer, 1) * sizeof(CUtensorMap));
     L.step_bar = carve(off, 32);  // arrival count (u64), epoch (u64), abort flag (int, + pad), handed-over token (u64)
     L.phase_times = carve(off, (size_t)L.n_phase_times * 8);
     L.trace = carve(off, (size_t)L.n_phase_times * L.step_grid * 5 * 8);
@@ -561,6 +569,7 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
     m->step_stages = L.step_stages;
     m->step_scratch = L.step_scratch;
     m->step_layers = reinterpret_cast<StepLayer *>(ws + L.step_layers);
+    m->kv_maps_dev = reinterpret_cast<CUtensorMap *>(ws + L.kv_maps);
     m->step_bar = reinterpret_cast<unsigned *>(ws + L.step_bar);
     m->step_abort = reinterpret_cast<int *>(ws + L.step_bar + 16);
     m->phase_times = reinterpret_cast<unsigned long long *>(ws + L.phase_times);
@@ -666,6 +675,53 @@ extern "C" DS_API void ds_model_destroy(ds_model *m) { delete m; }
 
 extern "C" DS_API void *ds_model_workspace(ds_model *m) { return m ? m->ws : nullptr; }
 
+// Positions per K/V stage of the step kernel's ring (K rows then V rows of
+// one head in a 64 KB stage, a multiple of 64 and of the block size, at most
+// 256), or 0 when the cache geometry cannot stream through the ring.
+int kv_stage_positions(const ds_model_config &c, int block_tokens) {
+    const int es = c.kv_dtype == DS_BF16 ? 2 : 4;
+    const int row = c.head_dim * es;
+    if (row % 16 || c.head_dim > 128 || ((long long)c.n_kvh * row) % 16) return 0;
+    int P = std::min(256, 65536 / (2 * row)) / 64 * 64;
+    if (P < 64 || block_tokens < 1 || block_tokens > 256 || P % block_tokens) return 0;
+    // every box of a block lands block_tokens * row bytes after the previous
+    // one: tensor copies need 128-byte-aligned shared-memory destinations
+    if (((long long)block_tokens * row) % 128 || ((long long)P * row) % 128) return 0;
+    return P;
+}
+
+// Encode the step kernel's per-layer K/V maps for this cache and upload them,
+// when the cache differs from the one they were made for.  Runs before any
+// capture (a synchronous copy of a few KB).
+int ensure_kv_maps(ds_model *m, const ds_kv_cache *kv, cudaStream_t s) {
+    const ds_model_config &c = m->cfg;
+    if (!m->step_ok || m->batched) return DS_OK;
+    if (m->kv_k0 == kv->k[0] && m->kv_rows_enc == kv->rows && m->kv_bt_enc == kv->block_tokens) return DS_OK;
+    m->kv_tma_cur = 0;
+    if (kv_stage_positions(c, kv->block_tokens) > 0) {
+        std::vector<CUtensorMap> maps((size_t)2 * c.n_layer);
+        const int es = c.kv_dtype == DS_BF16 ? 2 : 4;
+        const long long cols = (long long)c.n_kvh * c.head_dim;
+        bool ok = true;
+        for (int l = 0; l < c.n_layer && ok; ++l)
+            ok = encode_tiled_2d(&maps[2 * l], kv->k[l], c.kv_dtype, cols, kv->rows, cols * es, c.head_dim,
+                                 kv->block_tokens, false) &&
+                 encode_tiled_2d(&maps[2 * l + 1], kv->v[l], c.kv_dtype, cols, kv->rows, cols * es, c.head_dim,
+                                 kv->block_tokens, false);
+        if (ok) {
+            if (cudaMemcpyAsync(m->kv_maps_dev, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice,
+                                s) != cudaSuccess ||
+                cudaStreamSynchronize(s) != cudaSuccess)
+                return DS_CUDA_ERROR;
+            m->kv_tma_cur = 1;
+        }
+    }
+    m->kv_k0 = kv->k[0];
+    m->kv_rows_enc = kv->rows;
+    m->kv_bt_enc = kv->block_tokens;
+    return DS_OK;
+}
+
 // One step through the persistent step kernel (and the sampler after it).
 int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_seqs,
                    const ds_sampling *sampling, const float *u, int32_t *next_ids, float *logits_out, unsigned flags,
@@ -730,6 +786,10 @@ int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t 
     p.nb_d = m->nb_d;
     p.attn_splits = m->step_splits;
     p.stages = m->step_stages;
+    p.kv_maps = m->kv_maps_dev;
+    p.kv_tma = m->kv_tma_cur && m->kv_bt_enc == kv->block_tokens && m->kv_k0 == kv->k[0];
+    p.kv_stage_pos = p.kv_tma ? kv_stage_positions(c, kv->block_tokens) : 0;
+    p.kv_align = p.kv_tma ? std::max(8, kv->block_tokens) : 1;
     p.scratch_floats = m->step_scratch;
     for (int l = 0; l < c.n_layer; ++l) {
         p.kc[l] = kv->k[l];
@@ -931,6 +991,8 @@ extern "C" DS_API int ds_decode_step(ds_model *m, const ds_kv_cache *kv, int32_t
                                      float *logits_out, unsigned flags, ds_stream_t stream) {
     int st = check_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids);
     if (st != DS_OK) return st;
+    st = ensure_kv_maps(m, kv, reinterpret_cast<cudaStream_t>(stream));
+    if (st != DS_OK) return st;
     return dispatch_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags,
                          reinterpret_cast<cudaStream_t>(stream));
 }
@@ -942,6 +1004,8 @@ extern "C" DS_API int ds_decode_steps(ds_model *m, const ds_kv_cache *kv, int32_
     int st = check_step(m, kv, tokens, pos, 1, nullptr, nullptr, next_ids);
     if (st != DS_OK) return st;
     if (!m->step_ok || m->batched) return DS_BAD_ARGUMENT;  // the persistent batch-1 kernel only
+    st = ensure_kv_maps(m, kv, reinterpret_cast<cudaStream_t>(stream));
+    if (st != DS_OK) return st;
     return run_step_fused(m, kv, tokens, pos, 1, nullptr, nullptr, next_ids, nullptr, flags & DS_STEP_ADVANCE,
                           reinterpret_cast<cudaStream_t>(stream), n_steps, ids_out);
 }
@@ -967,6 +1031,8 @@ extern "C" DS_API int ds_step_graph_create(ds_model *m, const ds_kv_cache *kv, i
     if (st != DS_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!s) return DS_BAD_ARGUMENT;  // the legacy stream cannot be captured
+    st = ensure_kv_maps(m, kv, s);  // uploads, if any, happen outside the capture
+    if (st != DS_OK) return st;
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return DS_CUDA_ERROR;
     st = dispatch_step(m, kv, tokens, pos, n_seqs, sampling, u, next_ids, logits_out, flags, s);
     cudaGraph_t graph = nullptr;

@@ -111,7 +111,7 @@ __device__ __forceinline__ unsigned char *ring_acquire(const Ring &r, uint32_t f
 // layer the q|k|v, o, gate|up and down boxes of this CTA's range, then its
 // rows of the head.
 struct StageCursor {
-    int l, ph;  // layer and projection (0 q|k|v, 1 o, 2 gate|up, 3 down); l == n_layer: head
+    int l, ph;  // layer and phase (0 q|k|v, 4 cached K/V, 1 o, 2 gate|up, 3 down); l == n_layer: head
     const CUtensorMap *m0, *m1;
     int UB, sub_band_cols;
     uint32_t box_bytes;
@@ -120,15 +120,46 @@ struct StageCursor {
     int rr, r1, rps;
     long long row_bytes;
     bool done;
+    int n_ctx;        // positions the step attends (its own included)
+    int kv_t, kv_tc;  // K/V phase: the next cached position to stream, and the end
 };
 
 struct StageDesc {
-    bool head;
+    bool head, kv;
     const CUtensorMap *m0, *m1;
     int col, row0, nb;
     uint32_t box_bytes, bytes;
     const char *src;
+    int kv_t, layer;
 };
+
+// Positions per attention split and the number of splits in use for a step
+// attending n_ctx positions: at least kStAttnMinPer per split, rounded up to
+// whole cache blocks when the cached K/V streams through the ring.
+// Does this step stream its cached K/V through the ring?  Only when a split
+// holds at least one full stage of positions: shorter splits are served
+// sooner from L2 (prefetched during the q|k|v phase) than from a ring slot
+// queued behind the q|k|v weights.  The producer and the consumers decide
+// alike, from the same position.
+__device__ __forceinline__ bool kv_streamed(int n_ctx, const StepParams &p) {
+    return p.kv_tma && (n_ctx + p.attn_splits - 1) / p.attn_splits >= p.kv_stage_pos;
+}
+
+// Positions per attention split and the number of splits in use for a step
+// attending n_ctx positions: at least kStAttnMinPer per split, rounded up to
+// whole cache blocks when the cached K/V streams through the ring.
+__device__ __forceinline__ void attention_split_n(int n_ctx, const StepParams &p, int &per, int &n_eff) {
+    per = max(kStAttnMinPer, (n_ctx + p.attn_splits - 1) / p.attn_splits);
+    if (kv_streamed(n_ctx, p)) per = (per + p.kv_align - 1) / p.kv_align * p.kv_align;
+    n_eff = (n_ctx + per - 1) / per;
+}
+
+// The phase after `ph` in a layer's order q|k|v, [K/V], o, gate|up, down.
+__device__ __forceinline__ int next_ph(int ph, int n_ctx, const StepParams &p) {
+    if (ph == 0) return kv_streamed(n_ctx, p) ? 4 : 1;
+    if (ph == 4) return 1;
+    return ph + 1;  // 1 -> 2 -> 3 -> 4 means "next layer" (handled by the caller)
+}
 
 template <int ES>
 __device__ void cursor_phase(StageCursor &c, const StepParams &p) {
@@ -143,6 +174,21 @@ __device__ void cursor_phase(StageCursor &c, const StepParams &p) {
             c.r1 = (int)(rows * (blockIdx.x + 1) / G0);
             c.done = c.rr >= c.r1;
             return;
+        }
+        if (c.ph == 4) {  // this CTA's cached K/V positions, if it has an attention item
+            const int n_items = p.n_kvh * p.attn_splits;
+            c.kv_t = c.kv_tc = 0;
+            if ((int)blockIdx.x < n_items) {
+                const int split = blockIdx.x % p.attn_splits;
+                int per, n_eff;
+                attention_split_n(c.n_ctx, p, per, n_eff);
+                const int t0 = min(c.n_ctx, split * per), t1 = min(c.n_ctx, t0 + per);
+                c.kv_t = t0;
+                c.kv_tc = min(t1, c.n_ctx - 1);
+            }
+            if (c.kv_t < c.kv_tc) return;
+            c.ph = 1;  // nothing cached to stream here
+            continue;
         }
         const StepLayer &L = p.layers[c.l];
         int K, nb;
@@ -165,7 +211,13 @@ __device__ void cursor_phase(StageCursor &c, const StepParams &p) {
             c.j1 = (int)min((long long)c.UB, c.j + (c.u1 - c.u));
             return;
         }
-        if (++c.ph == 4) { c.ph = 0; ++c.l; }  // nothing for this CTA here
+        // nothing for this CTA here
+        if (c.ph == 3) {
+            c.ph = 0;
+            ++c.l;
+        } else {
+            c.ph = next_ph(c.ph, c.n_ctx, p);
+        }
     }
 }
 
@@ -188,6 +240,17 @@ __device__ bool cursor_desc(const StageCursor &c, const StepParams &p, StageDesc
         return true;
     }
     d.head = false;
+    d.kv = c.ph == 4;
+    if (d.kv) {
+        const int P = p.kv_stage_pos, bt = p.block_tokens;
+        const int t_end = min(c.kv_t + P, c.kv_tc);
+        d.kv_t = c.kv_t;
+        d.layer = c.l;
+        d.nb = (t_end - c.kv_t + bt - 1) / bt;  // whole blocks (kv_t is block-aligned)
+        d.box_bytes = (uint32_t)(bt * p.hd * (p.kv_dtype == DS_BF16 ? 2 : 4));
+        d.bytes = 2u * (uint32_t)d.nb * d.box_bytes;
+        return true;
+    }
     d.m0 = c.m0;
     d.m1 = c.m1;
     d.col = c.band * c.sub_band_cols;
@@ -206,6 +269,13 @@ __device__ void cursor_advance(StageCursor &c, const StepParams &p) {
         c.done = c.rr >= c.r1;
         return;
     }
+    if (c.ph == 4) {
+        c.kv_t += p.kv_stage_pos;
+        if (c.kv_t < c.kv_tc) return;
+        c.ph = 1;
+        cursor_phase<ES>(c, p);
+        return;
+    }
     const int nb = min(kStBoxesPerStage, c.j1 - c.j);
     c.j += nb;
     c.u += nb;
@@ -216,17 +286,34 @@ __device__ void cursor_advance(StageCursor &c, const StepParams &p) {
         c.j1 = (int)min((long long)c.UB, c.j + (c.u1 - c.u));
         return;
     }
-    if (++c.ph == 4) {
+    if (c.ph == 3) {
         c.ph = 0;
         ++c.l;
+    } else {
+        c.ph = next_ph(c.ph, c.n_ctx, p);
     }
     cursor_phase<ES>(c, p);
 }
 
 // Issue the copies of one stage into ring slot `s`.
-__device__ __forceinline__ void issue_stage(const StageDesc &d, unsigned char *dst, uint64_t *bar, uint64_t pol) {
+__device__ __forceinline__ void issue_stage(const StageDesc &d, unsigned char *dst, uint64_t *bar, uint64_t pol,
+                                            const StepParams &p) {
     if (d.head) {
         bulk_g2s(dst, d.src, d.bytes, bar, pol);
+        return;
+    }
+    if (d.kv) {  // whole blocks of this CTA's KV head: K rows, then (kv_stage_pos rows further) V rows
+        const int bt = p.block_tokens;
+        const int g = blockIdx.x / p.attn_splits;
+        const CUtensorMap *mk = p.kv_maps + 2 * d.layer, *mv = mk + 1;
+        const int x = g * p.hd;
+        const int row_bytes = (int)d.box_bytes / bt;
+        for (int i = 0; i < d.nb; ++i) {
+            const int b = (d.kv_t + i * bt) / bt;
+            const int blk = p.block_table ? __ldg(p.block_table + b) : b;
+            tma_box_g2s(dst + i * d.box_bytes, mk, x, blk * bt, bar, pol);
+            tma_box_g2s(dst + (size_t)p.kv_stage_pos * row_bytes + i * d.box_bytes, mv, x, blk * bt, bar, pol);
+        }
         return;
     }
     for (int b = 0; b < d.nb; ++b) {
@@ -241,8 +328,11 @@ __device__ void produce_all(const Ring &r, const StepParams &p) {
     const uint64_t pol = policy_evict_first();
     uint32_t fill = 0;
     bool ok = true;
+    const int pos0 = __ldcg(p.pos);
+    const int cap = p.max_blocks * p.block_tokens;
     for (int step = 0; step < p.n_steps && ok; ++step) {  // weights do not depend on the token
         StageCursor fc;
+        fc.n_ctx = min(max(pos0 + step + 1, 1), cap);
         cursor_begin<ES>(fc, p);
         StageDesc d;
         while (cursor_desc<ES>(fc, p, d)) {
@@ -253,7 +343,7 @@ __device__ void produce_all(const Ring &r, const StepParams &p) {
                 break;
             }
             mbar_arrive_expect_tx(&r.full[s], d.bytes);
-            issue_stage(d, r.base + (size_t)s * kStStageBytes, &r.full[s], pol);
+            issue_stage(d, r.base + (size_t)s * kStStageBytes, &r.full[s], pol, p);
             cursor_advance<ES>(fc, p);
             ++fill;
         }
@@ -690,8 +780,7 @@ __device__ __forceinline__ void load4(const KT *base, long long off, bool ok, fl
 
 // Positions per attention split and the number of splits in use.
 __device__ __forceinline__ void attention_split(const StepCtx &cx, const StepParams &p, int &per, int &n_eff) {
-    per = max(kStAttnMinPer, (cx.n_ctx + p.attn_splits - 1) / p.attn_splits);
-    n_eff = (cx.n_ctx + per - 1) / per;
+    attention_split_n(cx.n_ctx, p, per, n_eff);
 }
 
 // Request into L2 the K/V rows of this CTA's attention item of `layer`:
@@ -699,7 +788,7 @@ __device__ __forceinline__ void attention_split(const StepCtx &cx, const StepPar
 template <typename KT>
 __device__ void prefetch_attention(int layer, const StepCtx &cx, const StepParams &p) {
     const int n_items = p.n_kvh * p.attn_splits;
-    if ((int)blockIdx.x >= n_items) return;
+    if (kv_streamed(cx.n_ctx, p) || (int)blockIdx.x >= n_items) return;  // streamed through the ring instead
     const int g = blockIdx.x / p.attn_splits, split = blockIdx.x % p.attn_splits;
     int per, n_eff;
     attention_split(cx, p, per, n_eff);
@@ -728,8 +817,8 @@ __device__ void prefetch_attention(int layer, const StepCtx &cx, const StepParam
 // merged, in split order, by whoever reads the attention output next (the o
 // projection's prologue).
 template <typename KT, int GQ>
-__device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *scratch, const StepParams &p,
-                                  int phase) {
+__device__ void consume_attention(const Ring &r, uint32_t &fill, int layer, int pid, const StepCtx &cx,
+                                  float *scratch, const StepParams &p, int phase) {
     constexpr int RUN = 8;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int hd = p.hd;
@@ -808,7 +897,8 @@ __device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *
         }
     };
     int tb = t0 + warp * RUN;
-    if (tb < tc) load_run(tb);  // K/V requests go out before q is polled
+    const bool streamed = kv_streamed(cx.n_ctx, p);
+    if (!streamed && tb < tc) load_run(tb);  // K/V requests go out before q is polled
     // the current position's k and v (handed over by the q|k|v phase), read by
     // the last warp: requested now, their arrival checked after the cached run
     const bool cur_warp = has_cur && warp == kStConsumerWarps - 1;
@@ -883,6 +973,57 @@ __device__ void consume_attention(int layer, int pid, const StepCtx &cx, float *
             m[j] = mx;
         }
     };
+    if (streamed) {
+        // the cached positions arrive through the ring, kv_stage_pos per stage
+        // (K rows, then V rows); warp w takes a stage's w-th eighth in runs
+        const int P = p.kv_stage_pos, per_warp = P / kStConsumerWarps;
+        const int row_bytes = hd * (int)sizeof(KT);
+        for (int ts = t0; ts < tc; ts += P) {
+            const int s = fill % r.stages;
+            const uint32_t use = fill / r.stages;
+            if (st_wait(&r.full[s], use & 1, p)) {
+                const unsigned char *kb = r.base + (size_t)s * kStStageBytes;
+                const unsigned char *vb = kb + (size_t)P * row_bytes;
+                for (int rb = warp * per_warp; rb < (warp + 1) * per_warp; rb += RUN) {
+                    const int nt = min(RUN, tc - (ts + rb));
+                    if (nt <= 0) break;
+#pragma unroll
+                    for (int i = 0; i < RUN; ++i) {
+                        const bool ok = active && i < nt;
+                        const size_t off = (size_t)(rb + i) * row_bytes + (size_t)d0 * sizeof(KT);
+                        if (sizeof(KT) == 2) {
+                            uint2 kw = make_uint2(0u, 0u), vw = make_uint2(0u, 0u);
+                            if (ok) {
+                                kw = *reinterpret_cast<const uint2 *>(kb + off);
+                                vw = *reinterpret_cast<const uint2 *>(vb + off);
+                            }
+                            kf[i][0] = __uint_as_float(kw.x << 16);
+                            kf[i][1] = __uint_as_float(kw.x & 0xffff0000u);
+                            kf[i][2] = __uint_as_float(kw.y << 16);
+                            kf[i][3] = __uint_as_float(kw.y & 0xffff0000u);
+                            vf[i][0] = __uint_as_float(vw.x << 16);
+                            vf[i][1] = __uint_as_float(vw.x & 0xffff0000u);
+                            vf[i][2] = __uint_as_float(vw.y << 16);
+                            vf[i][3] = __uint_as_float(vw.y & 0xffff0000u);
+                        } else {
+                            float4 kw = make_float4(0.f, 0.f, 0.f, 0.f), vw = kw;
+                            if (ok) {
+                                kw = *reinterpret_cast<const float4 *>(kb + off);
+                                vw = *reinterpret_cast<const float4 *>(vb + off);
+                            }
+                            kf[i][0] = kw.x; kf[i][1] = kw.y; kf[i][2] = kw.z; kf[i][3] = kw.w;
+                            vf[i][0] = vw.x; vf[i][1] = vw.y; vf[i][2] = vw.z; vf[i][3] = vw.w;
+                        }
+                    }
+                    update(nt);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&r.empty[s]);
+            ++fill;
+        }
+        tb = tc;
+    }
     while (tb < tc) {
         const int nt = min(RUN, tc - tb), tn = tb + kStConsumerWarps * RUN;
         if constexpr (PACKED) {
@@ -1280,7 +1421,7 @@ __global__ void __launch_bounds__(kStThreads, 1) step_kernel(const __grid_consta
         consume_gt<T, ST_QKV, SRC_NORM, GQ>(r, fill, p.d, p.nq_cols + 2 * p.nkv_cols, p.nb_qkv, p.xt, x_in, L.n1,
                                             p.qt, 0, l, ph, cx, scratch, p, phase - 1);
         mark_phase(p, phase);
-        consume_attention<KT, GQ>(l, ph + 1, cx, scratch, p, phase - 1);
+        consume_attention<KT, GQ>(r, fill, l, ph + 1, cx, scratch, p, phase - 1);
         mark_phase(p, phase);
         consume_gt<T, ST_ADD, SRC_ATTN, GQ>(r, fill, p.nq_cols, p.d, p.nb_o, nullptr, cx.seq(ph + 1), nullptr, p.xt,
                                             x_in, l, ph + 2, cx, scratch, p, phase - 1);

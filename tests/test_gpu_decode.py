@@ -301,3 +301,31 @@ def test_qwen_full_size_step_from_synthetic_context(M):
     if top2_gap(ref) > TIE_GAP:
         assert gid == O.argmax(ref.astype(np.float32))[0]
     assert g.error_word() == 0
+
+
+@pytest.mark.parametrize("shape,n_ctx", [("llama", 4096), ("qwen", 2048)])
+def test_long_context_attention_streamed_through_the_ring(M, shape, n_ctx):
+    """Contexts long enough that every attention split fills a K/V stage, so
+    the persistent kernel streams the cached K/V through its shared-memory
+    ring (bf16 K/V for the 8B widths, fp32 for the Qwen widths): two steps
+    from a synthetic prefilled context against the oracle."""
+    cfg = small_bf16(C.LLAMA3_8B if shape == "llama" else C.QWEN3_0_6B, 2)
+    W = synth.model_weights(cfg, seed=9, device="cuda")
+    g = M.DecodeModel(cfg, W, capacity=n_ctx + 16, block_tokens=16)
+    ks, vs = synth.synthetic_kv(cfg, n_ctx, seed=10, device="cuda")
+    for l in range(cfg["n_layer"]):
+        g.k_cache[l][:n_ctx].copy_(ks[l])
+        g.v_cache[l][:n_ctx].copy_(vs[l])
+    o = oracle_model(cfg, synth.weights_to_numpy(W), g.capacity)
+    for l in range(cfg["n_layer"]):
+        o.k[l][:ks[l].numel()] = host(ks[l]).ravel()
+        o.v[l][:vs[l].numel()] = host(vs[l]).ravel()
+    toks = synth.prompt_ids(cfg, 2, seed=11)
+    for i, t in enumerate(toks):
+        g.set_state([t], [n_ctx + i])
+        g.step()
+        ref = o.step(t, n_ctx + i)
+        assert rel_err(host(g.logits[0]), ref) <= BF16_TOL, i
+        if top2_gap(ref) > TIE_GAP:
+            assert int(g.next_ids[0]) == O.argmax(ref.astype(np.float32))[0]
+    assert g.error_word() == 0
