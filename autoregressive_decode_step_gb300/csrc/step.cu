@@ -464,13 +464,21 @@ struct StepCtx {
 // ---------------------------------------------------------------- consumers
 __device__ __forceinline__ float silu_st(float z) { return z / (1.0f + expf(-z)); }
 
+// The first square-sum word thread t < 32 adds in scale_from_sst, loaded
+// ahead of time (0 for the other threads).
+__device__ __forceinline__ u64 sst_first(const StepParams &p) {
+    return threadIdx.x < 32 && (int)threadIdx.x < p.n_ss ? ld_tag(p.sst + threadIdx.x) : 0ull;
+}
+
 // RMS scale 1/sqrt(mean(r^2) + eps) of the residual whose per-band square sums
-// (tagged `tag`) are p.sst[0..n_ss), summed in lane order then across lanes.
-__device__ float scale_from_sst(const StepParams &p, int n, uint32_t tag, float *red) {
+// (tagged `tag`) are p.sst[0..n_ss), summed in lane order then across lanes;
+// `first` is thread t's word p.sst[t] as sst_first loaded it.
+__device__ float scale_from_sst(const StepParams &p, int n, uint32_t tag, float *red, u64 first) {
     const int t = threadIdx.x;
     if (t < 32) {
         float v = 0.0f;
-        for (int b = t; b < p.n_ss; b += 32) v += ld_wait(p.sst + b, tag, p);
+        if (t < p.n_ss) v += tag_value(first, p.sst + t, tag, p);
+        for (int b = t + 32; b < p.n_ss; b += 32) v += ld_wait(p.sst + b, tag, p);
         v = warp_sum(v);
         if (t == 0) red[0] = v;
     }
@@ -591,11 +599,42 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
 
     float scale = 1.0f;
     bool have_scale = !NORM;
+    // the RMSNorm's square sums, requested now and summed at the first epilogue
+    const u64 ss_w = NORM ? sst_first(p) : 0ull;
+    // What an epilogue of `band` reads besides the column sums, requested
+    // before those are waited for so that one L2 round trip covers all: for
+    // q|k|v, RoPE's cos/sin of this thread's column and the cache row of pos.
+    struct EpiIn {
+        float c, sn;
+        long long row;
+    };
+    auto epi_in = [&](int band) {
+        EpiIn e{1.0f, 0.0f, 0};
+        if (EPI == ST_QKV && cx.pos_ok) {
+            const int col = band * BAND_COLS + t;
+            if (t < BAND_COLS && col < p.nq_cols + p.nkv_cols) {
+                const int hd = p.hd, half = hd >> 1;
+                const int i = (col - (col < p.nq_cols ? 0 : p.nq_cols)) % hd;
+                const int pair = p.rope_layout == DS_ROPE_HALF_SPLIT ? (i < half ? i : i - half) : i >> 1;
+                e.c = __ldg(p.rope_cos + (size_t)cx.pos * half + pair);
+                e.sn = __ldg(p.rope_sin + (size_t)cx.pos * half + pair);
+            }
+            const int blk = p.block_table ? __ldcg(p.block_table + cx.pos / p.block_tokens) : cx.pos / p.block_tokens;
+            e.row = (long long)blk * p.block_tokens + cx.pos % p.block_tokens;
+        }
+        return e;
+    };
+    // the band this CTA settles (see below) is the first of its range when
+    // that range starts inside a band and reaches the band's end
+    const int b_first = (int)(u0 / UB);
+    const bool settles = u0 % UB != 0 && u1 >= (long long)(b_first + 1) * UB;
+    const EpiIn own_in = settles ? epi_in(b_first) : EpiIn{1.0f, 0.0f, 0};
     // the fused epilogue of one band whose column sums v (thread t < BAND_COLS)
-    // are final; yw is the residual word already loaded (ST_ADD)
-    auto epilogue = [&](int band, float v, u64 yw) {
+    // are final; yw is the residual word already loaded (ST_ADD), ein what
+    // epi_in(band) loaded
+    auto epilogue = [&](int band, float v, u64 yw, const EpiIn &ein) {
         if (NORM && !have_scale) {
-            scale = scale_from_sst(p, K, in_tag, red);
+            scale = scale_from_sst(p, K, in_tag, red, ss_w);
             have_scale = true;
         }
         if (EPI == ST_STORE || EPI == ST_ADD) {
@@ -625,25 +664,18 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
                     const int hd = p.hd, half = hd >> 1;
                     const int region = col < p.nq_cols ? 0 : p.nq_cols;
                     const int i = (col - region) % hd;
-                    int pair;
                     float a, b;
                     bool first_of_pair;
                     if (p.rope_layout == DS_ROPE_HALF_SPLIT) {
                         first_of_pair = i < half;
-                        pair = first_of_pair ? i : i - half;
                         a = first_of_pair ? vals[t] : vals[t - half];
                         b = first_of_pair ? vals[t + half] : vals[t];
                     } else {
                         first_of_pair = (i & 1) == 0;
-                        pair = i >> 1;
                         a = first_of_pair ? vals[t] : vals[t - 1];
                         b = first_of_pair ? vals[t + 1] : vals[t];
                     }
-                    float c = 1.0f, sn = 0.0f;
-                    if (cx.pos_ok) {
-                        c = p.rope_cos[(size_t)cx.pos * half + pair];
-                        sn = p.rope_sin[(size_t)cx.pos * half + pair];
-                    }
+                    const float c = ein.c, sn = ein.sn;  // 1 and 0 where pos is past the tables
                     out = first_of_pair ? a * c - b * sn : a * sn + b * c;
                 }
                 if (col < p.nq_cols) {
@@ -651,9 +683,7 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
                 } else {
                     const int kv = col - p.nq_cols;  // k then v
                     if (cx.pos_ok) {
-                        const int blk = p.block_table ? __ldcg(p.block_table + cx.pos / p.block_tokens)
-                                                      : cx.pos / p.block_tokens;
-                        const long long row = (long long)blk * p.block_tokens + cx.pos % p.block_tokens;
+                        const long long row = ein.row;
                         if (kv < p.nkv_cols)
                             store_as(p.kc[layer], row * p.nkv_cols + kv, p.kv_dtype, out);
                         else
@@ -719,7 +749,7 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
         if (j0 == 0 && j1 == UB) {  // whole band here: final now
             u64 yw = 0;
             if (EPI == ST_ADD && t < BAND_COLS && band * BAND_COLS + t < sub_cols) yw = ld_tag(y + band * BAND_COLS + t);
-            epilogue(band, v, yw);
+            epilogue(band, v, yw, epi_in(band));
         } else if (j1 == UB) {  // this CTA holds the band's last box: it settles
             own_band = band;
             own_v = v;
@@ -750,7 +780,7 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
             }
             tot += own_v;
         }
-        epilogue(own_band, tot, yw);
+        epilogue(own_band, tot, yw, own_in);
     }
     trace_point(p, phase, 3);
 }
@@ -809,17 +839,31 @@ __device__ void prefetch_attention(int layer, const StepCtx &cx, const StepParam
 }
 
 // One CTA's share of the attention phase (id `pid`): item (kv head g, split)
-// = this CTA (CTAs past the items have none).  Eight warps take runs of eight
+// = this CTA (CTAs past the items have none).  Eight warps take runs of RUN
 // cached positions with an online softmax; the current position comes from
 // the tagged copy the q|k|v phase handed over.  Warps merge in shared memory
 // and the CTA publishes its split's (max, sum, accumulator) as tagged words;
 // splits past the context publish an empty record.  The splits of a head are
 // merged, in split order, by whoever reads the attention output next (the o
 // projection's prologue).
+//
+// Within a warp, lane L holds dims 4L..4L+3 of every row.  The RUN x GQ
+// partial dot products of a run are summed across the warp by halving
+// exchanges (at each round a lane keeps one half of its values and sends the
+// other half to the lane `b` apart), V - 1 shuffles in all instead of five per
+// product; afterwards lane L holds the whole score of pair L >> SH (head
+// pair / RUN, position pair % RUN), the lanes of one head form an aligned
+// group, and the softmax runs on one score per lane.  The weights reach every
+// lane through a few words of shared memory for the P.V products.
 template <typename KT, int GQ>
 __device__ void consume_attention(const Ring &r, uint32_t &fill, int layer, int pid, const StepCtx &cx,
                                   float *scratch, const StepParams &p, int phase) {
-    constexpr int RUN = 8;
+    constexpr int RUN = GQ >= 8 ? 4 : 8;              // positions per run
+    constexpr int V = RUN * GQ;                       // scores per run (<= 32)
+    constexpr int LV = V >= 32 ? 5 : V >= 16 ? 4 : V >= 8 ? 3 : V >= 4 ? 2 : 1;
+    constexpr int SH = 5 - LV;                        // lane bits below a pair's index
+    constexpr int WS = V + 8;                         // per-warp words: weights, then corrections
+    static_assert(V <= 32 && (1 << LV) == V, "RUN * GQ must be a power of two up to 32");
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int hd = p.hd;
     const int n_items = p.n_kvh * p.attn_splits;
@@ -833,6 +877,9 @@ __device__ void consume_attention(const Ring &r, uint32_t &fill, int layer, int 
     float *s_m = s_acc + kStConsumerWarps * GQ * hd;          // [8][GQ]
     float *s_l = s_m + kStConsumerWarps * GQ;                 // [8][GQ]
     float *s_q = s_l + kStConsumerWarps * GQ;                 // [GQ][hd]
+    float *s_w = s_q + GQ * hd + warp * WS;                   // this warp's [V] weights, [GQ] corrections
+    float *s_M = s_q + GQ * hd + kStConsumerWarps * WS;       // [GQ] merged max
+    float *s_L = s_M + GQ;                                    // [GQ] merged sum
 
     int per, n_eff;
     attention_split(cx, p, per, n_eff);
@@ -853,46 +900,50 @@ __device__ void consume_attention(const Ring &r, uint32_t &fill, int layer, int 
 
     float kf[RUN][4], vf[RUN][4];
     // bf16 caches: a run's rows are fetched packed (two registers per row) one
-    // run ahead and unpacked when their turn comes, so the next run's loads are
-    // in flight during this run's arithmetic
+    // run ahead; K is unpacked for the scores and V for the products, each
+    // just before its own next-run loads go out
     constexpr bool PACKED = sizeof(KT) == 2;
     uint2 rk[PACKED ? RUN : 1], rv[PACKED ? RUN : 1];
-    auto load_run = [&](int tb) {
-        const int nt = min(RUN, tc - tb);
+    auto row_off = [&](int tt) {
+        const int b = tt / p.block_tokens;
+        const long long blk = p.block_table ? (long long)__ldcg(p.block_table + b) : (long long)b;
+        return (blk * p.block_tokens + tt % p.block_tokens) * row_elems + (long long)g * hd + d0;
+    };
+    auto load_packed = [&](uint2 (&rw)[PACKED ? RUN : 1], const KT *base, int tb) {
+        if constexpr (PACKED) {
+            const int nt = min(RUN, tc - tb);
 #pragma unroll
-        for (int i = 0; i < RUN; ++i) {
-            const bool ok = active && i < nt;
-            long long off = 0;
-            if (ok) {
-                const int tt = tb + i, b = tt / p.block_tokens;
-                const long long blk = p.block_table ? (long long)__ldcg(p.block_table + b) : (long long)b;
-                off = (blk * p.block_tokens + tt % p.block_tokens) * row_elems + (long long)g * hd + d0;
+            for (int i = 0; i < RUN; ++i) {
+                rw[i] = make_uint2(0u, 0u);
+                if (active && i < nt)
+                    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];"
+                                 : "=r"(rw[i].x), "=r"(rw[i].y) : "l"(base + row_off(tb + i)));
             }
-            if constexpr (PACKED) {
-                rk[i] = make_uint2(0u, 0u);
-                rv[i] = make_uint2(0u, 0u);
-                if (ok) {
-                    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(rk[i].x), "=r"(rk[i].y) : "l"(kc + off));
-                    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(rv[i].x), "=r"(rv[i].y) : "l"(vc + off));
-                }
-            } else {
+        }
+    };
+    auto load_run = [&](int tb) {
+        if constexpr (PACKED) {
+            load_packed(rk, kc, tb);
+            load_packed(rv, vc, tb);
+        } else {
+            const int nt = min(RUN, tc - tb);
+#pragma unroll
+            for (int i = 0; i < RUN; ++i) {
+                const bool ok = active && i < nt;
+                const long long off = ok ? row_off(tb + i) : 0;
                 load4<KT>(kc, off, ok, kf[i]);
                 load4<KT>(vc, off, ok, vf[i]);
             }
         }
     };
-    auto unpack_run = [&]() {
+    auto unpack = [&](const uint2 (&rw)[PACKED ? RUN : 1], float (&f)[RUN][4]) {
         if constexpr (PACKED) {
 #pragma unroll
             for (int i = 0; i < RUN; ++i) {
-                kf[i][0] = __uint_as_float(rk[i].x << 16);
-                kf[i][1] = __uint_as_float(rk[i].x & 0xffff0000u);
-                kf[i][2] = __uint_as_float(rk[i].y << 16);
-                kf[i][3] = __uint_as_float(rk[i].y & 0xffff0000u);
-                vf[i][0] = __uint_as_float(rv[i].x << 16);
-                vf[i][1] = __uint_as_float(rv[i].x & 0xffff0000u);
-                vf[i][2] = __uint_as_float(rv[i].y << 16);
-                vf[i][3] = __uint_as_float(rv[i].y & 0xffff0000u);
+                f[i][0] = __uint_as_float(rw[i].x << 16);
+                f[i][1] = __uint_as_float(rw[i].x & 0xffff0000u);
+                f[i][2] = __uint_as_float(rw[i].y << 16);
+                f[i][3] = __uint_as_float(rw[i].y & 0xffff0000u);
             }
         }
     };
@@ -930,54 +981,108 @@ __device__ void consume_attention(const Ring &r, uint32_t &fill, int layer, int 
         }
         named_sync(1, kStConsumers);
     }
+    trace_point(p, phase, 1);
     const float scale = 1.0f / sqrtf((float)hd);
-    float m[GQ], l[GQ], acc[GQ][4];
+    const int pair = lane >> SH, pos_i = pair % RUN;
+    const bool pair_lead = (lane & ((1 << SH) - 1)) == 0;
+    float mh = -INFINITY, lh = 0.0f;  // this lane's head (pair / RUN): running max and sum
+    float acc[GQ][4];
 #pragma unroll
-    for (int j = 0; j < GQ; ++j) {
-        m[j] = -INFINITY;
-        l[j] = 0.0f;
+    for (int j = 0; j < GQ; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
-    }
-    // one online-softmax update by `nt` positions whose K/V rows are in kf/vf
-    auto update = [&](int nt) {
+    // the scores of the `nt` positions whose K rows are in kf: online-softmax
+    // state updated, their weights and the heads' corrections left in s_w
+    auto scores = [&](int nt) {
+        float v[V];
 #pragma unroll
         for (int j = 0; j < GQ; ++j) {
-            // q of head j, dims d0.. (read from shared memory where it was staged)
             const float4 qj = active ? *reinterpret_cast<const float4 *>(s_q + j * hd + d0) : make_float4(0.f, 0.f, 0.f, 0.f);
-            float sc[RUN];
 #pragma unroll
             for (int i = 0; i < RUN; ++i) {
-                float dd = fmaf(qj.x, kf[i][0], 0.0f);
+                float dd = qj.x * kf[i][0];
                 dd = fmaf(qj.y, kf[i][1], dd);
                 dd = fmaf(qj.z, kf[i][2], dd);
                 dd = fmaf(qj.w, kf[i][3], dd);
-                sc[i] = warp_sum(dd) * scale;
+                v[j * RUN + i] = dd;
             }
-            float mx = m[j];
-#pragma unroll
-            for (int i = 0; i < RUN; ++i)
-                if (i < nt) mx = fmaxf(mx, sc[i]);
-            const float corr = expf(m[j] - mx);
-            l[j] *= corr;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[j][e] *= corr;
-#pragma unroll
-            for (int i = 0; i < RUN; ++i)
-                if (i < nt) {
-                    const float w = expf(sc[i] - mx);
-                    l[j] += w;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[j][e] = fmaf(w, vf[i][e], acc[j][e]);
-                }
-            m[j] = mx;
         }
+#pragma unroll
+        for (int c = V, b = 16; c > 1; c >>= 1, b >>= 1) {
+            const bool up = (lane & b) != 0;
+#pragma unroll
+            for (int k = 0; k < c / 2; ++k) {
+                const float send = up ? v[k] : v[k + c / 2];
+                const float keep = up ? v[k + c / 2] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, b);
+            }
+        }
+        float s = v[0];
+#pragma unroll
+        for (int b = 1; b < (1 << SH); b <<= 1) s += __shfl_xor_sync(0xffffffffu, s, b);
+        s = pos_i < nt ? s * scale : -INFINITY;
+        float mx = s;
+#pragma unroll
+        for (int b = 1 << SH; b < (RUN << SH); b <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, b));
+        const float mn = fmaxf(mh, mx);  // finite: nt >= 1
+        const float corr = expf(mh - mn);
+        const float w = pos_i < nt ? expf(s - mn) : 0.0f;
+        float ws = w;
+#pragma unroll
+        for (int b = 1 << SH; b < (RUN << SH); b <<= 1) ws += __shfl_xor_sync(0xffffffffu, ws, b);
+        lh = fmaf(lh, corr, ws);
+        mh = mn;
+        if (pair_lead) {
+            s_w[pair] = w;
+            if (pos_i == 0) s_w[V + pair / RUN] = corr;
+        }
+        __syncwarp();
+    };
+    // acc = acc * correction + weights . V rows (in vf); s_w free afterwards
+    auto accumulate = [&]() {
+#pragma unroll
+        for (int j = 0; j < GQ; ++j) {
+            const float cj = s_w[V + j];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][e] *= cj;
+#pragma unroll
+            for (int i4 = 0; i4 < RUN; i4 += 4) {
+                const float4 w4 = *reinterpret_cast<const float4 *>(s_w + j * RUN + i4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[j][e] = fmaf(w4.x, vf[i4][e], acc[j][e]);
+                    acc[j][e] = fmaf(w4.y, vf[i4 + 1][e], acc[j][e]);
+                    acc[j][e] = fmaf(w4.z, vf[i4 + 2][e], acc[j][e]);
+                    acc[j][e] = fmaf(w4.w, vf[i4 + 3][e], acc[j][e]);
+                }
+            }
+        }
+        __syncwarp();
     };
     if (streamed) {
         // the cached positions arrive through the ring, kv_stage_pos per stage
         // (K rows, then V rows); warp w takes a stage's w-th eighth in runs
         const int P = p.kv_stage_pos, per_warp = P / kStConsumerWarps;
         const int row_bytes = hd * (int)sizeof(KT);
+        auto read_rows = [&](const unsigned char *base, int rb, int nt, float (&f)[RUN][4]) {
+#pragma unroll
+            for (int i = 0; i < RUN; ++i) {
+                const bool ok = active && i < nt;
+                const size_t off = (size_t)(rb + i) * row_bytes + (size_t)d0 * sizeof(KT);
+                if (sizeof(KT) == 2) {
+                    uint2 w = make_uint2(0u, 0u);
+                    if (ok) w = *reinterpret_cast<const uint2 *>(base + off);
+                    f[i][0] = __uint_as_float(w.x << 16);
+                    f[i][1] = __uint_as_float(w.x & 0xffff0000u);
+                    f[i][2] = __uint_as_float(w.y << 16);
+                    f[i][3] = __uint_as_float(w.y & 0xffff0000u);
+                } else {
+                    float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (ok) w = *reinterpret_cast<const float4 *>(base + off);
+                    f[i][0] = w.x; f[i][1] = w.y; f[i][2] = w.z; f[i][3] = w.w;
+                }
+            }
+        };
         for (int ts = t0; ts < tc; ts += P) {
             const int s = fill % r.stages;
             const uint32_t use = fill / r.stages;
@@ -987,35 +1092,10 @@ __device__ void consume_attention(const Ring &r, uint32_t &fill, int layer, int 
                 for (int rb = warp * per_warp; rb < (warp + 1) * per_warp; rb += RUN) {
                     const int nt = min(RUN, tc - (ts + rb));
                     if (nt <= 0) break;
-#pragma unroll
-                    for (int i = 0; i < RUN; ++i) {
-                        const bool ok = active && i < nt;
-                        const size_t off = (size_t)(rb + i) * row_bytes + (size_t)d0 * sizeof(KT);
-                        if (sizeof(KT) == 2) {
-                            uint2 kw = make_uint2(0u, 0u), vw = make_uint2(0u, 0u);
-                            if (ok) {
-                                kw = *reinterpret_cast<const uint2 *>(kb + off);
-                                vw = *reinterpret_cast<const uint2 *>(vb + off);
-                            }
-                            kf[i][0] = __uint_as_float(kw.x << 16);
-                            kf[i][1] = __uint_as_float(kw.x & 0xffff0000u);
-                            kf[i][2] = __uint_as_float(kw.y << 16);
-                            kf[i][3] = __uint_as_float(kw.y & 0xffff0000u);
-                            vf[i][0] = __uint_as_float(vw.x << 16);
-                            vf[i][1] = __uint_as_float(vw.x & 0xffff0000u);
-                            vf[i][2] = __uint_as_float(vw.y << 16);
-                            vf[i][3] = __uint_as_float(vw.y & 0xffff0000u);
-                        } else {
-                            float4 kw = make_float4(0.f, 0.f, 0.f, 0.f), vw = kw;
-                            if (ok) {
-                                kw = *reinterpret_cast<const float4 *>(kb + off);
-                                vw = *reinterpret_cast<const float4 *>(vb + off);
-                            }
-                            kf[i][0] = kw.x; kf[i][1] = kw.y; kf[i][2] = kw.z; kf[i][3] = kw.w;
-                            vf[i][0] = vw.x; vf[i][1] = vw.y; vf[i][2] = vw.z; vf[i][3] = vw.w;
-                        }
-                    }
-                    update(nt);
+                    read_rows(kb, rb, nt, kf);
+                    scores(nt);
+                    read_rows(vb, rb, nt, vf);
+                    accumulate();
                 }
             }
             __syncwarp();
@@ -1027,11 +1107,16 @@ __device__ void consume_attention(const Ring &r, uint32_t &fill, int layer, int 
     while (tb < tc) {
         const int nt = min(RUN, tc - tb), tn = tb + kStConsumerWarps * RUN;
         if constexpr (PACKED) {
-            unpack_run();
-            if (tn < tc) load_run(tn);  // the next run's loads go out before this run's arithmetic
-            update(nt);
+            // the next run's loads go out before this run's arithmetic
+            unpack(rk, kf);
+            if (tn < tc) load_packed(rk, kc, tn);
+            scores(nt);
+            unpack(rv, vf);
+            if (tn < tc) load_packed(rv, vc, tn);
+            accumulate();
         } else {
-            update(nt);
+            scores(nt);
+            accumulate();
             if (tn < tc) load_run(tn);
         }
         tb = tn;
@@ -1039,40 +1124,59 @@ __device__ void consume_attention(const Ring &r, uint32_t &fill, int layer, int 
     if (cur_warp) {  // the current position
         tag_fix_at<8>(cw, ca, q_tag, p);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            kf[0][e] = active ? tag_f(cw[e]) : 0.0f;
-            vf[0][e] = active ? tag_f(cw[4 + e]) : 0.0f;
-        }
-        update(1);
+        for (int i = 0; i < RUN; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                kf[i][e] = i == 0 && active ? tag_f(cw[e]) : 0.0f;
+                vf[i][e] = i == 0 && active ? tag_f(cw[4 + e]) : 0.0f;
+            }
+        scores(1);
+        accumulate();
+    }
+    if (pair_lead && pos_i == 0) {
+        s_m[warp * GQ + pair / RUN] = mh;
+        s_l[warp * GQ + pair / RUN] = lh;
     }
 #pragma unroll
-    for (int j = 0; j < GQ; ++j) {
-        if (lane == 0) {
-            s_m[warp * GQ + j] = m[j];
-            s_l[warp * GQ + j] = l[j];
-        }
+    for (int j = 0; j < GQ; ++j)
         if (active)
 #pragma unroll
             for (int e = 0; e < 4; ++e) s_acc[(warp * GQ + j) * hd + d0 + e] = acc[j][e];
-    }
     named_sync(1, kStConsumers);
     trace_point(p, phase, 2);
 
+    // the warps' weights exp(m_w - M) per head, and the merged max and sum:
+    // warp 0, one (head, warp) pair per lane, eight lanes per head
+    if (warp == 0)
+        for (int p0 = 0; p0 < GQ * kStConsumerWarps; p0 += 32) {
+            const int pr = p0 + lane, j = pr / kStConsumerWarps, w = pr % kStConsumerWarps;
+            const bool ok = pr < GQ * kStConsumerWarps;
+            const float mw = ok ? s_m[w * GQ + j] : -INFINITY;
+            float M = mw;
+#pragma unroll
+            for (int b = 1; b < kStConsumerWarps; b <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, b));
+            const float c = mw == -INFINITY ? 0.0f : expf(mw - M);
+            float L = ok ? s_l[w * GQ + j] * c : 0.0f;
+#pragma unroll
+            for (int b = 1; b < kStConsumerWarps; b <<= 1) L += __shfl_xor_sync(0xffffffffu, L, b);
+            if (ok) {
+                s_m[w * GQ + j] = c;  // each lane rewrites only the entry it read
+                if (w == 0) {
+                    s_M[j] = M;
+                    s_L[j] = L;
+                }
+            }
+        }
+    named_sync(1, kStConsumers);
     for (int idx = t; idx < GQ * hd; idx += kStConsumers) {
         const int j = idx / hd;
-        float M = -INFINITY;
-        for (int w = 0; w < kStConsumerWarps; ++w) M = fmaxf(M, s_m[w * GQ + j]);
-        float L = 0.0f, A = 0.0f;
-        if (M != -INFINITY)
-            for (int w = 0; w < kStConsumerWarps; ++w) {
-                const float c = expf(s_m[w * GQ + j] - M);
-                L = fmaf(s_l[w * GQ + j], c, L);
-                A = fmaf(s_acc[(w * GQ + j) * hd + idx % hd], c, A);
-            }
+        float A = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kStConsumerWarps; ++w) A = fmaf(s_acc[(w * GQ + j) * hd + idx % hd], s_m[w * GQ + j], A);
         st_tag(out + 2 * GQ + idx, A, out_tag);
         if (idx % hd == 0) {
-            st_tag(out + j, M, out_tag);
-            st_tag(out + GQ + j, L, out_tag);
+            st_tag(out + j, s_M[j], out_tag);
+            st_tag(out + GQ + j, s_L[j], out_tag);
         }
     }
     trace_point(p, phase, 3);
@@ -1206,7 +1310,7 @@ __device__ void consume_gn(const Ring &r, uint32_t &fill, uint32_t in_tag, float
         }
     }
     named_sync(1, kStConsumers);
-    const float scale = scale_from_sst(p, cols, in_tag, bestv);
+    const float scale = scale_from_sst(p, cols, in_tag, bestv, sst_first(p));
     trace_point(p, phase, 1);
 
     const int chunks = (int)(row_bytes / 16);
@@ -1466,7 +1570,8 @@ int step_scratch_floats(const ds_model_config *c, int grid, int nb_qkv, int nb_o
     gt += kStConsumerWarps * 256 + 256 + 16;
     const int gq = c->n_qh / c->n_kvh;
     const long long at = std::max((long long)kStConsumerWarps * gq * c->head_dim, 2LL * kStMaxSplits * gq + 2 * gq) +
-                         2LL * kStConsumerWarps * gq + (long long)gq * c->head_dim + 16;
+                         2LL * kStConsumerWarps * gq + (long long)gq * c->head_dim +
+                         kStConsumerWarps * 40LL + 2LL * gq + 16;  // + per-warp run weights, merged max/sum
     const long long row_bytes = (long long)c->d * es;
     const long long rps = std::max(1LL, (long long)kStStageBytes / row_bytes);
     const long long parts = rps >= kStConsumerWarps ? 1 : kStConsumerWarps / rps;
