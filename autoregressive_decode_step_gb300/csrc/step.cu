@@ -47,6 +47,9 @@ constexpr int kStBandBytes = 512;
 #define DS_ST_ATTN_MIN_PER 64
 #endif
 constexpr int kStAttnMinPer = DS_ST_ATTN_MIN_PER;  // fewest positions per attention split
+// split records an attention merge requests at once (all of a head's splits
+// in one batch up to this count)
+constexpr int kStMergeBatch = 20;
 constexpr int kStBoxesPerStage = kStStageBytes / (kStBoxRows * kStBandBytes);  // 8 boxes of 16 rows at 64 KB
 constexpr size_t kStSmemLimit = 227 * 1024;
 
@@ -1232,13 +1235,13 @@ __device__ void stage_attention_rows(int k0, int k1, float *xs, float *red, uint
         const int h = k / hd, g = h / GQ, j = h % GQ, hl = h - h_lo;
         const u64 *rp = p.at + (size_t)g * p.attn_splits * rec + 2 * GQ + j * hd + k % hd;
         float A = 0.0f;
-        for (int s0 = 0; s0 < n_eff; s0 += 16) {
-            u64 w[16];
+        for (int s0 = 0; s0 < n_eff; s0 += kStMergeBatch) {
+            u64 w[kStMergeBatch];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = s0 + i < n_eff ? ld_tag(rp + (size_t)(s0 + i) * rec) : 0ull;
-            tag_fix<16>(w, rp + (size_t)s0 * rec, rec, n_eff - s0, tag, p);
+            for (int i = 0; i < kStMergeBatch; ++i) w[i] = s0 + i < n_eff ? ld_tag(rp + (size_t)(s0 + i) * rec) : 0ull;
+            tag_fix<kStMergeBatch>(w, rp + (size_t)s0 * rec, rec, n_eff - s0, tag, p);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < kStMergeBatch; ++i)
                 if (s0 + i < n_eff) A = fmaf(tag_f(w[i]), wt[hl * kStMaxSplits + s0 + i], A);
         }
         xs[k - k0] = A / Lh[hl];
