@@ -269,23 +269,25 @@ def kernel_source_sha():
     return h.hexdigest()
 
 
-def profile_summary_traffic(kernel_src_sha):
-    """DRAM bytes per full-size step-kernel launch from the committed ncu
-    summary, if it was taken on the current kernel source (else None)."""
+def profile_summary_traffic_ratio(kernel_src_sha):
+    """DRAM bytes over algorithmic bytes of the step kernel, from the
+    committed ncu summary if it was taken on the current kernel source (else
+    None).  Traffic is proportional to the bytes streamed, so a launch's
+    traffic is this ratio times its algorithmic bytes."""
     try:
         text = open(STEP_PROFILE).read()
     except OSError:
         return None
-    sha = traffic = None
+    sha = ratio = None
     for line in text.splitlines():
         if line.startswith("- kernel source sha256:"):
             sha = line.split(":", 1)[1].strip()
-        if line.startswith("- dram bytes per launch:"):
+        if line.startswith("- dram bytes / algorithmic bytes:"):
             try:
-                traffic = float(line.split(":", 1)[1].strip().split()[0].replace(",", ""))
+                ratio = float(line.split(":", 1)[1].strip().split()[0])
             except ValueError:
-                traffic = None
-    return traffic if sha == kernel_src_sha else None
+                ratio = None
+    return ratio if sha == kernel_src_sha else None
 
 
 def run_batched(cfg, W, dev, rank, clocks_cls, bus, warmup=3, steps=None):
@@ -518,8 +520,10 @@ def run_ours(args, rank, world, local):
     alg_bytes = sum(step_bytes) / n_launch
     launch_us = ms * 1000.0 / n_launch
     achieved = alg_bytes / (launch_us / 1e6) / 1e9
+    ratio = profile_summary_traffic_ratio(kernel_source_sha()) if args.layers is None else None
+    traffic = ratio * alg_bytes if ratio is not None else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profile_summary_traffic(kernel_source_sha()) if args.layers is None else None,
+                "traffic": traffic,
                 "kernel": "step_kernel: persistent cooperative decode step (all layers + head + argmax); "
                           + ("%d greedy steps per launch, picks handed over on the device" % args.chunk
                              if chunks else "one launch per token"),
