@@ -52,6 +52,9 @@ constexpr int kTcEpiThreads = 128;
 constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
 constexpr int kTcMaxStages = 8;
 constexpr int kTcXchStride = 33;  // floats per feature row of the epilogue exchange buffer
+constexpr int kTcMaxN = 256;      // vectors per launch (the MMA's largest N)
+constexpr int kTcSmemInts = 16 + 2 * kTcMaxN;  // tmem address, flags, agreement words, per-vector rows
+constexpr int kTcMaxContrib = 4;  // split partials a last arriver requests at once
 constexpr size_t kTcSmemLimit = 227 * 1024;
 
 // ---------------------------------------------------------------- tcgen05 PTX
@@ -164,11 +167,22 @@ __device__ __forceinline__ bool tc_next_seg(long long &u, long long u1, int KB, 
 
 __device__ __forceinline__ float silu_tc(float z) { return z / (1.0f + expf(-z)); }
 
+// The residual values (TC_ADD) of one chunk for the tile's feature of this
+// thread, requested before the chunk's sums are waited for.
+__device__ __forceinline__ void tc_load_residual(const TcArgs &p, int tile, int chunk, int r, float (&old)[32]) {
+    const int j0 = chunk * 32, m = tile * kTcBM + r;
+    const int nj = min(32, p.n - j0);
+    const float *col = p.y + (long long)j0 * p.ldy + m;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) old[i] = (m < p.M && i < nj) ? __ldcg(col + (long long)i * p.ldy) : 0.0f;
+}
+
 // One chunk (32 sequences) of the fused epilogue for the tile's feature of
-// this thread (row r of the accumulator).
+// this thread (row r of the accumulator); `old` is the chunk's residual as
+// tc_load_residual left it (TC_ADD only).
 template <int EPI>
-__device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const float (&v)[32], float *xch,
-                                  int *s_row, int r) {
+__device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const float (&v)[32], const float (&old)[32],
+                                  float *xch, int *s_row, int r) {
     const int j0 = chunk * 32;
     if constexpr (EPI == TC_STORE || EPI == TC_ADD) {
         const int m = tile * kTcBM + r;
@@ -176,10 +190,6 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
             float *col = p.y + (long long)j0 * p.ldy + m;
             const int nj = min(32, p.n - j0);
             if constexpr (EPI == TC_ADD) {
-                // every residual load of the chunk goes out before the first store
-                float old[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) old[i] = i < nj ? __ldcg(col + (long long)i * p.ldy) : 0.0f;
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     if (i < nj) col[(long long)i * p.ldy] = old[i] + v[i];
@@ -194,24 +204,6 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
     // SILU and QKV exchange values between partner features through shared memory
 #pragma unroll
     for (int i = 0; i < 32; ++i) xch[r * kTcXchStride + i] = v[i];
-    if (EPI == TC_QKV && r < 32) {  // cache rows of this chunk's sequences
-        const int j = j0 + r;
-        int row = -1;
-        if (j < p.n) {
-            const int pos = __ldcg(p.pos + j);
-            const int cap = p.max_blocks * p.block_tokens;
-            if (pos >= 0 && pos < cap && pos < p.rope_rows) {
-                const int b = pos / p.block_tokens;
-                const long long blk = p.block_table ? (long long)__ldcg(p.block_table + (long long)j * p.max_blocks + b)
-                                                    : (long long)j * p.max_blocks + b;
-                const long long rr = blk * p.block_tokens + pos % p.block_tokens;
-                if (blk >= 0 && rr < p.cache_rows) row = (int)rr;
-            }
-            if (row < 0 && tile == 0) flag_error(p.err, DS_ERR_POSITION);
-            s_row[32 + r] = pos;
-        }
-        s_row[r] = row;
-    }
     named_sync(1, kTcEpiThreads);
     if constexpr (EPI == TC_SILU) {
         const int g = tile * (kTcBM / 2) + r;
@@ -262,7 +254,7 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
                 cs[i] = 1.0f;
                 sn[i] = 0.0f;
                 if (rot && i < nj) {
-                    const int pos = s_row[32 + i];
+                    const int pos = s_row[kTcMaxN + j0 + i];
                     if (pos >= 0 && pos < p.rope_rows) {
                         cs[i] = __ldg(p.rope_cos + (long long)pos * half + pair);
                         sn[i] = __ldg(p.rope_sin + (long long)pos * half + pair);
@@ -274,7 +266,7 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
                 const int j = j0 + i;
                 if (i >= nj) break;
                 float out = xch[r * kTcXchStride + i];
-                const int row = s_row[i];
+                const int row = s_row[j0 + i];
                 if (rot) {
                     const float o = xch[partner * kTcXchStride + i];
                     out = first ? out * cs[i] - o * sn[i] : o * sn[i] + out * cs[i];
@@ -313,9 +305,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     uint64_t *mma_done = acc_empty + 2;          // [1]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(mma_done + 1);
     int *s_flags = reinterpret_cast<int *>(s_tmem + 1);  // [0] abort, [1] last-arriver broadcast
-    int *s_row = s_flags + 2;                             // [64]
-    int *s_ok = s_row + 64;                               // [2][4]
-    float *xch = reinterpret_cast<float *>(s_ok + 8);     // [128][33]
+    int *s_ok = s_flags + 2;                              // [2][4]
+    int *s_row = s_ok + 8;                                // [2][kTcMaxN] cache row, position (q|k|v)
+    float *xch = reinterpret_cast<float *>(s_row + 2 * kTcMaxN);  // [128][33]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = (p.K + kTcBK - 1) / kTcBK;
@@ -469,6 +461,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         int seg_i = 0;
         TcSeg sg;
         const int n_chunks = p.n_pad / 32;
+        if (EPI == TC_QKV) {  // every vector's cache row and position, before any accumulator is awaited
+            const int cap = p.max_blocks * p.block_tokens;
+            for (int j = et; j < p.n_pad; j += kTcEpiThreads) {
+                int row = -1, pos = -1;
+                if (j < p.n) {
+                    pos = __ldcg(p.pos + j);
+                    if (pos >= 0 && pos < cap && pos < p.rope_rows) {
+                        const int b = pos / p.block_tokens;
+                        const long long blk = p.block_table
+                                                  ? (long long)__ldcg(p.block_table + (long long)j * p.max_blocks + b)
+                                                  : (long long)j * p.max_blocks + b;
+                        const long long rr = blk * p.block_tokens + pos % p.block_tokens;
+                        if (blk >= 0 && rr < p.cache_rows) row = (int)rr;
+                    }
+                    if (row < 0 && blockIdx.x == 0) flag_error(p.err, DS_ERR_POSITION);
+                }
+                s_row[j] = row;
+                s_row[kTcMaxN + j] = pos;
+            }
+            named_sync(1, kTcEpiThreads);
+        }
         while (tc_next_seg(u, u1, KB, sg)) {
             const int buf = seg_i & 1;
             // the four warps agree on whether the accumulator arrived, so none
@@ -486,14 +499,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             if (whole) {
                 for (int h = 0; h < MS; ++h)
                     for (int c = 0; c < n_chunks; ++c) {
-                        float v[32];
+                        float v[32], old[32];
+                        if (EPI == TC_ADD) tc_load_residual(p, sg.tile * MS + h, c, r, old);
                         tmem_ld32(tbase + h * p.n_pad + c * 32, v);
                         if (h == MS - 1 && c == n_chunks - 1) {  // the buffer may be reused once every lane has read it
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&acc_empty[buf]);
                         }
-                        tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, xch, s_row, r);
+                        tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, old, xch, s_row, r);
                     }
             } else {
                 // partial accumulators to this (CTA, tile) slot, feature-fastest per sub-tile
@@ -525,16 +539,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                     __threadfence();
                     for (int h = 0; h < MS; ++h)
                         for (int c = 0; c < n_chunks; ++c) {
-                            float v[32];
+                            float v[32], old[32];
+                            if (EPI == TC_ADD) tc_load_residual(p, sg.tile * MS + h, c, r, old);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-                            for (int cc = c_first; cc <= c_last; ++cc) {
-                                const float *src =
-                                    p.partials + ((size_t)cc + sg.tile) * MS * sub_floats + h * sub_floats;
+                            // up to kTcMaxContrib contributors' partials requested at once,
+                            // added in CTA order
+                            for (int c0 = c_first; c0 <= c_last; c0 += kTcMaxContrib) {
+                                float t[kTcMaxContrib][32];
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) v[i] += __ldcg(src + (size_t)(c * 32 + i) * kTcBM + r);
+                                for (int k = 0; k < kTcMaxContrib; ++k)
+                                    if (c0 + k <= c_last) {
+                                        const float *src =
+                                            p.partials + ((size_t)(c0 + k) + sg.tile) * MS * sub_floats + h * sub_floats;
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) t[k][i] = __ldcg(src + (size_t)(c * 32 + i) * kTcBM + r);
+                                    }
+#pragma unroll
+                                for (int k = 0; k < kTcMaxContrib; ++k)
+                                    if (c0 + k <= c_last)
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) v[i] += t[k][i];
                             }
-                            tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, xch, s_row, r);
+                            tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, old, xch, s_row, r);
                         }
                 }
                 named_sync(1, kTcEpiThreads);
@@ -556,14 +583,14 @@ int tc_n_pad(int n) { return std::max(32, (n + 31) / 32 * 32); }
 
 int tc_stages(int n_pad, int split, int msub) {
     const size_t stage = (size_t)msub * kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
-    const size_t fixed = 1024 + 256 + 72 * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
+    const size_t fixed = 1024 + 256 + kTcSmemInts * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
     int s = (int)((kTcSmemLimit - fixed) / stage);
     return std::min(s, kTcMaxStages);
 }
 
 size_t tc_smem_bytes(int n_pad, int split, int msub, int stages) {
     const size_t stage = (size_t)msub * kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
-    return 1024 + (size_t)stages * stage + 256 + 72 * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
+    return 1024 + (size_t)stages * stage + 256 + kTcSmemInts * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
 }
 
 int tc_m_tiles(int M, int epi) { return epi == TC_SILU ? (M + kTcBM / 2 - 1) / (kTcBM / 2) : (M + kTcBM - 1) / kTcBM; }
