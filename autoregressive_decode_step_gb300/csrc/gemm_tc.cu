@@ -53,7 +53,7 @@ constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
 constexpr int kTcMaxStages = 8;
 constexpr int kTcXchStride = 33;  // floats per feature row of the epilogue exchange buffer
 constexpr int kTcMaxN = 256;      // vectors per launch (the MMA's largest N)
-constexpr int kTcSmemInts = 16 + 2 * kTcMaxN;  // tmem address, flags, agreement words, per-vector rows
+constexpr int kTcSmemInts = 16 + 3 * kTcMaxN;  // tmem address, flags, agreement words, per-vector rows, scales
 constexpr int kTcMaxContrib = 4;  // split partials a last arriver requests at once
 constexpr size_t kTcSmemLimit = 227 * 1024;
 
@@ -182,13 +182,13 @@ __device__ __forceinline__ void tc_load_residual(const TcArgs &p, int tile, int 
 // tc_load_residual left it (TC_ADD only).
 template <int EPI>
 __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const float (&v)[32], const float (&old)[32],
-                                  float *xch, int *s_row, int r) {
+                                  float *xch, int *s_row, const float *s_scale, int r) {
     const int j0 = chunk * 32;
     if constexpr (EPI == TC_STORE || EPI == TC_ADD) {
         const int m = tile * kTcBM + r;
+        const int nj = min(32, p.n - j0);
         if (m < p.M) {
             float *col = p.y + (long long)j0 * p.ldy + m;
-            const int nj = min(32, p.n - j0);
             if constexpr (EPI == TC_ADD) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
@@ -199,11 +199,45 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
                     if (i < nj) col[(long long)i * p.ldy] = v[i];
             }
         }
+        if (EPI == TC_ADD && p.nw) {  // the next RMSNorm's input and this tile's square sums
+            float sq[32];
+            const float wm = m < p.M ? __ldg(p.nw + m) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float x = (m < p.M && i < nj) ? old[i] + v[i] : 0.0f;
+                sq[i] = x * x;
+                if (m < p.M && i < nj) {
+                    __nv_bfloat16 hi, lo;
+                    split_bf16(x * wm, hi, lo);
+                    const long long o = (long long)(j0 + i) * p.ldy + m;
+                    p.hb[o] = hi;
+                    p.hb[o + p.hb_lo] = lo;
+                }
+            }
+            // halving exchanges: lane L ends with the warp's 32 features summed for vector L
+            const int lane = r & 31;
+#pragma unroll
+            for (int c = 32, b = 16; c > 1; c >>= 1, b >>= 1) {
+                const bool up = (lane & b) != 0;
+#pragma unroll
+                for (int k = 0; k < c / 2; ++k) {
+                    const float send = up ? sq[k] : sq[k + c / 2];
+                    const float keep = up ? sq[k + c / 2] : sq[k];
+                    sq[k] = keep + __shfl_xor_sync(0xffffffffu, send, b);
+                }
+            }
+            xch[(r >> 5) * 32 + lane] = sq[0];
+            named_sync(1, kTcEpiThreads);
+            if (r < 32 && r < nj)
+                p.ssq[(long long)tile * p.ss_ld + j0 + r] = ((xch[r] + xch[32 + r]) + xch[64 + r]) + xch[96 + r];
+            named_sync(1, kTcEpiThreads);
+        }
         return;
     } else {
-    // SILU and QKV exchange values between partner features through shared memory
+    // SILU and QKV exchange values between partner features through shared
+    // memory, scaled by the folded RMSNorm (1 where there is none)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) xch[r * kTcXchStride + i] = v[i];
+    for (int i = 0; i < 32; ++i) xch[r * kTcXchStride + i] = v[i] * s_scale[j0 + i];
     named_sync(1, kTcEpiThreads);
     if constexpr (EPI == TC_SILU) {
         const int g = tile * (kTcBM / 2) + r;
@@ -307,7 +341,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     int *s_flags = reinterpret_cast<int *>(s_tmem + 1);  // [0] abort, [1] last-arriver broadcast
     int *s_ok = s_flags + 2;                              // [2][4]
     int *s_row = s_ok + 8;                                // [2][kTcMaxN] cache row, position (q|k|v)
-    float *xch = reinterpret_cast<float *>(s_row + 2 * kTcMaxN);  // [128][33]
+    float *s_scale = reinterpret_cast<float *>(s_row + 2 * kTcMaxN);  // [kTcMaxN] folded RMSNorm scales
+    float *xch = s_scale + kTcMaxN;                                   // [128][33]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = (p.K + kTcBK - 1) / kTcBK;
@@ -480,6 +515,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                 s_row[j] = row;
                 s_row[kTcMaxN + j] = pos;
             }
+        }
+        if (EPI == TC_QKV || EPI == TC_SILU) {  // the folded RMSNorm's scale of every vector
+            for (int j = et; j < p.n_pad; j += kTcEpiThreads) {
+                float sc = 1.0f;
+                if (p.ssq_in && j < p.n) {
+                    float tot = 0.0f;
+                    for (int t0 = 0; t0 < p.ss_tiles; t0 += 8) {
+                        float w[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            w[k] = t0 + k < p.ss_tiles ? __ldcg(p.ssq_in + (long long)(t0 + k) * p.ss_ld + j) : 0.0f;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (t0 + k < p.ss_tiles) tot += w[k];
+                    }
+                    sc = 1.0f / sqrtf(tot / (float)p.ss_d + p.eps);
+                }
+                s_scale[j] = sc;
+            }
             named_sync(1, kTcEpiThreads);
         }
         while (tc_next_seg(u, u1, KB, sg)) {
@@ -507,7 +561,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&acc_empty[buf]);
                         }
-                        tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, old, xch, s_row, r);
+                        tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, old, xch, s_row, s_scale, r);
                     }
             } else {
                 // partial accumulators to this (CTA, tile) slot, feature-fastest per sub-tile
@@ -561,7 +615,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
                                         for (int i = 0; i < 32; ++i) v[i] += t[k][i];
                             }
-                            tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, old, xch, s_row, r);
+                            tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, old, xch, s_row, s_scale, r);
                         }
                 }
                 named_sync(1, kTcEpiThreads);

@@ -95,7 +95,7 @@ using namespace ds;
 struct Layout {
     size_t x, q, att, f, logits, rope_cos, rope_sin, g_counters, g_partials, a_counters, a_partials, am_val,
         am_idx, am_counter, step_layers, step_bar, phase_times, trace, st_x, st_q, st_kv, st_f, st_ss, st_part,
-        st_att, h_bf, att_bf, f_bf, tc_counters, tc_partials, b_am_counters, kv_maps, total;
+        st_att, h_bf, att_bf, f_bf, tc_counters, tc_partials, tc_ssq, b_am_counters, kv_maps, total;
     int b_splits, tc_tiles;
     size_t st_part_stride;
     int grid_qkv, grid_o, grid_gu, grid_d, grid_head, nb_qkv, nb_o, nb_gu, nb_d, attn_splits;
@@ -229,6 +229,8 @@ Layout make_layout(const ds_model_config *c) {
         L.f_bf = carve(off, (size_t)2 * S * c->ff * 2);
         L.tc_counters = carve(off, (size_t)L.tc_tiles * 4);
         L.tc_partials = carve(off, tc_partial_floats(L.tc_tiles, tc_n_pad(S), 2) * 4);
+        // per 128-feature tile of the residual, each sequence's square sum (the folded RMSNorms)
+        L.tc_ssq = carve(off, (size_t)tc_m_tiles(c->d, TC_ADD) * S * 4);
         L.b_am_counters = carve(off, (size_t)S * 4);
     }
     L.total = off;
@@ -646,6 +648,28 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
             ok = ok && mk(TC_ADD, 1, m->wd[l], nullptr, (long long)cfg->d * es, cfg->d, cfg->ff, m->f_bf, dn, 1);
             dn.y = m->x;
             dn.ldy = cfg->d;
+            // RMSNorms folded into the projections: o and down also write the
+            // next norm's input (x * weight, hi/lo) and per-tile square sums;
+            // gate|up and the next layer's q|k|v apply the 1/rms scale
+            float *ssq = reinterpret_cast<float *>(ws + L.tc_ssq);
+            auto fold_out = [&](TcArgs &a, const float *nw) {
+                a.nw = nw;
+                a.hb = static_cast<__nv_bfloat16 *>(m->h_bf);
+                a.hb_lo = (long long)S * cfg->d;
+                a.ssq = ssq;
+                a.ss_ld = S;
+            };
+            auto fold_in = [&](TcArgs &a) {
+                a.ssq_in = ssq;
+                a.ss_tiles = tc_m_tiles(cfg->d, TC_ADD);
+                a.ss_ld = S;
+                a.ss_d = cfg->d;
+                a.eps = cfg->eps;
+            };
+            fold_out(o, w->n2[l]);
+            fold_in(gu);
+            if (l + 1 < cfg->n_layer) fold_out(dn, w->n1[l + 1]);
+            if (l > 0) fold_in(q);
         }
         TcArgs &hd = m->tc[(size_t)4 * cfg->n_layer];
         ok = ok && mk(TC_STORE, 0, m->out, nullptr, (long long)cfg->d * es, cfg->vocab, cfg->d, m->h_bf, hd, 2);
@@ -841,7 +865,9 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
     const long long h_lo = (long long)c.max_seqs * c.d;  // hi rows, then lo rows
     DS_TRYB(launch_embed(m->emb, c.w_dtype, c.vocab, c.d, tokens, m->x, m->err, n, s, pdl));
     for (int l = 0; l < c.n_layer; ++l) {
-        DS_TRYB(launch_rmsnorm_rows_bf16(m->x, m->n1[l], c.eps, m->h_bf, h_lo, n, c.d, s, pdl));
+        // the first layer's norm runs alone; every later one is folded into
+        // the projection writing the residual and the one reading it
+        if (l == 0) DS_TRYB(launch_rmsnorm_rows_bf16(m->x, m->n1[l], c.eps, m->h_bf, h_lo, n, c.d, s, pdl));
         TcArgs a = m->tc[4 * l + 0];
         a.n = n;
         a.pos = pos;
@@ -928,7 +954,6 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
         a = m->tc[4 * l + 1];
         a.n = n;
         DS_TRYB(gemm(a));
-        DS_TRYB(launch_rmsnorm_rows_bf16(m->x, m->n2[l], c.eps, m->h_bf, h_lo, n, c.d, s, pdl));
         a = m->tc[4 * l + 2];
         a.n = n;
         DS_TRYB(gemm(a));

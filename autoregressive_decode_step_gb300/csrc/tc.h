@@ -45,6 +45,20 @@ struct TcArgs {
     int nq_cols, nkv_cols, head_dim, rope_layout;
     void *k_cache, *v_cache;
     int kv_dtype;
+    // TC_ADD with nw set: the next RMSNorm folded in.  Besides y += acc it
+    // writes x * nw (x the updated residual) as bf16 hi/lo to hb[s * ldy + m]
+    // (lo part hb_lo elements further) and each 128-feature tile's square sums
+    // of x to ssq[tile * ss_ld + s].
+    const float *nw;
+    __nv_bfloat16 *hb;
+    long long hb_lo;
+    float *ssq;
+    // TC_QKV / TC_SILU with ssq_in set: the consuming side of that norm.  The
+    // output of vector s is scaled by 1 / sqrt(sum_t ssq_in[t * ss_ld + s] /
+    // ss_d + eps) (t < ss_tiles, added in order) before RoPE or SiLU.
+    const float *ssq_in;
+    int ss_tiles, ss_ld, ss_d;
+    float eps;
     // split tiles: partial accumulators and arrival counters (zero between launches)
     float *partials;
     int *counters;
