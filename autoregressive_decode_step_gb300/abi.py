@@ -92,6 +92,7 @@ _sig("ds_gemv_transposed", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64,
 _sig("ds_gemv", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P)
 _sig("ds_gemm_workspace_bytes", SZ, I64, I64, I64)
 _sig("ds_decode_steps", ctypes.c_int, P, P, P, P, ctypes.c_int, P, P, ctypes.c_uint, P)
+_sig("ds_step_seq", ctypes.c_int, P, P, P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P)
 _sig("ds_gemm_transposed", ctypes.c_int, P, I64, P, I64, I64, I64, I64, P, I64, P, SZ, P)
 _sig("ds_gemm", ctypes.c_int, P, I64, P, I64, I64, I64, I64, P, I64, P, SZ, P)
 _sig("ds_gemv_transposed_noalloc", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P)

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const __grid_co
     grid_dependency_wait();
 
     const int cap = p.max_blocks * p.block_tokens;
+    const int cseq = p.row_seq ? p.row_seq[seq] : seq;  // whose blocks this row reads
     int n_ctx = p.seq_lens ? p.seq_lens[seq] : p.pos[seq] + 1;
     if (n_ctx < 1 || n_ctx > cap) {
         if (threadIdx.x == 0 && split == 0 && g == 0) flag_error(p.err, DS_ERR_POSITION);
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < kAttnRun; ++i) {
             const bool ok = active && i < nt;
-            const long long off = ok ? kv_row(seq, tb + i, p.block_table, p.max_blocks, p.block_tokens) * row_elems +
+            const long long off = ok ? kv_row(cseq, tb + i, p.block_table, p.max_blocks, p.block_tokens) * row_elems +
                                            (long long)g * hd + d0
                                      : 0;
             load_dims<KT, DPL>(kc, off, ok, kf[i]);

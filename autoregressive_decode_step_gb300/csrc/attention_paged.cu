@@ -201,8 +201,9 @@ __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_kernel
             for (long long u = u0; u < u1; ++u) {
                 while (u >= sq.first[s + 1]) ++s;
                 const int b = (int)(u - sq.first[s]);
-                const long long blk = p.block_table ? (long long)__ldg(p.block_table + (long long)s * p.max_blocks + b)
-                                                    : (long long)s * p.max_blocks + b;
+                const long long cs = p.row_seq ? __ldg(p.row_seq + s) : s;
+                const long long blk = p.block_table ? (long long)__ldg(p.block_table + cs * p.max_blocks + b)
+                                                    : cs * p.max_blocks + b;
                 bool ok = blk >= 0 && (blk + 1) * kPaBt <= p.cache_rows;
                 if (!ok) flag_error(p.err, DS_ERR_POSITION);
                 const char *src[2] = {static_cast<const char *>(p.k_cache), static_cast<const char *>(p.v_cache)};
@@ -509,8 +510,9 @@ __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_tc_ker
             for (long long u = u0; u < u1; ++u) {
                 while (u >= sq.first[s + 1]) ++s;
                 const int b = (int)(u - sq.first[s]);
-                const long long blk = p.block_table ? (long long)__ldg(p.block_table + (long long)s * p.max_blocks + b)
-                                                    : (long long)s * p.max_blocks + b;
+                const long long cs = p.row_seq ? __ldg(p.row_seq + s) : s;
+                const long long blk = p.block_table ? (long long)__ldg(p.block_table + cs * p.max_blocks + b)
+                                                    : cs * p.max_blocks + b;
                 const bool ok = blk >= 0 && (blk + 1) * kPaBt <= p.cache_rows;
                 if (!ok) flag_error(p.err, DS_ERR_POSITION);
                 const int row0 = ok ? (int)(blk * kPaBt) : 0;

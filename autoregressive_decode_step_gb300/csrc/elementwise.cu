@@ -171,6 +171,21 @@ cudaError_t launch_embed(const void *emb, int w_dtype, int vocab, int d, const i
                      tokens, x, err);
 }
 
+// Rows of a prompt chunk: row j is the token at position pos0 + j of
+// sequence seq.
+__global__ void chunk_rows_kernel(int *pos, int *row_seq, int pos0, int seq, int n) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j < n) {
+        pos[j] = pos0 + j;
+        row_seq[j] = seq;
+    }
+}
+
+cudaError_t launch_chunk_rows(int *pos, int *row_seq, int pos0, int seq, int n, cudaStream_t stream) {
+    return launch_ex(chunk_rows_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, false, pos, row_seq, pos0, seq,
+                     n);
+}
+
 cudaError_t launch_rope_table(float *cos_t, float *sin_t, int rows, int hd, double base, cudaStream_t stream) {
     const long long n = (long long)rows * (hd / 2);
     const int blocks = (int)((n + 255) / 256);

@@ -504,9 +504,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                     pos = __ldcg(p.pos + j);
                     if (pos >= 0 && pos < cap && pos < p.rope_rows) {
                         const int b = pos / p.block_tokens;
-                        const long long blk = p.block_table
-                                                  ? (long long)__ldcg(p.block_table + (long long)j * p.max_blocks + b)
-                                                  : (long long)j * p.max_blocks + b;
+                        const long long sj = p.row_seq ? __ldcg(p.row_seq + j) : j;
+                        const long long blk = p.block_table ? (long long)__ldcg(p.block_table + sj * p.max_blocks + b)
+                                                            : sj * p.max_blocks + b;
                         const long long rr = blk * p.block_tokens + pos % p.block_tokens;
                         if (blk >= 0 && rr < p.cache_rows) row = (int)rr;
                     }

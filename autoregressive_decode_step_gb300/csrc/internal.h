@@ -138,6 +138,7 @@ struct AttnArgs {
     int max_blocks, block_tokens;
     const int *seq_lens;  // [n_seqs] or nullptr (then n_ctx = pos[s] + 1)
     const int *pos;
+    const int *row_seq;   // [n_seqs]: the sequence whose blocks row s reads, or nullptr (s itself)
     int n_qh, n_kvh, hd;
     float scale;
     float *out;           // [n_seqs][n_qh * hd]
@@ -163,6 +164,7 @@ struct PagedAttnArgs {
     int max_blocks;
     const int *seq_lens;   // [n_seqs] or nullptr (then n_ctx = pos[s] + 1)
     const int *pos;
+    const int *row_seq;    // [n_seqs]: the sequence whose blocks row s reads, or nullptr (s itself)
     int n_seqs, n_qh, n_kvh;
     float scale;
     float *out;            // [n_seqs][n_qh * 128]
@@ -191,6 +193,9 @@ cudaError_t launch_rope_table(float *cos_t, float *sin_t, int rows, int head_dim
                               cudaStream_t stream);
 cudaError_t launch_rmsnorm_rows_bf16(const float *x, const float *w, float eps, void *h, long long lo_off,
                                      int n_rows, int d, cudaStream_t stream, bool pdl);
+// pos[j] = pos0 + j and row_seq[j] = seq for j < n (no programmatic overlap
+// with the launch before it)
+cudaError_t launch_chunk_rows(int *pos, int *row_seq, int pos0, int seq, int n, cudaStream_t stream);
 
 // ------------------------------------------------------------------ picking
 struct ArgmaxArgs {

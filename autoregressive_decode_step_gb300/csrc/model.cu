@@ -67,6 +67,7 @@ struct ds_model {
     int b_splits;
     void *h_bf, *att_bf, *f_bf;  // projection inputs as bf16 pairs: [2][max_seqs][d | nq | ff], hi then lo
     int *b_am_counters;          // argmax arrival counters, one per sequence
+    int *seq_rows;               // [2][max_seqs]: a prompt chunk's positions, then each row's sequence
     std::vector<ds::TcArgs> tc;  // per layer: q|k|v, o, gate|up, down; then the head
     // tensor maps of the K/V buffers for the paged attention, per layer, and
     // the cache they were encoded for (re-encoded when a step passes another)
@@ -95,7 +96,7 @@ using namespace ds;
 struct Layout {
     size_t x, q, att, f, logits, rope_cos, rope_sin, g_counters, g_partials, a_counters, a_partials, am_val,
         am_idx, am_counter, step_layers, step_bar, phase_times, trace, st_x, st_q, st_kv, st_f, st_ss, st_part,
-        st_att, h_bf, att_bf, f_bf, tc_counters, tc_partials, tc_ssq, b_am_counters, kv_maps, total;
+        st_att, h_bf, att_bf, f_bf, tc_counters, tc_partials, tc_ssq, b_am_counters, seq_rows, kv_maps, total;
     int b_splits, tc_tiles;
     size_t st_part_stride;
     int grid_qkv, grid_o, grid_gu, grid_d, grid_head, nb_qkv, nb_o, nb_gu, nb_d, attn_splits;
@@ -232,6 +233,7 @@ Layout make_layout(const ds_model_config *c) {
         // per 128-feature tile of the residual, each sequence's square sum (the folded RMSNorms)
         L.tc_ssq = carve(off, (size_t)tc_m_tiles(c->d, TC_ADD) * S * 4);
         L.b_am_counters = carve(off, (size_t)S * 4);
+        L.seq_rows = carve(off, (size_t)2 * S * 4);  // a prompt chunk's positions, then its rows' sequence
     }
     L.total = off;
     return L;
@@ -594,6 +596,7 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
         m->att_bf = ws + L.att_bf;
         m->f_bf = ws + L.f_bf;
         m->b_am_counters = reinterpret_cast<int *>(ws + L.b_am_counters);
+        m->seq_rows = reinterpret_cast<int *>(ws + L.seq_rows);
         const int S = cfg->max_seqs, es = 2;
         const int nq = cfg->n_qh * cfg->head_dim, nkv = cfg->n_kvh * cfg->head_dim, nqkv = nq + 2 * nkv;
         // pair = 2: two 128-feature sub-tiles per stage share one activation tile
@@ -849,13 +852,13 @@ int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t 
 // gate|up (SiLU-gate to bf16) -> down (+ residual); final RMSNorm rows ->
 // head -> per-row greedy argmax or sampler.  Every launch may begin while its
 // predecessor drains (programmatic dependent launch).
-int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n,
-                     const ds_sampling *sampling, const float *u, int32_t *next_ids, float *logits_out, unsigned flags,
-                     cudaStream_t s) {
+// Embed and every layer of a batched step over n rows: row r is token
+// tokens[r] at position pos[r], its K/V written to and read from the blocks
+// of sequence row_seq[r] (row r's own when row_seq is null).  Leaves the
+// residual of every row in m->x.
+int run_layers_batched(ds_model *m, const ds_kv_cache *kv, const int32_t *tokens, const int32_t *pos,
+                       const int32_t *row_seq, int n, cudaStream_t s) {
     const ds_model_config &c = m->cfg;
-    const bool greedy = sampling == nullptr || !(sampling->temperature > 0.0f);
-    const bool advance = (flags & DS_STEP_ADVANCE) != 0;
-    float *logits = logits_out ? logits_out : m->logits;
     const bool pdl = true;
 #define DS_TRYB(expr)                               \
     do {                                            \
@@ -871,6 +874,7 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
         TcArgs a = m->tc[4 * l + 0];
         a.n = n;
         a.pos = pos;
+        a.row_seq = row_seq;
         a.block_table = kv->block_table;
         a.max_blocks = kv->max_blocks;
         a.block_tokens = kv->block_tokens;
@@ -915,6 +919,7 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
             pa.max_blocks = kv->max_blocks;
             pa.seq_lens = nullptr;
             pa.pos = pos;
+            pa.row_seq = row_seq;
             pa.n_seqs = n;
             pa.n_qh = c.n_qh;
             pa.n_kvh = c.n_kvh;
@@ -938,6 +943,7 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
             at.block_tokens = kv->block_tokens;
             at.seq_lens = nullptr;
             at.pos = pos;
+            at.row_seq = row_seq;
             at.n_qh = c.n_qh;
             at.n_kvh = c.n_kvh;
             at.hd = c.head_dim;
@@ -961,6 +967,28 @@ int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_
         a.n = n;
         DS_TRYB(gemm(a));
     }
+#undef DS_TRYB
+    return DS_OK;
+}
+
+int run_step_batched(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n,
+                     const ds_sampling *sampling, const float *u, int32_t *next_ids, float *logits_out, unsigned flags,
+                     cudaStream_t s) {
+    const ds_model_config &c = m->cfg;
+    const bool greedy = sampling == nullptr || !(sampling->temperature > 0.0f);
+    const bool advance = (flags & DS_STEP_ADVANCE) != 0;
+    float *logits = logits_out ? logits_out : m->logits;
+    const bool pdl = true;
+#define DS_TRYB(expr)                               \
+    do {                                            \
+        if ((expr) != cudaSuccess) return DS_CUDA_ERROR; \
+    } while (0)
+    {
+        const int st = run_layers_batched(m, kv, tokens, pos, nullptr, n, s);
+        if (st != DS_OK) return st;
+    }
+    const long long h_lo = (long long)c.max_seqs * c.d;  // hi rows, then lo rows
+    auto gemm = [&](TcArgs a) { return launch_tc_gemm(a, tc_grid(a.m_tiles, a.K), s, pdl); };
     DS_TRYB(launch_rmsnorm_rows_bf16(m->x, m->final_norm, c.eps, m->h_bf, h_lo, n, c.d, s, pdl));
     TcArgs hd = m->tc[(size_t)4 * c.n_layer];
     hd.n = n;
@@ -1033,6 +1061,57 @@ extern "C" DS_API int ds_decode_steps(ds_model *m, const ds_kv_cache *kv, int32_
     if (st != DS_OK) return st;
     return run_step_fused(m, kv, tokens, pos, 1, nullptr, nullptr, next_ids, nullptr, flags & DS_STEP_ADVANCE,
                           reinterpret_cast<cudaStream_t>(stream), n_steps, ids_out);
+}
+
+extern "C" DS_API int ds_step_seq(ds_model *m, const ds_kv_cache *kv, const int32_t *tokens, int64_t tokens_len,
+                                  int32_t seq, int32_t offset, int32_t count, int32_t *next_id, float *logits_out,
+                                  ds_stream_t stream) {
+    if (!m) return DS_BAD_ARGUMENT;
+    if (count < 1) return DS_EMPTY_DIMENSION;
+    if (tokens_len != count) return DS_A_LENGTH_MISMATCH;
+    if (!tokens || !next_id) return DS_BAD_ARGUMENT;
+    if (!m->batched) return DS_BAD_ARGUMENT;  // chunks are batches of rows: the tensor-core path
+    int st = check_kv(m, kv);
+    if (st != DS_OK) return st;
+    const ds_model_config &c = m->cfg;
+    if (seq < 0 || seq >= c.max_seqs) return DS_BAD_ARGUMENT;
+    const int64_t cap = std::min<int64_t>((int64_t)kv->block_tokens * kv->max_blocks, c.max_ctx);
+    if (offset < 0 || (int64_t)offset + count > cap) return DS_CACHE_CAPACITY_EXCEEDED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int S = c.max_seqs;
+    int last = 0;  // rows of the last chunk
+    for (int c0 = 0; c0 < count; c0 += S) {
+        const int nc = std::min(S, count - c0);
+        // the chunk's positions and sequence, written after everything
+        // before it on the stream has finished reading the last chunk's
+        if (launch_chunk_rows(m->seq_rows, m->seq_rows + S, offset + c0, seq, nc, s) != cudaSuccess)
+            return DS_CUDA_ERROR;
+        st = run_layers_batched(m, kv, tokens + c0, m->seq_rows, m->seq_rows + S, nc, s);
+        if (st != DS_OK) return st;
+        last = nc;
+    }
+    // the last token only: final norm, head, greedy pick
+    float *logits = logits_out ? logits_out : m->logits;
+    const long long h_lo = (long long)S * c.d;
+    if (launch_rmsnorm_rows_bf16(m->x + (long long)(last - 1) * c.d, m->final_norm, c.eps, m->h_bf, h_lo, 1, c.d, s,
+                                 true) != cudaSuccess)
+        return DS_CUDA_ERROR;
+    TcArgs hd = m->tc[(size_t)4 * c.n_layer];
+    hd.n = 1;
+    hd.y = logits;
+    if (launch_tc_gemm(hd, tc_grid(hd.m_tiles, hd.K), s, true) != cudaSuccess) return DS_CUDA_ERROR;
+    ArgmaxArgs am = {};
+    am.logits = logits;
+    am.n_rows = 1;
+    am.n = c.vocab;
+    am.ids = next_id;
+    am.part_val = m->am_val;
+    am.part_idx = m->am_idx;
+    am.counters = m->b_am_counters;
+    am.err = m->err;
+    am.blocks_per_row = argmax_blocks_per_row(c.vocab);
+    if (launch_argmax(am, s, true) != cudaSuccess) return DS_CUDA_ERROR;
+    return DS_OK;
 }
 
 extern "C" DS_API int ds_model_phase_times(ds_model *m, uint64_t *ns_out, int cap, int *n_out, ds_stream_t stream) {

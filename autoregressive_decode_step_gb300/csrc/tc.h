@@ -45,6 +45,9 @@ struct TcArgs {
     int nq_cols, nkv_cols, head_dim, rope_layout;
     void *k_cache, *v_cache;
     int kv_dtype;
+    // the sequence whose blocks row s addresses: row_seq[s], or s when null
+    // (a prompt chunk of one sequence gives every row the same sequence)
+    const int *row_seq;
     // TC_ADD with nw set: the next RMSNorm folded in.  Besides y += acc it
     // writes x * nw (x the updated residual) as bf16 hi/lo to hb[s * ldy + m]
     // (lo part hb_lo elements further) and each 128-feature tile's square sums

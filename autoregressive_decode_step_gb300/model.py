@@ -124,6 +124,19 @@ class DecodeModel:
                                           n_steps, abi.ptr(ids_out), abi.ptr(self.next_ids), flags,
                                           abi.stream_handle(stream)), "ds_decode_steps")
 
+    def step_seq(self, tokens, seq=0, offset=0, stream=None):
+        """stepSeq: the tokens of sequence `seq` at positions offset,
+        offset + 1, ... run as chunks of up to max_seqs rows on the batched
+        path (ds_step_seq).  The greedy pick after the last token goes to
+        next_ids[seq] and that token's logits to logits[seq]."""
+        t = torch.as_tensor(tokens, dtype=torch.int32).to(self.device)
+        # addresses, not views: the library itself refuses a sequence outside the model
+        pick = ctypes.c_void_p(self.next_ids.data_ptr() + 4 * seq)
+        logits = ctypes.c_void_p(self.logits.data_ptr() + 4 * seq * self.cfg["vocab"])
+        abi.check(abi.lib.ds_step_seq(self._h, ctypes.byref(self._kv), abi.ptr(t), t.numel(), seq, offset,
+                                      t.numel(), pick, logits, abi.stream_handle(stream)), "ds_step_seq")
+        return t
+
     def graph(self, n_seqs=1, sampling=None, advance=True, write_logits=False, stream=None):
         """A captured step (created once per argument set); returns a
         callable that replays it on `stream`."""

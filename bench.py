@@ -27,6 +27,7 @@ sys.path.insert(0, ROOT)
 METRIC = "batch-1 decode tokens/s and % of GB300 HBM roofline; per-op us vs CPU oracle"
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -41,6 +42,8 @@ def parse():
     p.add_argument("--batched-only", action="store_true",
                    help="time only the batched (64-sequence) decode (a profiling case; the line's batch-1 keys are "
                         "then absent)")
+    p.add_argument("--prompt-only", action="store_true",
+                   help="time only the chunked prompt (stepSeq) leg (a profiling case)")
     p.add_argument("--batched-steps", type=int, default=None,
                    help="timed steps of the batched decode (default: the workload's 128)")
     p.add_argument("--chunk", type=int, default=32,
@@ -382,6 +385,87 @@ def run_batched(cfg, W, dev, rank, clocks_cls, bus, warmup=3, steps=None):
     return out
 
 
+def run_step_seq(cfg, W, dev, rank, clocks_cls, bus, prompt_len=1024, rows=256, warmup=1, reps=3):
+    """A prompt of one sequence through ds_step_seq on the same 8B-shaped
+    weights: prompt_len random tokens from position 0, chunks of `rows` rows
+    on the batched path (q|k|v, o, gate|up, down as GEMMs over the chunk's
+    rows on the tensor cores; each row attends its own causal prefix), then
+    the last token's head and greedy pick.  The K/V of the prompt goes to
+    one sequence's blocks of a paged pool."""
+    import torch
+
+    from autoregressive_decode_step_gb300 import configs as C
+    from autoregressive_decode_step_gb300 import synth
+    from autoregressive_decode_step_gb300.model import DecodeModel
+
+    bt = 16
+    mb = (prompt_len + bt - 1) // bt
+    table = torch.zeros(rows, mb, dtype=torch.int32)
+    table[0] = torch.randperm(mb, generator=torch.Generator().manual_seed(rank + 5)).to(torch.int32)
+    model = DecodeModel(cfg, W, capacity=mb * bt, device=dev, block_tokens=bt, block_table=table.to(dev),
+                        n_blocks=mb, max_seqs=rows)
+    prompt = synth.prompt_ids(cfg, prompt_len, seed=rank + 6)
+    toks = torch.as_tensor(prompt, dtype=torch.int32).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            model.step_seq(toks, seq=0, offset=0, stream=stream)
+    stream.synchronize()
+    clocks = clocks_cls(bus)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(reps):
+            model.step_seq(toks, seq=0, offset=0, stream=stream)
+            ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    t_wall1 = time.perf_counter()
+    ms = ev[0].elapsed_time(ev[-1]) / reps
+    time.sleep(0.2)
+    clocks.stop()
+    err = model.error_word()
+    if err:
+        raise RuntimeError("device error word %d during the prompt timed region" % err)
+    n_chunks = (prompt_len + rows - 1) // rows
+    nq = cfg["n_qh"] * cfg["head_dim"]
+    # the method's arithmetic: 2 flops per weight per token for the
+    # projections, the head once, and q.K plus p.V over each causal prefix
+    flops = (2.0 * cfg["n_layer"] * C.layer_params(cfg) * prompt_len + 2.0 * cfg["vocab"] * cfg["d"]
+             + 4.0 * cfg["n_layer"] * nq * prompt_len * (prompt_len + 1) / 2)
+    wbytes = C.weight_bytes_per_step(cfg)
+    alg_bytes = n_chunks * (wbytes - cfg["vocab"] * cfg["d"] * 2) + cfg["vocab"] * cfg["d"] * 2 \
+        + prompt_len * C.kv_bytes_per_token(cfg)
+    hbm, kind = peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tf_peak, tf_kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        tf_peak, tf_kind = FALLBACK_BF16_TFLOPS, "fallback"
+    sec = ms / 1e3
+    out = {"workload": "llama3-8b-shape, one sequence, %d-token random prompt from position 0 in chunks of %d rows "
+                       "(stepSeq on the batched path), last token's head + greedy pick, paged K/V pool of %d-position "
+                       "blocks" % (prompt_len, rows, bt),
+           "value": prompt_len / sec, "unit": "prompt tokens/s", "ms_per_prompt": ms, "reps": reps,
+           "warmup": warmup, "chunks": n_chunks,
+           "tensor_roofline": {"achieved": flops / sec / 1e12, "peak": tf_peak, "unit": "TFLOP/s",
+                               "frac": flops / sec / 1e12 / tf_peak, "peak_source": tf_kind,
+                               "algorithmic_flops": flops,
+                               "note": "the projections multiply each fp32 activation as a bf16 pair hi + lo, so "
+                                       "the tensor pipe executes twice these flops"},
+           "hbm_roofline": {"achieved": alg_bytes / sec / 1e9, "peak": hbm, "unit": "GB/s",
+                            "frac": alg_bytes / sec / 1e9 / hbm, "peak_source": kind,
+                            "algorithmic_bytes": alg_bytes},
+           "gpu_launches_per_prompt": n_chunks * (5 * cfg["n_layer"] + 3) + 3,
+           "clocks": clocks.summary(t_wall0, t_wall1)}
+    del model
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -399,13 +483,16 @@ def run_ours(args, rank, world, local):
     K, Wm = args.steps, args.warmup
     cap = args.ctx + max(Wm, K) + 8
     W = synth.model_weights(cfg, seed=0, device=dev)
-    if args.batched_only:
+    if args.batched_only or args.prompt_only:
         props = torch.cuda.get_device_properties(dev)
         bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), getattr(props, "pci_bus_id", 0),
                                     getattr(props, "pci_device_id", 0))
-        line = {"metric": METRIC, "n_gpus": world, "data": "synthetic",
-                "batched": run_batched(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus,
-                                       steps=args.batched_steps)}
+        line = {"metric": METRIC, "n_gpus": world, "data": "synthetic"}
+        if args.batched_only:
+            line["batched"] = run_batched(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus,
+                                          steps=args.batched_steps)
+        if args.prompt_only:
+            line["prompt_chunks"] = run_step_seq(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return 0
@@ -548,6 +635,7 @@ def run_ours(args, rank, world, local):
     if args.layers is None and not args.no_batched:
         line["batched"] = run_batched(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus,
                                       steps=args.batched_steps)
+        line["prompt_chunks"] = run_step_seq(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus)
     del W
     torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

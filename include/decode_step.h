@@ -424,6 +424,29 @@ DS_API int ds_decode_step(ds_model *model, const ds_kv_cache *kv, int32_t *token
 DS_API int ds_decode_steps(ds_model *model, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, int n_steps,
                            int32_t *ids_out, int32_t *next_ids, unsigned flags, ds_stream_t stream);
 
+/* stepSeq(sequence, tokens, offset, count): `count` prompt tokens of one
+ * sequence at positions offset .. offset + count - 1, run as chunks of at
+ * most max_seqs rows, each chunk one batch of rows through the batched path
+ * ("Inside the engine", section 1: prefill runs a chunk of prompt tokens as a
+ * batch of rows through the batched projections; decode is the one-token
+ * chunk of the same step).  Row j of a chunk is the token at position
+ * offset + c0 + j: its K and V are written to sequence `seq`'s blocks and it
+ * attends positions 0 .. offset + c0 + j of that sequence (earlier chunks'
+ * rows and its own chunk's earlier rows included), so the cache ends as
+ * `count` decode steps would leave it.  Only the last token goes through the
+ * final norm, the head and the greedy argmax.
+ *   tokens: device int32 [count] (tokens_len must equal count, else 562);
+ *   seq in [0, max_seqs) (577; with a block table, its row seq, else the
+ *   contiguous slot seq); next_id: device int32 [1], the greedy pick after
+ *   the last token; logits_out: optional device fp32 [vocab], that token's
+ *   logits (the model's own buffer is used when NULL).
+ * Models with max_seqs > 1 only (577 otherwise); count >= 1 (561);
+ * offset >= 0 and offset + count within the cache and max_ctx (571).
+ * Uses the model's workspace: calls on one model are serialised on a stream. */
+DS_API int ds_step_seq(ds_model *model, const ds_kv_cache *kv, const int32_t *tokens, int64_t tokens_len,
+                       int32_t seq, int32_t offset, int32_t count, int32_t *next_id, float *logits_out,
+                       ds_stream_t stream);
+
 /* Device timestamps (ns, globaltimer) of the last step run with
  * DS_STEP_PHASE_TIMES: [0] start, then the start of every phase in order
  * (per layer: q|k|v, attention, o, gate|up, down), then the head, then the

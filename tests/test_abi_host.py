@@ -170,3 +170,13 @@ def test_batched_projection_refusals(abi):
         abi.DS_GEMV_X_LENGTH_MISMATCH
     assert L.ds_gemm_workspace_bytes(0, 64, 64) == 0
     assert L.ds_gemm_workspace_bytes(257, 64, 64) == 0
+
+
+def test_step_seq_refuses_before_any_launch(abi):
+    """stepSeq's host checks, in order: no model, then an empty prompt and a
+    token count that disagrees with the buffer's length."""
+    L = abi.lib
+    assert L.ds_step_seq(None, None, None, 4, 0, 0, 4, None, None, None) == abi.DS_BAD_ARGUMENT
+    fake = ctypes.c_void_p(16)  # never dereferenced: the counts are refused first
+    assert L.ds_step_seq(fake, None, None, 0, 0, 0, 0, None, None, None) == abi.DS_EMPTY_DIMENSION
+    assert L.ds_step_seq(fake, None, fake, 3, 0, 0, 4, fake, None, None) == abi.DS_A_LENGTH_MISMATCH
