@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int stages = p.stages;
     const int MS = p.msub;
+    const bool one_acc = p.acc_bufs == 1;  // a single accumulator (MS x n_pad columns)
     const int a_bytes = MS * kTcABytes;        // the tile's weight sub-tiles
     const int b_bytes = p.n_pad * kTcBK * 2;  // one activation tile (the hi part when split)
     const int stage_bytes = a_bytes + b_bytes * (p.split ? 2 : 1);
@@ -447,8 +448,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             TcSeg sg;
             bool ok = true;
             while (ok && tc_next_seg(u, u1, KB, sg)) {
-                const int buf = seg_i & 1;
-                if (seg_i >= 2 && !tc_wait(&acc_empty[buf], ((seg_i >> 1) - 1) & 1, abort_flag, p.err)) {
+                const int buf = one_acc ? 0 : (seg_i & 1);
+                const int use = one_acc ? seg_i : (seg_i >> 1);  // earlier uses of this accumulator
+                if (use >= 1 && !tc_wait(&acc_empty[buf], (use - 1) & 1, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
@@ -537,10 +539,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             named_sync(1, kTcEpiThreads);
         }
         while (tc_next_seg(u, u1, KB, sg)) {
-            const int buf = seg_i & 1;
+            const int buf = one_acc ? 0 : (seg_i & 1);
+            const int use = one_acc ? seg_i : (seg_i >> 1);
             // the four warps agree on whether the accumulator arrived, so none
             // of them can be left alone at a named barrier
-            bool ok = __all_sync(0xffffffffu, tc_wait(&acc_full[buf], (seg_i >> 1) & 1, abort_flag, p.err));
+            bool ok = __all_sync(0xffffffffu, tc_wait(&acc_full[buf], use & 1, abort_flag, p.err));
             if (lane == 0) s_ok[(seg_i & 1) * 4 + q] = ok ? 1 : 0;
             named_sync(1, kTcEpiThreads);
             ok = s_ok[(seg_i & 1) * 4 + 0] && s_ok[(seg_i & 1) * 4 + 1] && s_ok[(seg_i & 1) * 4 + 2] &&
@@ -683,7 +686,9 @@ static bool g_tc_ready = false;
 
 cudaError_t launch_tc_gemm(const TcArgs &a, int grid, cudaStream_t stream, bool pdl) {
     if (a.n_pad < 32 || a.n_pad > 256 || a.n_pad % 32 || a.stages < 2 || a.stages > kTcMaxStages) return cudaErrorInvalidValue;
-    if ((a.msub != 1 && a.msub != 2) || a.tmem_cols < 2 * a.msub * a.n_pad || a.tmem_cols > 512) return cudaErrorInvalidValue;
+    if ((a.msub != 1 && a.msub != 2) || a.tmem_cols < (a.acc_bufs == 1 ? 1 : 2) * a.msub * a.n_pad ||
+        a.tmem_cols > 512)
+        return cudaErrorInvalidValue;
     if (!g_tc_ready) {
         cudaError_t e = prepare_tc_kernels();
         if (e != cudaSuccess) return e;
@@ -754,6 +759,7 @@ int tc_run(const void *A, const void *X, int64_t n, int64_t M, int64_t K, int a_
     a.n_pad = tc_n_pad((int)n);
     a.epi = TC_STORE;
     a.msub = 1;
+    a.acc_bufs = 2;
     a.m_tiles = tc_m_tiles(a.M, a.epi);
     a.stages = tc_stages(a.n_pad, 0, 1);
     a.tmem_cols = 32;

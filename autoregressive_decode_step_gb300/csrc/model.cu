@@ -612,11 +612,16 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
             a.split = 1;  // fp32 activations as bf16 hi + lo rows, S rows apart
             a.b_lo_row = S;
             a.epi = epi;
-            a.msub = (pair == 2 && a.n_pad <= 128) ? 2 : 1;
+            a.msub = pair == 2 ? 2 : 1;
+            // two accumulators (one tile's epilogue overlapping the next
+            // tile's MMAs) where TMEM holds them; above 128 vectors a paired
+            // tile keeps one, which still halves the activation tiles
+            // streamed per weight byte
+            a.acc_bufs = 2 * a.msub * a.n_pad <= 512 ? 2 : 1;
             a.m_tiles = (tc_m_tiles(M, epi) + a.msub - 1) / a.msub;
             a.stages = tc_stages(a.n_pad, 1, a.msub);
             a.tmem_cols = 32;
-            while (a.tmem_cols < 2 * a.msub * a.n_pad) a.tmem_cols *= 2;
+            while (a.tmem_cols < a.acc_bufs * a.msub * a.n_pad) a.tmem_cols *= 2;
             a.partials = reinterpret_cast<float *>(ws + L.tc_partials);
             a.counters = reinterpret_cast<int *>(ws + L.tc_counters);
             a.err = m->err;

@@ -31,6 +31,7 @@ struct TcArgs {
     int b_lo_row;
     int epi, m_tiles, stages, tmem_cols;
     int msub;         // 128-feature sub-tiles per tile (1 or 2): a tile's sub-tiles share one activation tile
+    int acc_bufs;     // TMEM accumulators (1: a tile's MMAs wait for the previous tile's epilogue; else 2)
     float *y;             // TC_STORE / TC_ADD: y[s * ldy + m]; TC_QKV: q [n][ldy]
     __nv_bfloat16 *yb;    // TC_SILU: silu(gate) * up as bf16, yb[s * ldy + g] (hi part when yb_lo > 0)
     long long yb_lo;      // TC_SILU: elements from the hi part to the lo part (0: hi only)
