@@ -41,7 +41,9 @@ def lib():
         L.or_rmsnorm.argtypes = [P, P, ctypes.c_int, I64, D, P]
         L.or_add_rmsnorm.argtypes = [P, P, P, ctypes.c_int, I64, D, P]
         L.or_silu_mul.argtypes = [P, P, P, I64]
-        L.or_rope.argtypes = [P, I64, I64, I64, D, ctypes.c_int]
+        L.or_rope.argtypes = [P, I64, I64, I64, D, ctypes.c_int, P]
+        L.or_rope_freq.argtypes = [I64, I64, D, P]
+        L.or_rope_freq.restype = D
         L.or_kv_cache_append.argtypes = [P, ctypes.c_int, I64, I64, P, I64, I64]
         L.or_gqa_attention.argtypes = [P, P, P, ctypes.c_int, P, I64, I64, I64, I64, I64, I64, I64, D, P]
         L.or_argmax.argtypes = [P, I64, P]
@@ -147,10 +149,26 @@ def silu_mul(gate, up):
     return out
 
 
-def rope(vec, n_heads, head_dim, pos, base, layout):
+def rope_scaling_vector(scaling):
+    """{factor, low_freq_factor, high_freq_factor, original_max_position} as
+    the oracle's four doubles; None: no scaling (factor 0)."""
+    if not scaling:
+        return np.zeros(4, dtype=np.float64)
+    return np.array([scaling["factor"], scaling["low_freq_factor"], scaling["high_freq_factor"],
+                     scaling["original_max_position"]], dtype=np.float64)
+
+
+def rope_freq(p, head_dim, base, scaling=None):
+    """Rotation frequency of pair p, optionally with long-context scaling."""
+    sc = rope_scaling_vector(scaling)
+    return lib().or_rope_freq(p, head_dim, base, _ptr(sc))
+
+
+def rope(vec, n_heads, head_dim, pos, base, layout, scaling=None):
     v = _c(vec, np.float64).copy()
     assert v.size == n_heads * head_dim
-    lib().or_rope(_ptr(v), n_heads, head_dim, pos, base, layout)
+    sc = rope_scaling_vector(scaling)
+    lib().or_rope(_ptr(v), n_heads, head_dim, pos, base, layout, _ptr(sc))
     return v
 
 
@@ -200,7 +218,8 @@ class Model:
     own host KV caches, and one ``step`` per decode step.
 
     ``cfg`` keys: vocab, d, n_layer, n_qh, n_kvh, head_dim, ff, rope_base,
-    rope_layout, tied, w_dtype, kv_dtype, eps; cache geometry
+    rope_layout, tied, w_dtype, kv_dtype, eps, optional rope_scaling (see
+    ``rope_scaling_vector``); cache geometry
     block_tokens / max_blocks (a sequence's capacity is their product) and
     n_seqs; optional block_table (int32 [n_seqs, max_blocks]) for a paged pool
     with ``n_blocks`` physical blocks.
@@ -237,7 +256,8 @@ class Model:
         self._iv = np.array([c["vocab"], c["d"], c["n_layer"], c["n_qh"], c["n_kvh"],
                              c["head_dim"], c["ff"], c["rope_layout"], c["tied"], wdt,
                              c["kv_dtype"], c["block_tokens"], c["max_blocks"]], dtype=np.int64)
-        self._dv = np.array([c["rope_base"], c["eps"]], dtype=np.float64)
+        self._dv = np.concatenate([np.array([c["rope_base"], c["eps"]], dtype=np.float64),
+                                   rope_scaling_vector(c.get("rope_scaling"))])
         bt = c.get("block_table")
         self._bt = None if bt is None else _c(bt, np.int32)
         n_blocks = c.get("n_blocks", c["n_seqs"] * c["max_blocks"])

@@ -191,18 +191,39 @@ void or_silu_mul(const double *gate, const double *up, double *out, int64_t n) {
 #define OR_ROPE_HALF_SPLIT 0
 #define OR_ROPE_INTERLEAVED 1
 
+/* Rotation frequency of pair p (0 <= p < hd/2): base^(-2p/hd).  With
+ * long-context scaling (sc != NULL and sc[0] != 0; sc = {factor, low_factor,
+ * high_factor, orig_max_pos}) the frequency is remapped by its wavelength
+ * w = 2 pi / f, as Llama 3.1 checkpoints define it (not on the pages): a pair
+ * that turns more than high_factor times within orig_max_pos positions keeps
+ * f, one that turns fewer than low_factor times turns factor times slower,
+ * and in between f / factor and f are blended with the weight
+ * s = (orig_max_pos / w - low_factor) / (high_factor - low_factor) on f. */
+double or_rope_freq(int64_t p, int64_t hd, double base, const double *sc) {
+    const double f = pow(base, -(double)(2 * p) / (double)hd);
+    if (!sc || sc[0] == 0.0) return f;
+    const double factor = sc[0], lo = sc[1], hi = sc[2], orig = sc[3];
+    const double two_pi = 6.283185307179586476925286766559;
+    const double w = two_pi / f;
+    if (w < orig / hi) return f;
+    if (w > orig / lo) return f / factor;
+    const double s = (orig / w - lo) / (hi - lo);
+    return (1.0 - s) * (f / factor) + s * f;
+}
+
 /* Rotate every head of `vec` (n_heads * hd values) to position `pos`.
- * Pair p (0 <= p < hd/2) turns by theta_p = pos * base^(-2p/hd):
+ * Pair p turns by theta_p = pos * f_p (f_p from or_rope_freq; unscaled,
+ * f_p = base^(-2p/hd)):
  *   a' = a cos(theta) - b sin(theta),  b' = a sin(theta) + b cos(theta).
  * Interleaved layout pairs (2p, 2p+1) ("The forward pass end to end", "The
  * code", rope); half-split layout pairs (p, p + hd/2), the GPT-NeoX split-half
  * convention ("LLM inference kernels", "Two gaps, not three").  Angles are
  * formed in fp64 ("decode-ops", "API — Method"). */
-void or_rope(double *vec, int64_t n_heads, int64_t hd, int64_t pos, double base, int layout) {
+void or_rope(double *vec, int64_t n_heads, int64_t hd, int64_t pos, double base, int layout, const double *sc) {
     for (int64_t h = 0; h < n_heads; ++h) {
         double *v = vec + h * hd;
         for (int64_t p = 0; p < hd / 2; ++p) {
-            double theta = (double)pos * pow(base, -(double)(2 * p) / (double)hd);
+            double theta = (double)pos * or_rope_freq(p, hd, base, sc);
             double c = cos(theta), s = sin(theta);
             int64_t ia = layout == OR_ROPE_INTERLEAVED ? 2 * p : p;
             int64_t ib = layout == OR_ROPE_INTERLEAVED ? 2 * p + 1 : p + hd / 2;
@@ -403,6 +424,7 @@ typedef struct {
     int64_t kv_dtype;
     int64_t block_tokens, max_blocks; /* cache geometry, see cache_row */
     double rope_base, eps;
+    double rope_scaling[4]; /* factor (0: none), low_factor, high_factor, orig_max_pos */
 } or_model;
 
 static void unpack(or_model *m, const int64_t *iv, const double *dv) {
@@ -421,6 +443,7 @@ static void unpack(or_model *m, const int64_t *iv, const double *dv) {
     m->max_blocks = iv[12];
     m->rope_base = dv[0];
     m->eps = dv[1];
+    for (int i = 0; i < 4; ++i) m->rope_scaling[i] = dv[2 + i];
 }
 
 /* Weight pointers, in this order:
@@ -469,8 +492,8 @@ int or_decode_step(const int64_t *iv, const double *dv, const void *const *weigh
         or_gemv_transposed(L[1], (int)m.w_dtype, h, d, nqkv, qkv);
         double *q = qkv, *k = qkv + nq, *v = qkv + nq + nkv;
         /* rotate q and k (never v) to this position */
-        or_rope(q, m.n_qh, hd, pos, m.rope_base, (int)m.rope_layout);
-        or_rope(k, m.n_kvh, hd, pos, m.rope_base, (int)m.rope_layout);
+        or_rope(q, m.n_qh, hd, pos, m.rope_base, (int)m.rope_layout, m.rope_scaling);
+        or_rope(k, m.n_kvh, hd, pos, m.rope_base, (int)m.rope_layout, m.rope_scaling);
         /* append this position's K and V before attending */
         int64_t row = cache_row(seq, pos, block_table, m.max_blocks, m.block_tokens);
         for (int64_t i = 0; i < nkv; ++i) {

@@ -205,6 +205,79 @@ def test_rope_half_split_is_interleaved_under_permutation():
     np.testing.assert_allclose(a[perm], b, atol=1e-15)
 
 
+# Long-context RoPE scaling as Llama 3.1 checkpoints define it (not on the
+# pages): pinned by reductions, band limits, continuity and invariants.
+LLAMA31_SCALING = {"factor": 8.0, "low_freq_factor": 1.0, "high_freq_factor": 4.0,
+                   "original_max_position": 8192.0}
+
+
+def test_rope_scaling_with_factor_one_is_the_unscaled_rope():
+    sc = dict(LLAMA31_SCALING, factor=1.0)
+    for p in range(64):
+        f = 500000.0 ** (-2.0 * p / 128)
+        assert O.rope_freq(p, 128, 500000.0, sc) == pytest.approx(f, rel=1e-15)
+    v = np.random.default_rng(12).standard_normal(128)
+    np.testing.assert_allclose(O.rope(v, 1, 128, 777, 500000.0, O.ROPE_HALF_SPLIT, sc),
+                               O.rope(v, 1, 128, 777, 500000.0, O.ROPE_HALF_SPLIT), atol=1e-12)
+
+
+def test_rope_scaling_bands_on_the_llama31_parameters():
+    """Wavelength 2 pi / f below 8192 / 4 keeps f; above 8192 / 1 divides it
+    by 8; in between it lies strictly inside, and the ratio to the unscaled
+    frequency never rises as the pairs slow down."""
+    hd, base = 128, 500000.0
+    ratios = []
+    n_keep = n_slow = n_mid = 0
+    for p in range(hd // 2):
+        f = base ** (-2.0 * p / hd)
+        g = O.rope_freq(p, hd, base, LLAMA31_SCALING)
+        w = 2 * math.pi / f
+        if w < 2048.0:
+            assert g == f
+            n_keep += 1
+        elif w > 8192.0:
+            assert g == pytest.approx(f / 8.0, rel=1e-15)
+            n_slow += 1
+        else:
+            assert f / 8.0 < g < f
+            n_mid += 1
+        ratios.append(g / f)
+    assert all(a >= b for a, b in zip(ratios, ratios[1:]))
+    assert n_keep > 0 and n_slow > 0 and n_mid > 0
+    assert O.rope_freq(0, hd, base, LLAMA31_SCALING) == 1.0  # the fastest pair turns one radian per position
+
+
+@pytest.mark.parametrize("edge", ["high", "low"])
+def test_rope_scaling_is_continuous_at_both_band_edges(edge):
+    """Move original_max_position across the value that puts pair p's
+    wavelength exactly on a band edge: the frequency must not jump (it meets
+    f at the high-frequency edge and f / factor at the low-frequency edge)."""
+    hd, base, p = 128, 500000.0, 40
+    f = base ** (-2.0 * p / hd)
+    w = 2 * math.pi / f
+    sc = dict(LLAMA31_SCALING)
+    at = w * (sc["high_freq_factor"] if edge == "high" else sc["low_freq_factor"])
+    want = f if edge == "high" else f / sc["factor"]
+    for eps in (-1e-9, 1e-9):
+        sc["original_max_position"] = at * (1 + eps)
+        assert O.rope_freq(p, hd, base, sc) == pytest.approx(want, rel=1e-7)
+
+
+def test_scaled_rope_is_relative_and_identity_at_zero():
+    rng = np.random.default_rng(13)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    sc = LLAMA31_SCALING
+    assert np.array_equal(O.rope(q, 1, 128, 0, 500000.0, O.ROPE_HALF_SPLIT, sc), q)
+    d1 = O.rope(q, 1, 128, 9000, 500000.0, O.ROPE_HALF_SPLIT, sc) @ O.rope(k, 1, 128, 8000, 500000.0,
+                                                                           O.ROPE_HALF_SPLIT, sc)
+    d2 = O.rope(q, 1, 128, 1000, 500000.0, O.ROPE_HALF_SPLIT, sc) @ O.rope(k, 1, 128, 0, 500000.0,
+                                                                           O.ROPE_HALF_SPLIT, sc)
+    assert d1 == pytest.approx(d2, rel=1e-9)
+    # and the scaling matters at long range: the slow pairs turn 8 times less
+    assert not np.allclose(O.rope(q, 1, 128, 9000, 500000.0, O.ROPE_HALF_SPLIT, sc),
+                           O.rope(q, 1, 128, 9000, 500000.0, O.ROPE_HALF_SPLIT), atol=1e-3)
+
+
 # ----------------------------------------------------------------- KV cache
 def test_kv_cache_append_worked_example():
     g = gold("p1_kv_cache_append.json")
