@@ -59,7 +59,9 @@ F64 = ctypes.c_double
 class ModelConfig(ctypes.Structure):
     _fields_ = [("vocab", I32), ("d", I32), ("n_layer", I32), ("n_qh", I32), ("n_kvh", I32),
                 ("head_dim", I32), ("ff", I32), ("rope_layout", I32), ("rope_base", F64), ("eps", F32),
-                ("tied", I32), ("w_dtype", I32), ("kv_dtype", I32), ("max_seqs", I32), ("max_ctx", I32)]
+                ("tied", I32), ("w_dtype", I32), ("kv_dtype", I32), ("max_seqs", I32), ("max_ctx", I32),
+                ("rope_factor", F64), ("rope_low_freq_factor", F64), ("rope_high_freq_factor", F64),
+                ("rope_orig_max_pos", F64)]
 
 
 class ModelWeights(ctypes.Structure):

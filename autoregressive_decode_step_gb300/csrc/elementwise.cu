@@ -75,12 +75,25 @@ __global__ void rope_kernel(float *q, int n_qh, float *k, int n_kh, long long po
 // cos/sin of pos * base^(-2p/hd) for every position row and pair, fp64
 // angles rounded to fp32 once (the shared RoPE table of "LLM inference
 // kernels", "The hot loop doesn't call kv_cache_append_flat").
-__global__ void rope_table_kernel(float *cos_t, float *sin_t, int rows, int hd, double base) {
+__global__ void rope_table_kernel(float *cos_t, float *sin_t, int rows, int hd, double base, RopeScaling sc) {
     const int half = hd >> 1;
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long long)rows * half) return;
     const int pos = (int)(i / half), pr = (int)(i % half);
-    const double theta = (double)pos * pow(base, -(double)(2 * pr) / (double)hd);
+    double f = pow(base, -(double)(2 * pr) / (double)hd);
+    if (sc.factor != 0.0) {
+        // long-context scaling by the pair's wavelength (Llama 3.1's remap):
+        // fast pairs keep f, slow pairs turn factor times slower, the band
+        // between blends the two linearly in orig_max_pos / wavelength
+        const double w = 6.283185307179586476925286766559 / f;
+        if (w > sc.orig_max_pos / sc.low_freq_factor) {
+            f = f / sc.factor;
+        } else if (!(w < sc.orig_max_pos / sc.high_freq_factor)) {
+            const double s = (sc.orig_max_pos / w - sc.low_freq_factor) / (sc.high_freq_factor - sc.low_freq_factor);
+            f = (1.0 - s) * (f / sc.factor) + s * f;
+        }
+    }
+    const double theta = (double)pos * f;
     cos_t[i] = (float)cos(theta);
     sin_t[i] = (float)sin(theta);
 }
@@ -186,10 +199,12 @@ cudaError_t launch_chunk_rows(int *pos, int *row_seq, int pos0, int seq, int n, 
                      n);
 }
 
-cudaError_t launch_rope_table(float *cos_t, float *sin_t, int rows, int hd, double base, cudaStream_t stream) {
+cudaError_t launch_rope_table(float *cos_t, float *sin_t, int rows, int hd, double base, RopeScaling sc,
+                              cudaStream_t stream) {
     const long long n = (long long)rows * (hd / 2);
     const int blocks = (int)((n + 255) / 256);
-    return launch_ex(rope_table_kernel, dim3(blocks), dim3(256), 0, stream, false, cos_t, sin_t, rows, hd, base);
+    return launch_ex(rope_table_kernel, dim3(blocks), dim3(256), 0, stream, false, cos_t, sin_t, rows, hd, base,
+                     sc);
 }
 
 static int blocks_for(long long n, int threads) {

@@ -189,7 +189,11 @@ cudaError_t launch_attention(const AttnArgs &a, int n_seqs, cudaStream_t stream,
 // ------------------------------------------------------------------ small ops
 cudaError_t launch_embed(const void *emb, int w_dtype, int vocab, int d, const int *tokens,
                          float *x, int *err, int n_seqs, cudaStream_t stream, bool pdl);
-cudaError_t launch_rope_table(float *cos_t, float *sin_t, int rows, int head_dim, double base,
+// Long-context frequency scaling of the RoPE table (factor 0: none).
+struct RopeScaling {
+    double factor, low_freq_factor, high_freq_factor, orig_max_pos;
+};
+cudaError_t launch_rope_table(float *cos_t, float *sin_t, int rows, int head_dim, double base, RopeScaling sc,
                               cudaStream_t stream);
 cudaError_t launch_rmsnorm_rows_bf16(const float *x, const float *w, float eps, void *h, long long lo_off,
                                      int n_rows, int d, cudaStream_t stream, bool pdl);

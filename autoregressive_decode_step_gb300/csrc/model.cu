@@ -126,6 +126,11 @@ int validate(const ds_model_config *c) {
     if (gemv_t_band_cols(es) % c->head_dim) return DS_BAD_ARGUMENT;
     if (!gemv_n_streamable(nullptr, c->vocab, c->d, es)) return DS_BAD_ARGUMENT;
     if (!(c->eps >= 0.0f) || !(c->rope_base > 0.0)) return DS_BAD_ARGUMENT;
+    if (c->rope_factor != 0.0 &&
+        !(c->rope_factor >= 1.0 && c->rope_low_freq_factor > 0.0 &&
+          c->rope_high_freq_factor > c->rope_low_freq_factor && c->rope_orig_max_pos > 0.0 &&
+          c->rope_factor < 1e300 && c->rope_high_freq_factor < 1e300 && c->rope_orig_max_pos < 1e300))
+        return DS_BAD_ARGUMENT;
     if (c->max_seqs > 256) return DS_DIMENSION_TOO_LARGE;
     if (c->max_seqs > 1) {
         // the batched step runs its projections on bf16 tensor cores, with
@@ -693,7 +698,10 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
         step_layer_fill(layer_img.data() + (size_t)l * step_layer_bytes(), &m->maps[5 * l], w->n1[l], w->n2[l]);
     if (prepare_kernels() != cudaSuccess || cudaMemset(workspace, 0, L.total) != cudaSuccess ||
         cudaMemcpy(m->step_layers, layer_img.data(), layer_img.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
-        launch_rope_table(m->rope_cos, m->rope_sin, cfg->max_ctx, cfg->head_dim, cfg->rope_base, nullptr) !=
+        launch_rope_table(m->rope_cos, m->rope_sin, cfg->max_ctx, cfg->head_dim, cfg->rope_base,
+                          RopeScaling{cfg->rope_factor, cfg->rope_low_freq_factor, cfg->rope_high_freq_factor,
+                                      cfg->rope_orig_max_pos},
+                          nullptr) !=
             cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         delete m;

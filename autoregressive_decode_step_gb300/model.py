@@ -42,6 +42,10 @@ class DecodeModel:
         mc.rope_layout, mc.rope_base, mc.eps = c["rope_layout"], c["rope_base"], c.get("eps", 1e-5)
         mc.tied, mc.w_dtype, mc.kv_dtype = c["tied"], c["w_dtype"], c["kv_dtype"]
         mc.max_seqs, mc.max_ctx = max_seqs, self.capacity
+        sc = c.get("rope_scaling")
+        if sc:
+            mc.rope_factor, mc.rope_low_freq_factor = sc["factor"], sc["low_freq_factor"]
+            mc.rope_high_freq_factor, mc.rope_orig_max_pos = sc["high_freq_factor"], sc["original_max_position"]
         self._mc = mc
         W = weights
         self._arrays = {k: _ptr_array(W[k]) for k in ("n1", "wqkv", "wo", "n2", "wgu", "wd")}

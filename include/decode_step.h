@@ -324,6 +324,19 @@ typedef struct {
                           * decode), which needs bf16 weights (else 572) and a head_dim that
                           * divides 128 (else 577). */
     int32_t max_ctx;     /* largest position + 1 a step will see */
+    /* Long-context RoPE scaling as Llama 3.1 checkpoints define it (not on the
+     * pages): pair p's frequency f = rope_base^(-2p/head_dim), wavelength
+     * w = 2 pi / f, becomes f where w < rope_orig_max_pos / rope_high_freq_factor,
+     * f / rope_factor where w > rope_orig_max_pos / rope_low_freq_factor, and
+     * (1 - s) f / rope_factor + s f in between, with
+     * s = (rope_orig_max_pos / w - rope_low_freq_factor) /
+     *     (rope_high_freq_factor - rope_low_freq_factor).
+     * rope_factor 0 (a zeroed struct): no scaling.  Otherwise rope_factor >= 1,
+     * 0 < rope_low_freq_factor < rope_high_freq_factor and rope_orig_max_pos > 0
+     * (else 577).  Applies to every position of the model's RoPE table. */
+    double rope_factor;
+    double rope_low_freq_factor, rope_high_freq_factor;
+    double rope_orig_max_pos;
 } ds_model_config;
 
 /* Device pointers to the weights, in this storage layout:

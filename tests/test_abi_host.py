@@ -143,6 +143,18 @@ def test_model_config_validation(abi):
         assert abi.lib.ds_model_workspace_bytes(ctypes.byref(mc(cfg))) > 0
     assert abi.lib.ds_model_workspace_bytes(ctypes.byref(mc(C.LLAMA3_8B, n_qh=30))) == 0   # 30 % 8
     assert abi.lib.ds_model_workspace_bytes(ctypes.byref(mc(C.LLAMA3_8B, head_dim=96))) == 0  # band split
+    # long-context RoPE scaling: accepted with Llama 3.1's parameters, refused
+    # when the bands are empty or inverted or the factor speeds pairs up
+    def scaled(factor, lo, hi, orig):
+        m = mc(C.LLAMA3_8B)
+        m.rope_factor, m.rope_low_freq_factor, m.rope_high_freq_factor, m.rope_orig_max_pos = factor, lo, hi, orig
+        return abi.lib.ds_model_workspace_bytes(ctypes.byref(m))
+    assert scaled(8.0, 1.0, 4.0, 8192.0) > 0
+    assert scaled(8.0, 4.0, 1.0, 8192.0) == 0
+    assert scaled(8.0, 1.0, 1.0, 8192.0) == 0
+    assert scaled(0.5, 1.0, 4.0, 8192.0) == 0
+    assert scaled(8.0, 1.0, 4.0, 0.0) == 0
+    assert scaled(float("nan"), 1.0, 4.0, 8192.0) == 0
     out = ctypes.c_void_p()
     m = mc(C.TOY)
     assert abi.lib.ds_model_create(ctypes.byref(m), None, None, 0, ctypes.byref(out)) == abi.DS_BAD_ARGUMENT

@@ -329,3 +329,43 @@ def test_long_context_attention_streamed_through_the_ring(M, shape, n_ctx):
         if top2_gap(ref) > TIE_GAP:
             assert int(g.next_ids[0]) == O.argmax(ref.astype(np.float32))[0]
     assert g.error_word() == 0
+
+
+LLAMA31_SCALING = {"factor": 8.0, "low_freq_factor": 1.0, "high_freq_factor": 4.0,
+                   "original_max_position": 8192.0}
+
+
+def test_llama31_rope_scaling_past_the_original_context(M):
+    """Long-context RoPE scaling as Llama 3.1 checkpoints define it, in the
+    model's RoPE table: 8B widths, 2 layers, two steps at positions 9000 and
+    9001 from a synthetic prefilled context.  Logits and the K rows written
+    match the scaled oracle; the K rows are far from the unscaled rotation."""
+    cfg = dict(small_bf16(C.LLAMA3_8B, 2), rope_scaling=LLAMA31_SCALING)
+    n_ctx = 9000
+    W = synth.model_weights(cfg, seed=31, device="cuda")
+    g = M.DecodeModel(cfg, W, capacity=n_ctx + 16, block_tokens=16)
+    ks, vs = synth.synthetic_kv(cfg, n_ctx, seed=32, device="cuda")
+    for l in range(cfg["n_layer"]):
+        g.k_cache[l][:n_ctx].copy_(ks[l])
+        g.v_cache[l][:n_ctx].copy_(vs[l])
+    st = synth.weights_to_numpy(W)
+    o = oracle_model(cfg, st, g.capacity)
+    plain = oracle_model(dict(cfg, rope_scaling=None), st, g.capacity)
+    for oo in (o, plain):
+        for l in range(cfg["n_layer"]):
+            oo.k[l][:ks[l].numel()] = host(ks[l]).ravel()
+            oo.v[l][:vs[l].numel()] = host(vs[l]).ravel()
+    row = cfg["n_kvh"] * cfg["head_dim"]
+    for i, t in enumerate(synth.prompt_ids(cfg, 2, seed=33)):
+        pos = n_ctx + i
+        g.set_state([t], [pos])
+        g.step()
+        ref = o.step(t, pos)
+        plain.step(t, pos)
+        assert rel_err(host(g.logits[0]), ref) <= BF16_TOL, i
+        if top2_gap(ref) > TIE_GAP:
+            assert int(g.next_ids[0]) == O.argmax(ref.astype(np.float32))[0]
+        kg = O.bf16_bits_to_f64(host(g.k_cache[0][pos]))
+        assert rel_err(kg, O.bf16_bits_to_f64(o.k[0][pos * row:(pos + 1) * row])) <= BF16_TOL
+        assert rel_err(kg, O.bf16_bits_to_f64(plain.k[0][pos * row:(pos + 1) * row])) > 0.1
+    assert g.error_word() == 0
