@@ -42,6 +42,7 @@ def parse():
     p.add_argument("--batched-only", action="store_true",
                    help="time only the batched (64-sequence) decode (a profiling case; the line's batch-1 keys are "
                         "then absent)")
+    p.add_argument("--no-ops", action="store_true", help="skip the op-level timings")
     p.add_argument("--prompt-only", action="store_true",
                    help="time only the chunked prompt (stepSeq) leg (a profiling case)")
     p.add_argument("--batched-steps", type=int, default=None,
@@ -466,6 +467,143 @@ def run_step_seq(cfg, W, dev, rank, clocks_cls, bus, prompt_len=1024, rows=256, 
     return out
 
 
+def op_inputs():
+    """The op-level workload's seeded inputs (fp32 N(0,1) unless stated): GEMV
+    matrices 4096 x 4096 and 4096 x 14336 (three copies each, rotated so
+    every launch streams its matrix from HBM) with their vectors; residual
+    add + RMSNorm over 4096 with weights N(1, 0.1); half-split RoPE on 32 q
+    and 8 k heads of 128 at a position drawn uniform in [0, 8192), base 1e4;
+    128,256 logits with the maximum planted at 3 random indices; one uniform
+    draw for the sampler (temperature 0.8, top_k 50, top_p 0.95)."""
+    import torch
+
+    from autoregressive_decode_step_gb300 import synth
+
+    d = {}
+    for rows, cols in ((4096, 4096), (4096, 14336)):
+        d["gemv", rows, cols] = ([synth.normal((rows * cols,), seed=rows + cols + i) for i in range(3)],
+                                 synth.normal((rows,), seed=rows * 3 + 1))
+    n = 4096
+    d["norm"] = (synth.normal((n,), seed=1), synth.normal((n,), seed=2),
+                 synth.normal((n,), seed=3, mean=1.0, std=0.1))
+    d["rope"] = (int(torch.randint(0, 8192, (1,), generator=torch.Generator().manual_seed(0))),
+                 synth.normal((32 * 128,), seed=10), synth.normal((8 * 128,), seed=20))
+    V = 128256
+    L = synth.normal((V,), seed=40)
+    L[torch.randperm(V, generator=torch.Generator().manual_seed(41))[:3]] = float(L.max()) + 1.0
+    d["logits"] = L
+    d["u"] = synth.uniform_draws(1, seed=0)
+    return d
+
+
+OP_NAMES = ("gemv_transposed_4096x4096", "gemv_transposed_4096x14336", "add_rmsnorm_4096",
+            "rope_half_split_32q_8k_x128", "greedy_argmax_128256", "sample_t0.8_k50_p0.95_128256")
+
+
+def op_bytes():
+    V = 128256
+    return {"gemv_transposed_4096x4096": 4096 * 4096 * 4 + 4096 * 4 * 2,
+            "gemv_transposed_4096x14336": 4096 * 14336 * 4 + (4096 + 14336) * 4,
+            "add_rmsnorm_4096": 5 * 4096 * 4,
+            "rope_half_split_32q_8k_x128": 2 * 40 * 128 * 4,
+            "greedy_argmax_128256": V * 4, "sample_t0.8_k50_p0.95_128256": V * 4}
+
+
+def run_ops(dev, reps=200, warmup=5):
+    """The decode glue one op at a time at the pages' op-level sizes, through
+    the C ABI: each op's device time per launch over `reps` launches between
+    CUDA events on the launching stream after `warmup` launches, and its
+    algorithmic bytes over that time."""
+    import torch
+
+    from autoregressive_decode_step_gb300 import abi as A
+
+    stream = torch.cuda.current_stream(dev)
+    d = op_inputs()
+    us = {}
+
+    def gpu_us(fn):
+        for i in range(warmup):
+            fn(i)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            fn(i)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    for rows, cols in ((4096, 4096), (4096, 14336)):
+        mats, x = d["gemv", rows, cols]
+        mats_d = [m.to(dev) for m in mats]
+        xd = x.to(dev)
+        y = torch.empty(cols, device=dev)
+        ws = A.workspace(A.ds_gemv_workspace_bytes(rows, cols, A.DS_F32), dev)
+        us["gemv_transposed_%dx%d" % (rows, cols)] = gpu_us(
+            lambda i: A.ds_gemv_transposed(mats_d[i % 3], xd, rows, cols, y, ws))
+        del mats_d
+        torch.cuda.empty_cache()
+    r, x, w = (t.to(dev) for t in d["norm"])
+    h = torch.empty(4096, device=dev)
+    us["add_rmsnorm_4096"] = gpu_us(lambda i: A.ds_add_rmsnorm(r, x, w, 1e-5, h, 4096))
+    pos, q, k = d["rope"]
+    qd, kd = q.to(dev), k.to(dev)
+    us["rope_half_split_32q_8k_x128"] = gpu_us(lambda i: A.ds_rope(qd, kd, pos, 32, 8, 128, 10000.0, 0))
+    V = 128256
+    Ld = d["logits"].to(dev)
+    ids = torch.empty(1, dtype=torch.int32, device=dev)
+    mx = torch.empty(1, device=dev)
+    ws = A.workspace(A.ds_argmax_workspace_bytes(1, V), dev)
+    us["greedy_argmax_128256"] = gpu_us(lambda i: A.ds_greedy_argmax(Ld, 1, V, ids, mx, ws))
+    ud = d["u"].to(dev)
+    ws = A.workspace(A.ds_sample_workspace_bytes(1, V), dev)
+    us["sample_t0.8_k50_p0.95_128256"] = gpu_us(lambda i: A.ds_sample(Ld, 1, V, 0.8, 50, 0.95, ud, ids, ws))
+    torch.cuda.synchronize()
+    nb = op_bytes()
+    return {"ops": {k: {"gpu_us": v, "gpu_gbs": nb[k] / (v * 1e-6) / 1e9, "algorithmic_bytes": nb[k]}
+                    for k, v in us.items()},
+            "reps": reps, "warmup": warmup,
+            "workload": "op-level decode glue, fp32, seeded N(0,1) inputs at the pages' measured sizes; the "
+                        "GEMVs rotate three weight copies (larger than L2 together)"}
+
+
+def oracle_op_times():
+    """The oracle on the host cores for the same ops and inputs as run_ops:
+    best of at least 3 calls (and 0.2 s) per op, in microseconds."""
+    import oracle as O
+
+    d = op_inputs()
+    out = {}
+
+    def best_us(fn, min_calls=3, min_s=0.2):
+        best, t_all, calls = float("inf"), 0.0, 0
+        while calls < min_calls or t_all < min_s:
+            t0 = time.perf_counter()
+            fn()
+            dt = time.perf_counter() - t0
+            best, t_all, calls = min(best, dt), t_all + dt, calls + 1
+        return best * 1e6
+
+    for rows, cols in ((4096, 4096), (4096, 14336)):
+        mats, x = d["gemv", rows, cols]
+        a_np, x_np = mats[0].numpy(), x.double().numpy()
+        out["gemv_transposed_%dx%d" % (rows, cols)] = best_us(
+            lambda: O.gemv_transposed(a_np, x_np, rows, cols, O.DT_F32))
+    r, x, w = (t.numpy() for t in d["norm"])
+    out["add_rmsnorm_4096"] = best_us(lambda: O.add_rmsnorm(r, x, w, 1e-5, O.DT_F32))
+    pos, q, k = d["rope"]
+    qn, kn = q.double().numpy(), k.double().numpy()
+    out["rope_half_split_32q_8k_x128"] = best_us(
+        lambda: (O.rope(qn, 32, 128, pos, 10000.0, 0), O.rope(kn, 8, 128, pos, 10000.0, 0)))
+    Ln = d["logits"].numpy()
+    out["greedy_argmax_128256"] = best_us(lambda: O.argmax(Ln))
+    u0 = float(d["u"][0])
+    out["sample_t0.8_k50_p0.95_128256"] = best_us(lambda: O.sample(Ln, 0.8, 50, 0.95, u0))
+    return out
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -638,10 +776,21 @@ def run_ours(args, rank, world, local):
         line["prompt_chunks"] = run_step_seq(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus)
     del W
     torch.cuda.empty_cache()
+    if args.layers is None and not args.no_ops:
+        try:
+            line["ops"] = run_ops(dev)
+        except Exception as e:  # reported in the line, never fatal to the step's numbers
+            line["ops"] = {"error": "%s: %s" % (type(e).__name__, e)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         per_tok, threads, desc, parts = oracle_token_time(C.LLAMA3_8B, args.ctx, reps=3)
         line["cpu_baseline"] = {"value": 1.0 / per_tok, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                 "sample": desc, "head_s": parts[0], "one_layer_step_s": parts[1]}
+        if "ops" in line and "ops" in line["ops"]:
+            per_op = oracle_op_times()
+            line["cpu_baseline"]["per_op_us"] = per_op
+            for k, v in line["ops"]["ops"].items():
+                v["oracle_us"] = per_op[k]
+                v["oracle_over_gpu"] = per_op[k] / v["gpu_us"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
