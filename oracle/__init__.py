@@ -225,7 +225,9 @@ class Model:
     with ``n_blocks`` physical blocks.
 
     ``weights`` keys: emb, out (absent when tied), norm, and per layer lists
-    n1, wqkv, wo, n2, wgu, wd — flat float32 arrays or uint16 bf16 bits.
+    n1, wqkv, wo, n2, wgu, wd — flat float32 arrays or uint16 bf16 bits;
+    optional per layer lists q_norm and k_norm (float32 [head_dim]) turn on
+    the QK-norm of every q and k head before RoPE.
     """
 
     def __init__(self, cfg, weights):
@@ -251,11 +253,15 @@ class Model:
             ptrs += [hold(weights["n1"][l], DT_F32), hold(weights["wqkv"][l], wdt),
                      hold(weights["wo"][l], wdt), hold(weights["n2"][l], DT_F32),
                      hold(weights["wgu"][l], wdt), hold(weights["wd"][l], wdt)]
+        qk_norm = "q_norm" in weights
+        if qk_norm:
+            for l in range(c["n_layer"]):
+                ptrs += [hold(weights["q_norm"][l], DT_F32), hold(weights["k_norm"][l], DT_F32)]
         self._keep = keep
         self._wptrs = (ctypes.c_void_p * len(ptrs))(*ptrs)
         self._iv = np.array([c["vocab"], c["d"], c["n_layer"], c["n_qh"], c["n_kvh"],
                              c["head_dim"], c["ff"], c["rope_layout"], c["tied"], wdt,
-                             c["kv_dtype"], c["block_tokens"], c["max_blocks"]], dtype=np.int64)
+                             c["kv_dtype"], c["block_tokens"], c["max_blocks"], int(qk_norm)], dtype=np.int64)
         self._dv = np.concatenate([np.array([c["rope_base"], c["eps"]], dtype=np.float64),
                                    rope_scaling_vector(c.get("rope_scaling"))])
         bt = c.get("block_table")

@@ -423,6 +423,7 @@ typedef struct {
     int64_t w_dtype;     /* dtype of emb / out / projections */
     int64_t kv_dtype;
     int64_t block_tokens, max_blocks; /* cache geometry, see cache_row */
+    int64_t qk_norm;     /* 1: every q and k head is RMS-normalised before RoPE */
     double rope_base, eps;
     double rope_scaling[4]; /* factor (0: none), low_factor, high_factor, orig_max_pos */
 } or_model;
@@ -441,6 +442,7 @@ static void unpack(or_model *m, const int64_t *iv, const double *dv) {
     m->kv_dtype = iv[10];
     m->block_tokens = iv[11];
     m->max_blocks = iv[12];
+    m->qk_norm = iv[13];
     m->rope_base = dv[0];
     m->eps = dv[1];
     for (int i = 0; i < 4; ++i) m->rope_scaling[i] = dv[2 + i];
@@ -453,6 +455,8 @@ static void unpack(or_model *m, const int64_t *iv, const double *dv) {
  *   n1 [d] fp32 | wqkv [d, (n_qh + 2 n_kvh) hd] (q columns, then k, then v)
  *   | wo [n_qh hd, d] | n2 [d] fp32 | wgu [d, 2 ff] (gate columns, then up)
  *   | wd [ff, d]
+ *   and, with qk_norm, after the layers, per layer l at 3 + 6 n_layer + 2l:
+ *   q_norm [hd] fp32 | k_norm [hd] fp32
  * Caches: k_caches[l], v_caches[l], rows of n_kvh * hd in cache_row layout. */
 
 /* One token through the model at position `pos` of sequence `seq`, with the
@@ -479,6 +483,7 @@ int or_decode_step(const int64_t *iv, const double *dv, const void *const *weigh
     double *f = (double *)malloc((size_t)ff * sizeof(double));
     double *gate = (double *)malloc((size_t)ff * sizeof(double));
     double *up = (double *)malloc((size_t)ff * sizeof(double));
+    double *hbuf = (double *)malloc((size_t)hd * sizeof(double));
 
     /* x = E[token] */
     for (int64_t i = 0; i < d; ++i) x[i] = (float)load_elem(weights[0], token * d + i, (int)m.w_dtype);
@@ -491,6 +496,17 @@ int or_decode_step(const int64_t *iv, const double *dv, const void *const *weigh
         /* q | k | v = Wqkv^T h */
         or_gemv_transposed(L[1], (int)m.w_dtype, h, d, nqkv, qkv);
         double *q = qkv, *k = qkv + nq, *v = qkv + nq + nkv;
+        /* QK-norm as Qwen3 checkpoints define it (not on the pages): every q
+         * head and every k head RMS-normalised over its head_dim values with
+         * the layer's q_norm or k_norm weight, before the rotation */
+        if (m.qk_norm) {
+            const void *qn = weights[3 + 6 * m.n_layer + 2 * l], *kn = weights[3 + 6 * m.n_layer + 2 * l + 1];
+            for (int64_t hh = 0; hh < m.n_qh + m.n_kvh; ++hh) {
+                double *head = hh < m.n_qh ? q + hh * hd : k + (hh - m.n_qh) * hd;
+                or_rmsnorm(head, hh < m.n_qh ? qn : kn, OR_F32, hd, m.eps, hbuf);
+                for (int64_t i = 0; i < hd; ++i) head[i] = hbuf[i];
+            }
+        }
         /* rotate q and k (never v) to this position */
         or_rope(q, m.n_qh, hd, pos, m.rope_base, (int)m.rope_layout, m.rope_scaling);
         or_rope(k, m.n_kvh, hd, pos, m.rope_base, (int)m.rope_layout, m.rope_scaling);
@@ -535,6 +551,7 @@ int or_decode_step(const int64_t *iv, const double *dv, const void *const *weigh
     free(f);
     free(gate);
     free(up);
+    free(hbuf);
     return 0;
 }
 

@@ -129,3 +129,73 @@ def test_bf16_model_cached_equals_recompute_and_paged_equals_contiguous():
         b = mp.step(t, pos)
         np.testing.assert_array_equal(a, b)
     np.testing.assert_allclose(m.recompute(toks), a, rtol=0, atol=0)
+
+
+# QK-norm as Qwen3 checkpoints define it (not on the pages): every q and k
+# head RMS-normalised over head_dim with the layer's q_norm / k_norm weight,
+# before RoPE.
+def qk_norm_storage(cfg, seed):
+    st = random_storage(cfg, seed)
+    rng = np.random.default_rng(seed)
+    st["q_norm"] = [rng.normal(1.0, 0.3, cfg["head_dim"]).astype(np.float32) for _ in range(cfg["n_layer"])]
+    st["k_norm"] = [rng.normal(1.0, 0.3, cfg["head_dim"]).astype(np.float32) for _ in range(cfg["n_layer"])]
+    return st
+
+
+def test_qk_norm_k_row_is_each_head_normalised_then_rotated():
+    """Layer 0's K row at position 5, rebuilt from the separately pinned
+    primitives: RMSNorm of the embedding, the k columns of the projection,
+    each KV head normalised with k_norm (not q_norm), then rotated."""
+    cfg = small_cfg()
+    st = qk_norm_storage(cfg, 6)
+    m = O.Model(cfg, st)
+    tok, pos = 17, 5
+    m.step(tok, pos)
+    d, hd, nq, nkv = cfg["d"], cfg["head_dim"], cfg["n_qh"] * cfg["head_dim"], cfg["n_kvh"] * cfg["head_dim"]
+    x = st["emb"].reshape(cfg["vocab"], d)[tok].astype(np.float64)
+    h = O.rmsnorm(x, st["n1"][0], 1e-5)
+    qkv = O.gemv_transposed(st["wqkv"][0], h, d, nq + 2 * nkv)
+    k = qkv[nq:nq + nkv].copy()
+    for g in range(cfg["n_kvh"]):
+        k[g * hd:(g + 1) * hd] = O.rmsnorm(k[g * hd:(g + 1) * hd], st["k_norm"][0], 1e-5)
+    want = O.rope(k, cfg["n_kvh"], hd, pos, cfg["rope_base"], cfg["rope_layout"])
+    got = m.k[0][pos * nkv:(pos + 1) * nkv].astype(np.float64)
+    np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-7)
+    # the same row without QK-norm is far from it
+    plain = O.Model(cfg, random_storage(cfg, 6))
+    plain.step(tok, pos)
+    assert not np.allclose(plain.k[0][pos * nkv:(pos + 1) * nkv], got, rtol=1e-2)
+
+
+def test_qk_norm_makes_every_head_scale_free():
+    """Scaling one q head's and one k head's projection columns leaves every
+    logit unchanged under QK-norm (eps tiny), and changes them without it."""
+    cfg = small_cfg(eps=1e-12)
+    st = qk_norm_storage(cfg, 7)
+    hd, nq = cfg["head_dim"], cfg["n_qh"] * cfg["head_dim"]
+    cols = nq + 2 * cfg["n_kvh"] * hd
+    scaled = dict(st, wqkv=[w.copy() for w in st["wqkv"]])
+    for l in range(cfg["n_layer"]):
+        w = scaled["wqkv"][l].reshape(cfg["d"], cols)
+        w[:, 1 * hd:2 * hd] *= 4.0          # q head 1 (powers of two: exact in fp32)
+        w[:, nq:nq + hd] *= 0.25            # k of KV head 0
+    toks = [4, 60, 60, 13, 88]
+    a, b = O.Model(cfg, st), O.Model(cfg, scaled)
+    for pos, t in enumerate(toks):
+        # equal up to eps's share and the fp32 rounding of the stored K/V
+        np.testing.assert_allclose(b.step(t, pos), a.step(t, pos), rtol=1e-6, atol=1e-9)
+    plain = {k: v for k, v in st.items() if k not in ("q_norm", "k_norm")}
+    plain_scaled = {k: v for k, v in scaled.items() if k not in ("q_norm", "k_norm")}
+    pa, pb = O.Model(cfg, plain), O.Model(cfg, plain_scaled)
+    diff = max(np.max(np.abs(pa.step(t, pos) - pb.step(t, pos))) for pos, t in enumerate(toks))
+    assert diff > 1e-3
+
+
+def test_qk_norm_cached_decode_equals_recompute():
+    cfg = small_cfg()
+    st = qk_norm_storage(cfg, 8)
+    m = O.Model(cfg, st)
+    toks = [5, 9, 2, 77, 31, 31, 60]
+    for pos, t in enumerate(toks):
+        last = m.step(t, pos)
+    np.testing.assert_allclose(m.recompute(toks), last, rtol=0, atol=0)
