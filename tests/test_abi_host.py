@@ -192,3 +192,33 @@ def test_step_seq_refuses_before_any_launch(abi):
     fake = ctypes.c_void_p(16)  # never dereferenced: the counts are refused first
     assert L.ds_step_seq(fake, None, None, 0, 0, 0, 0, None, None, None) == abi.DS_EMPTY_DIMENSION
     assert L.ds_step_seq(fake, None, fake, 3, 0, 0, 4, fake, None, None) == abi.DS_A_LENGTH_MISMATCH
+
+
+def test_binding_structs_match_the_header_layout(abi, tmp_path):
+    """Every struct the binding mirrors has the header's size and field
+    offsets, as a C compiler lays them out (a drifted field would hand the
+    library shifted values without any error)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"ds_model_config": abi.ModelConfig, "ds_model_weights": abi.ModelWeights,
+               "ds_kv_cache": abi.KVCache, "ds_sampling": abi.Sampling}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "decode_step.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append('printf("%%s size %%zu\\n", "%s", sizeof(%s));' % (cname, cname))
+        for f in py._fields_:
+            lines.append('printf("%%s %%s %%zu\\n", "%s", "%s", offsetof(%s, %s));' % (cname, f[0], cname, f[0]))
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    for line in filter(None, out):
+        cname, field, value = line.split()
+        py = structs[cname]
+        want = ctypes.sizeof(py) if field == "size" else getattr(py, field).offset
+        assert int(value) == want, (cname, field)
