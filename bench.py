@@ -773,7 +773,10 @@ def run_ours(args, rank, world, local):
     if args.layers is None and not args.no_batched:
         line["batched"] = run_batched(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus,
                                       steps=args.batched_steps)
-        line["prompt_chunks"] = run_step_seq(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus)
+        try:
+            line["prompt_chunks"] = run_step_seq(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus)
+        except Exception as e:  # reported in the line, never fatal to the step's numbers
+            line["prompt_chunks"] = {"error": "%s: %s" % (type(e).__name__, e)}
     del W
     torch.cuda.empty_cache()
     if args.layers is None and not args.no_ops:
