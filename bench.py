@@ -379,7 +379,7 @@ def run_batched(cfg, W, dev, rank, clocks_cls, bus, warmup=3, steps=None):
                                  "algorithmic_bytes_per_step": alg,
                                  "algorithmic_bytes": "every weight byte once + K/V of every attended position of "
                                                       "every sequence", "peak_source": kind},
-           "gpu_launches_per_step": 7 * cfg["n_layer"] + 4,
+           "gpu_launches_per_step": 5 * cfg["n_layer"] + 5,  # embed, first norm, 5 per layer, final norm, head, sampler
            "clocks": clocks.summary(t_wall0, t_wall1)}
     del model
     torch.cuda.empty_cache()
