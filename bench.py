@@ -569,13 +569,17 @@ def run_ops(dev, reps=200, warmup=5):
                         "GEMVs rotate three weight copies (larger than L2 together)"}
 
 
-def oracle_op_times():
-    """The oracle on the host cores for the same ops and inputs as run_ops:
-    best of at least 3 calls (and 0.2 s) per op, in microseconds."""
+def oracle_op_times(threads=None):
+    """The oracle on the host cores (all of them, or `threads`) for the same
+    ops and inputs as run_ops: best of at least 3 calls (and 0.2 s) per op,
+    in microseconds."""
     import oracle as O
 
     d = op_inputs()
     out = {}
+    before = O.threads()
+    if threads:
+        O.set_threads(threads)
 
     def best_us(fn, min_calls=3, min_s=0.2):
         best, t_all, calls = float("inf"), 0.0, 0
@@ -601,6 +605,8 @@ def oracle_op_times():
     out["greedy_argmax_128256"] = best_us(lambda: O.argmax(Ln))
     u0 = float(d["u"][0])
     out["sample_t0.8_k50_p0.95_128256"] = best_us(lambda: O.sample(Ln, 0.8, 50, 0.95, u0))
+    if threads:
+        O.set_threads(before)
     return out
 
 
@@ -791,6 +797,7 @@ def run_ours(args, rank, world, local):
         if "ops" in line and "ops" in line["ops"]:
             per_op = oracle_op_times()
             line["cpu_baseline"]["per_op_us"] = per_op
+            line["cpu_baseline"]["per_op_us_one_core"] = oracle_op_times(threads=1)
             for k, v in line["ops"]["ops"].items():
                 v["oracle_us"] = per_op[k]
                 v["oracle_over_gpu"] = per_op[k] / v["gpu_us"]

@@ -32,6 +32,7 @@ def lib():
         I64 = ctypes.c_int64
         D = ctypes.c_double
         L.or_threads.restype = ctypes.c_int
+        L.or_set_threads.argtypes = [ctypes.c_int]
         L.or_f32_to_bf16.argtypes = [ctypes.c_float]
         L.or_f32_to_bf16.restype = ctypes.c_uint16
         L.or_residual_dims_check.argtypes = [I64, I64, I64]
@@ -72,6 +73,12 @@ def _stored(a, dt):
 def threads():
     """Threads the oracle's parallel loops use."""
     return lib().or_threads()
+
+
+def set_threads(n):
+    """Threads for the oracle's later parallel loops (timing only: every
+    output element is computed the same way whatever the count)."""
+    lib().or_set_threads(int(n))
 
 
 # ---------------------------------------------------------------- elements

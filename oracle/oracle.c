@@ -63,6 +63,15 @@ int or_threads(void) {
 #endif
 }
 
+/* Set the threads later OpenMP loops use (ignored without OpenMP). */
+void or_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------ */
 /* element access                                                      */
 /* ------------------------------------------------------------------ */
