@@ -78,6 +78,16 @@ class Sampling(ctypes.Structure):
     _fields_ = [("temperature", F32), ("top_k", I32), ("top_p", F32)]
 
 
+class SchedConfig(ctypes.Structure):
+    _fields_ = [("n_blocks", I32), ("block_tokens", I32), ("max_blocks", I32), ("max_running", I32),
+                ("chunk", I32), ("headroom_blocks", I32)]
+
+
+class SchedRow(ctypes.Structure):
+    _fields_ = [("request", I64), ("slot", I32), ("offset", I32), ("count", I32), ("decode", I32),
+                ("yields", I32)]
+
+
 def _sig(name, res, *args):
     f = getattr(lib, name)
     f.restype = res
@@ -95,6 +105,13 @@ _sig("ds_gemv", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P)
 _sig("ds_gemm_workspace_bytes", SZ, I64, I64, I64)
 _sig("ds_decode_steps", ctypes.c_int, P, P, P, P, ctypes.c_int, P, P, ctypes.c_uint, P)
 _sig("ds_step_seq", ctypes.c_int, P, P, P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P)
+_sig("ds_sched_create", ctypes.c_int, ctypes.POINTER(SchedConfig), P)
+_sig("ds_sched_destroy", None, P)
+_sig("ds_sched_submit", ctypes.c_int, P, I64, I32, I32)
+_sig("ds_sched_plan", ctypes.c_int, P, P, I32, P, P, P, P)
+_sig("ds_sched_commit", ctypes.c_int, P, P, I32)
+_sig("ds_sched_stats", ctypes.c_int, P, P)
+_sig("ds_sched_generated", I64, P, I64)
 _sig("ds_gemm_transposed", ctypes.c_int, P, I64, P, I64, I64, I64, I64, P, I64, P, SZ, P)
 _sig("ds_gemm", ctypes.c_int, P, I64, P, I64, I64, I64, I64, P, I64, P, SZ, P)
 _sig("ds_gemv_transposed_noalloc", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P)

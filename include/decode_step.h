@@ -522,6 +522,92 @@ DS_API int ds_decode_step_profile(ds_model *model, const ds_kv_cache *kv, int32_
                                   unsigned flags, int reps, float *ms_out, int32_t *kinds_out,
                                   int cap, int *n_out, ds_stream_t stream);
 
+/* ---------------------------------------------------------------------
+ * Continuous-batching scheduler slice over the paged K/V pool (host only)
+ * ("Inside the engine", section 2: admission, chunks, preemption, resume).
+ * It decides, step by step, which requests run, as prompt chunks or decode
+ * rows, and which pool blocks each one's block-table row maps; the caller
+ * runs the rows (ds_step_seq for a chunk, ds_decode_step for decode rows)
+ * and reports back.  Policy (the page's, read for a pool whose blocks hold
+ * every layer's K/V of block_tokens positions):
+ *   - a request's tokens are its prompt plus what it has generated; its
+ *     cached prefix is the positions whose K/V sit in its blocks;
+ *   - admission, strictly first come first served over the waiting list
+ *     (preempted requests first, by preemption order, then new ones by
+ *     submission): the head is admitted when a block-table row is free and
+ *     the free blocks cover all its tokens plus headroom_blocks; those
+ *     blocks are taken (lowest block numbers first); otherwise admission
+ *     stops for this step;
+ *   - chunks: a request with uncached tokens runs them in chunks of at most
+ *     `chunk`; the chunk that reaches the last token also yields the next
+ *     token; a request whose tokens are all cached but the last runs one
+ *     decode row (the last token), which yields the next token;
+ *   - preemption: a decode row whose position needs a new block takes the
+ *     lowest free one; with none free, the youngest running request (last
+ *     submitted) is preempted — its blocks and row freed, its cache
+ *     forgotten — until one is free or the request itself was the youngest;
+ *     older requests claim blocks first;
+ *   - resume: a preempted request waits ahead of new ones, first preempted
+ *     first, and recomputes its whole prefix (prompt and generated tokens)
+ *     through the chunked path;
+ *   - completion: a request that has generated max_new tokens, or that the
+ *     caller reports finished, frees its blocks and row at ds_sched_commit;
+ *     the next plan admits into them.
+ * ------------------------------------------------------------------- */
+typedef struct {
+    int32_t n_blocks;        /* blocks in the pool */
+    int32_t block_tokens;    /* positions per block */
+    int32_t max_blocks;      /* block-table width: blocks per request at most */
+    int32_t max_running;     /* block-table rows: requests running at once (a model's max_seqs) */
+    int32_t chunk;           /* prompt tokens a request runs per step at most */
+    int32_t headroom_blocks; /* free blocks demanded beyond a request's tokens at admission */
+} ds_sched_config;
+
+/* One row of a planned step. */
+typedef struct {
+    int64_t request; /* the caller's id */
+    int32_t slot;    /* block-table row (the sequence index the kernels address) */
+    int32_t offset;  /* position of the row's first token */
+    int32_t count;   /* tokens: a chunk of the prompt (or of a resumed prefix), or 1 */
+    int32_t decode;  /* 1: the decode row of a request whose tokens are all cached but the last */
+    int32_t yields;  /* 1: the row ends at the request's last token and yields its next one */
+} ds_sched_row;
+
+typedef struct ds_sched ds_sched;
+
+/* 561 for a count < 1 (headroom_blocks may be 0), 564 beyond DS_MAX_DIM,
+ * 577 for NULL.  The scheduler lives in host memory. */
+DS_API int ds_sched_create(const ds_sched_config *cfg, ds_sched **out);
+DS_API void ds_sched_destroy(ds_sched *sched);
+
+/* Queue a request (ids unique among live requests, else 577): prompt_len >= 1
+ * and max_new >= 1 (561); prompt_len + max_new - 1 positions must fit one
+ * block-table row (571). */
+DS_API int ds_sched_submit(ds_sched *sched, int64_t request, int32_t prompt_len, int32_t max_new);
+
+/* Plan the next step: admit, grow, preempt, and list one row per running
+ * request, oldest first, in rows[0 .. *n_rows) (cap >= max_running, else
+ * 574).  block_table (host int32 [max_running][max_blocks]) receives every
+ * row's blocks, -1 past a request's blocks and in free rows.  preempted
+ * (optional, capacity max_running) receives the ids preempted by this plan,
+ * *n_preempted their count.  A plan must be committed before the next one
+ * (577 otherwise). */
+DS_API int ds_sched_plan(ds_sched *sched, ds_sched_row *rows, int32_t cap, int32_t *n_rows,
+                         int32_t *block_table, int64_t *preempted, int32_t *n_preempted);
+
+/* The planned step ran: every row's tokens are cached, the rows that yield
+ * add a generated token, and requests that reached max_new or appear in
+ * finished[0 .. n_finished) free their blocks and rows.  577 without a plan
+ * to commit. */
+DS_API int ds_sched_commit(ds_sched *sched, const int64_t *finished, int32_t n_finished);
+
+/* Counts: [0] free blocks, [1] running, [2] waiting, [3] finished,
+ * [4] preemptions so far. */
+DS_API int ds_sched_stats(const ds_sched *sched, int64_t *out5);
+
+/* Generated tokens of a live or finished request (-1: unknown id). */
+DS_API int64_t ds_sched_generated(const ds_sched *sched, int64_t request);
+
 #ifdef __cplusplus
 }
 #endif
