@@ -116,6 +116,7 @@ _sig("ds_gemm_transposed", ctypes.c_int, P, I64, P, I64, I64, I64, I64, P, I64, 
 _sig("ds_gemm", ctypes.c_int, P, I64, P, I64, I64, I64, I64, P, I64, P, SZ, P)
 _sig("ds_gemv_transposed_noalloc", ctypes.c_int, P, I64, ctypes.c_int, P, I64, I64, I64, P, I64, P)
 _sig("ds_gemv_transposed_noalloc_max_bytes", SZ)
+_sig("ds_gemv_transposed_noalloc_error", ctypes.c_int, P, P)
 _sig("ds_residual_add", ctypes.c_int, P, I64, P, I64, P, I64, P)
 _sig("ds_add_rmsnorm", ctypes.c_int, P, I64, P, I64, P, I64, ctypes.c_int, F32, P, I64, I64, P)
 _sig("ds_rope", ctypes.c_int, P, I64, P, I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, F64, ctypes.c_int, P)
@@ -208,6 +209,14 @@ def ds_gemv_transposed(A, x, rows, cols, y, ws, stream=None):
 def ds_gemv_transposed_noalloc(A, x, rows, cols, y, stream=None):
     check(lib.ds_gemv_transposed_noalloc(ptr(A), A.numel(), dtype_code(A), ptr(x), x.numel(), rows, cols, ptr(y),
                                          y.numel(), stream_handle(stream)), "ds_gemv_transposed_noalloc")
+
+
+def ds_gemv_transposed_noalloc_error(stream=None):
+    """Read and clear the no-allocation area's error word (current device)."""
+    word = ctypes.c_int32(0)
+    check(lib.ds_gemv_transposed_noalloc_error(ctypes.byref(word), stream_handle(stream)),
+          "ds_gemv_transposed_noalloc_error")
+    return word.value
 
 
 def ds_gemv(W, x, rows, cols, y, stream=None):

@@ -39,6 +39,22 @@ def _deps_mtime():
     return max(os.path.getmtime(p) for p in paths)
 
 
+def _headers_mtime():
+    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if not f.endswith(".cu")]
+    paths += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
+    return max(os.path.getmtime(p) for p in paths)
+
+
+def _stale(src, force):
+    """An object is rebuilt when it is missing or older than its source or
+    any header (every translation unit includes the shared headers)."""
+    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+    if force or not os.path.exists(obj):
+        return True
+    t = os.path.getmtime(obj)
+    return t < os.path.getmtime(src) or t < _headers_mtime()
+
+
 def _compile(src, verbose_ptxas=False):
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc()] + ARCH + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose_ptxas else []) + ["-c", src, "-o", obj]
@@ -54,13 +70,14 @@ def build(force=False, verbose_ptxas=False, jobs=None):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     srcs = sources()
-    jobs = jobs or min(len(srcs), os.cpu_count() or 4)
+    todo = [s for s in srcs if _stale(s, force or verbose_ptxas)]
+    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
     logs = []
-    with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = []
-        for obj, log in ex.map(lambda s: _compile(s, verbose_ptxas), srcs):
-            objs.append(obj)
-            logs.append(log)
+    if todo:
+        jobs = jobs or min(len(todo), os.cpu_count() or 4)
+        with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
+            for _, log in ex.map(lambda s: _compile(s, verbose_ptxas), todo):
+                logs.append(log)
     tmp = LIB + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)

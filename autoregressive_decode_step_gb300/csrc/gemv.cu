@@ -806,19 +806,25 @@ extern "C" DS_API size_t ds_gemv_workspace_bytes(int64_t rows, int64_t cols, int
     return kWsHeader + align_up((size_t)n_bands * 4, 256) + gemv_t_partial_floats(grid, n_bands, es) * 4;
 }
 
-extern "C" DS_API int ds_gemv_transposed(const void *A, int64_t a_len, int a_dtype, const float *x,
-                                         int64_t x_len, int64_t rows, int64_t cols, float *y,
-                                         int64_t y_len, void *workspace, size_t workspace_bytes,
-                                         ds_stream_t stream) {
-    int st = check_matvec(A, a_len, a_dtype, x, x_len, rows, cols, y, y_len, rows, cols);
-    if (st != DS_OK) return st;
-    const size_t need = ds_gemv_workspace_bytes(rows, cols, a_dtype);
-    if (!workspace || workspace_bytes < need) return DS_WORKSPACE_TOO_SMALL;
-    if ((uintptr_t)workspace & 255) return DS_BAD_ARGUMENT;
+namespace ds {
+
+bool gemv_t_uses_workspace(const void *A, int64_t cols, int a_dtype) {
     const int es = a_dtype == DS_BF16 ? 2 : 4;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return gemv_t_streamable(A, nullptr, cols * es, (int)cols, es);
+}
+
+size_t gemv_t_zeroed_bytes(int64_t cols, int a_dtype) {
+    const int es = a_dtype == DS_BF16 ? 2 : 4;
+    const int band_cols = gemv_t_band_cols(es);
+    const int64_t n_bands = (cols + band_cols - 1) / band_cols;
+    return kWsHeader + align_up((size_t)n_bands * 4, 256);
+}
+
+int gemv_transposed_run(const void *A, int a_dtype, const float *x, int64_t rows, int64_t cols, float *y,
+                        char *ws, cudaStream_t s) {
+    const int es = a_dtype == DS_BF16 ? 2 : 4;
     cudaError_t e;
-    if (!gemv_t_streamable(A, nullptr, cols * es, (int)cols, es)) {
+    if (!gemv_t_uses_workspace(A, cols, a_dtype)) {
         const int threads = 256;
         const int blocks = (int)((cols + threads - 1) / threads);
         if (a_dtype == DS_BF16)
@@ -832,7 +838,6 @@ extern "C" DS_API int ds_gemv_transposed(const void *A, int64_t a_len, int a_dty
     const int band_cols = gemv_t_band_cols(es);
     const int n_bands = (int)((cols + band_cols - 1) / band_cols);
     const int grid = gemv_t_grid((int)rows, n_bands);
-    char *ws = static_cast<char *>(workspace);
     GemvTArgs a = {};
     a.a0 = static_cast<const char *>(A);
     a.row_stride = cols * es;
@@ -847,6 +852,21 @@ extern "C" DS_API int ds_gemv_transposed(const void *A, int64_t a_len, int a_dty
     if (!gemv_t_make_maps(a, a_dtype)) return DS_CUDA_ERROR;
     e = launch_gemv_t(a, a_dtype, PRO_PLAIN, EPI_STORE, grid, s, false);
     return e == cudaSuccess ? DS_OK : DS_CUDA_ERROR;
+}
+
+}  // namespace ds
+
+extern "C" DS_API int ds_gemv_transposed(const void *A, int64_t a_len, int a_dtype, const float *x,
+                                         int64_t x_len, int64_t rows, int64_t cols, float *y,
+                                         int64_t y_len, void *workspace, size_t workspace_bytes,
+                                         ds_stream_t stream) {
+    int st = check_matvec(A, a_len, a_dtype, x, x_len, rows, cols, y, y_len, rows, cols);
+    if (st != DS_OK) return st;
+    const size_t need = ds_gemv_workspace_bytes(rows, cols, a_dtype);
+    if (!workspace || workspace_bytes < need) return DS_WORKSPACE_TOO_SMALL;
+    if ((uintptr_t)workspace & 255) return DS_BAD_ARGUMENT;
+    return gemv_transposed_run(A, a_dtype, x, rows, cols, y, static_cast<char *>(workspace),
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" DS_API int ds_gemv(const void *W, int64_t w_len, int w_dtype, const float *x, int64_t x_len,

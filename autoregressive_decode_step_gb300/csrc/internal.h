@@ -103,6 +103,16 @@ bool gemv_t_streamable(const void *a0, const void *a1, long long row_stride, int
 bool gemv_t_make_maps(GemvTArgs &a, int dtype);
 cudaError_t launch_gemv_t(const GemvTArgs &a, int dtype, int pro, int epi, int grid,
                           cudaStream_t stream, bool pdl);
+// ds_gemv_transposed after its host checks: y = A^T x with the split
+// reduction's scratch at `ws` (ds_gemv_workspace_bytes bytes, unused when
+// gemv_t_uses_workspace is false: the plain-load kernel then runs).
+int gemv_transposed_run(const void *A, int a_dtype, const float *x, int64_t rows, int64_t cols, float *y,
+                        char *ws, cudaStream_t s);
+bool gemv_t_uses_workspace(const void *A, int64_t cols, int a_dtype);
+// Bytes at the start of ds_gemv_transposed's workspace that the streamed
+// path needs at zero when it starts: the header (error word) and the band
+// counters; the partial sums after them need no clearing.
+size_t gemv_t_zeroed_bytes(int64_t cols, int a_dtype);
 
 struct GemvNArgs {
     const char *W;        // [rows][cols]

@@ -17,16 +17,18 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = 1u << 20;  // 1 MiB
 
-// The scratch area (zero at load).  In host code this name is only a
-// stand-in for the device variable: its device address comes from
-// cudaGetSymbolAddress below.
+// The scratch area (zero at load).  Byte 0 is the error word, as in every
+// workspace; the band counters and partial sums follow.  In host code this
+// name is only a stand-in for the device variable: its device address comes
+// from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
 void *g_scratch_ptr[64] = {nullptr};
 
 // Device address of the scratch area on the current device, looked up once
-// per device (that first lookup is the set-up the header describes).
+// per device (that first lookup is the set-up the header describes) and kept
+// for the life of the process.
 void *scratch_on_current_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
@@ -57,18 +59,26 @@ extern "C" DS_API int ds_gemv_transposed_noalloc(const void *A, int64_t a_len, i
     if (x_len != rows) return DS_GEMV_X_LENGTH_MISMATCH;
     if (y_len != cols) return DS_A_LENGTH_MISMATCH;
     if (!A || !x || !y) return DS_BAD_ARGUMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // a matrix the streamed kernel cannot take runs the plain-load kernel,
+    // which uses no scratch at all
+    if (!ds::gemv_t_uses_workspace(A, cols, a_dtype)) return ds::gemv_transposed_run(A, a_dtype, x, rows, cols, y,
+                                                                                      nullptr, s);
     const size_t need = ds_gemv_workspace_bytes(rows, cols, a_dtype);
     if (need == 0 || need > kNoAllocScratchBytes) return DS_DIMENSION_TOO_LARGE;  // beyond the built-in area
+    char *scratch = static_cast<char *>(scratch_on_current_device());
+    if (!scratch) return DS_CUDA_ERROR;
+    // The area keeps whatever the previous call left: the band counters must
+    // start at zero.  The error word (byte 0) is left alone so that it keeps
+    // any bit a kernel set until ds_gemv_transposed_noalloc_error reads it.
+    const size_t zero_from = ds::kWsHeader, zero_to = ds::gemv_t_zeroed_bytes(cols, a_dtype);
+    if (cudaMemsetAsync(scratch + zero_from, 0, zero_to - zero_from, s) != cudaSuccess) return DS_CUDA_ERROR;
+    return ds::gemv_transposed_run(A, a_dtype, x, rows, cols, y, scratch, s);
+}
+
+extern "C" DS_API int ds_gemv_transposed_noalloc_error(int32_t *host_word, ds_stream_t stream) {
+    if (!host_word) return DS_BAD_ARGUMENT;
     void *scratch = scratch_on_current_device();
     if (!scratch) return DS_CUDA_ERROR;
-    // The area keeps whatever the previous call left; the error word and the
-    // split counters must start at zero.
-    const int es = a_dtype == DS_BF16 ? 2 : 4;
-    const int band_cols = ds::gemv_t_band_cols(es);
-    const size_t n_bands = (size_t)((cols + band_cols - 1) / band_cols);
-    const size_t zero_bytes = ds::kWsHeader + ds::align_up(n_bands * 4, 256);
-    if (cudaMemsetAsync(scratch, 0, zero_bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return DS_CUDA_ERROR;
-    return ds_gemv_transposed(A, a_len, a_dtype, x, x_len, rows, cols, y, y_len, scratch, kNoAllocScratchBytes,
-                              stream);
+    return ds_workspace_error(scratch, host_word, stream);
 }

@@ -139,19 +139,30 @@ DS_API int ds_gemv_transposed(const void *A, int64_t a_len, int a_dtype, const f
  * ds_gemv_transposed, minus the workspace: the split-reduction scratch comes
  * from a fixed area compiled into the library, which every GPU that loads the
  * library keeps (ds_gemv_transposed_noalloc_max_bytes() bytes, 1 MiB) until
- * the process exits.  A shape whose scratch (ds_gemv_workspace_bytes) does not
- * fit in it is refused with DS_DIMENSION_TOO_LARGE.  The call allocates
- * nothing: it clears the part of the area that must start at zero with one
- * asynchronous memset and launches the kernel on `stream`.
+ * the process exits.  A matrix on the streamed path (A 16-byte aligned and
+ * cols * element size a multiple of 16 bytes) whose scratch
+ * (ds_gemv_workspace_bytes) does not fit in the area is refused with
+ * DS_DIMENSION_TOO_LARGE; any other matrix runs the plain-load kernel, which
+ * uses no scratch.  The call allocates nothing: on the streamed path it clears
+ * the band counters with one asynchronous memset, then launches the kernel on
+ * `stream`.
  *  - The first call on a device (that device current) looks up the area's
- *    device address; make that first call before any stream capture.
+ *    device address, which is kept for the life of the process; make that
+ *    first call before any stream capture.  After cudaDeviceReset the kept
+ *    address is stale: the call must not be used again in that process.
  *  - All calls share the one area and it keeps the last call's contents:
  *    calls whose GPU work overlaps (other streams, other threads) race on it
- *    and must be ordered by the caller. */
+ *    and must be ordered by the caller.
+ *  - A kernel's error bits (DS_ERR_*) collect in the area's error word across
+ *    calls until ds_gemv_transposed_noalloc_error reads and clears it. */
 DS_API int ds_gemv_transposed_noalloc(const void *A, int64_t a_len, int a_dtype, const float *x,
                                       int64_t x_len, int64_t rows, int64_t cols, float *y,
                                       int64_t y_len, ds_stream_t stream);
 DS_API size_t ds_gemv_transposed_noalloc_max_bytes(void);
+/* Copy the no-allocation area's error word (of the current device) to
+ * *host_word and clear it, as ds_workspace_error does for a workspace.
+ * Synchronises `stream`. */
+DS_API int ds_gemv_transposed_noalloc_error(int32_t *host_word, ds_stream_t stream);
 
 /* y = W x: y[r] = sum_c W[r * cols + c] * x[c] for r < rows — the
  * untransposed form the "LLM inference kernels" page uses for lm_head.
