@@ -19,7 +19,8 @@
  *    are stored in the cache dtype after passing through fp32, because the
  *    model's activations are fp32 ("decode-ops", "Requirements and limits").
  *    Everything the model does not store is kept in fp64.
- *  - The sampler takes its decisions in fp32, in the order stated below.
+ *  - The sampler's scaled logits and exponentials are fp32; its sums and
+ *    decisions are fp64 (see or_sample).
  *
  * Parity pins for every function live in tests/ (worked examples printed on
  * the pages, closed forms, invariants, brute force).  Nothing here is tuned;
@@ -358,19 +359,23 @@ static int by_key_desc(const void *pa, const void *pb) {
 
 /* Temperature -> top-k -> softmax over survivors -> top-p -> renormalise ->
  * inverse CDF at the caller's uniform draw u in [0,1) ("decode-ops",
- * "API — Method", the HuggingFace warper order).  All arithmetic is fp32, in
- * the order written here, because the pages give the sampler f32 inputs and
- * an integer result is decided by it:
- *   l'_i = l_i / T;  survivors = first top_k of (l' desc, index asc), all if
- *   top_k <= 0 or top_k >= n;  e_i = expf(l'_i - l'_max);  S = sum e_i in
- *   survivor order;  p_i = e_i / S;  keep the prefix whose exclusive running
- *   sum of p is < top_p (at least one; top_p >= 1 keeps all);  S2 = sum of the
+ * "API — Method", the HuggingFace warper order).  The pages give the sampler
+ * f32 logits and exp (exp(0) == 1), and leave the precision of its running
+ * sums open; here the scaled logits and the exponentials are fp32 and every
+ * sum, ratio and comparison after them is fp64, so that the token depends on
+ * the method's values, not on the order in which a long sum is taken:
+ *   l'_i = l_i / T (fp32);  survivors = first top_k of (l' desc, index asc),
+ *   all if top_k <= 0 or top_k >= n;  e_i = expf(l'_i - l'_max) (fp32);
+ *   S = sum e_i;  p_i = e_i / S;  keep the prefix whose exclusive running sum
+ *   of p is < top_p (at least one; top_p >= 1 keeps all);  S2 = sum of the
  *   kept p;  token = first kept with inclusive running sum > u * S2, else the
  *   last kept.
  * T <= 0 means greedy.  `margin` (optional) receives the smallest distance,
- * relative to S2, between u * S2 and a kept inclusive running sum, so that a
- * caller can tell a draw that sits on a CDF boundary.  Returns the token id,
- * or -1 for a parameter outside its domain (top_p <= 0, u outside [0,1)). */
+ * as a fraction of the mass, between a running sum and the threshold it was
+ * compared with (top_p for the exclusive sums the top-p cut tests, u * S2 / S2
+ * for the inclusive sums of the draw), so that a caller can tell a draw or a
+ * cut that sits on a boundary.  Returns the token id, or -1 for a parameter
+ * outside its domain (top_p <= 0, u outside [0,1)). */
 int64_t or_sample(const float *logits, int64_t n, float temperature, int64_t top_k,
                   float top_p, float u, double *margin) {
     if (margin) *margin = INFINITY;
@@ -383,31 +388,40 @@ int64_t or_sample(const float *logits, int64_t n, float temperature, int64_t top
     }
     qsort(c, (size_t)n, sizeof(keyed), by_key_desc);
     int64_t k = (top_k <= 0 || top_k >= n) ? n : top_k;
-    float *p = (float *)malloc((size_t)k * sizeof(float));
-    float S = 0.0f;
+    double *p = (double *)malloc((size_t)k * sizeof(double));
+    double S = 0.0;
     for (int64_t i = 0; i < k; ++i) {
-        p[i] = expf(c[i].key - c[0].key);
+        const float e = expf(c[i].key - c[0].key);
+        p[i] = (double)e;
         S += p[i];
     }
     for (int64_t i = 0; i < k; ++i) p[i] = p[i] / S;
     int64_t kept = k;
     if (top_p < 1.0f) {
-        float excl = 0.0f;
+        double excl = 0.0;
         kept = 0;
-        while (kept < k && (kept == 0 || excl < top_p)) {
+        while (kept < k && (kept == 0 || excl < (double)top_p)) {
+            if (kept > 0 && margin) {
+                const double d = fabs(excl - (double)top_p);
+                if (d < *margin) *margin = d;
+            }
             excl += p[kept];
             ++kept;
         }
+        if (kept < k && margin) {  /* the comparison that stopped the cut */
+            const double d = fabs(excl - (double)top_p);
+            if (d < *margin) *margin = d;
+        }
     }
-    float S2 = 0.0f;
+    double S2 = 0.0;
     for (int64_t i = 0; i < kept; ++i) S2 += p[i];
-    float target = u * S2;
-    float incl = 0.0f;
+    const double target = (double)u * S2;
+    double incl = 0.0;
     int64_t chosen = -1;
     for (int64_t i = 0; i < kept; ++i) {
         incl += p[i];
         if (margin) {
-            double d = fabs((double)incl - (double)target) / (double)S2;
+            const double d = fabs(incl - target) / S2;
             if (d < *margin) *margin = d;
         }
         if (chosen < 0 && incl > target) chosen = i;

@@ -439,6 +439,44 @@ def test_sampler_topk_ties_keep_lower_indices():
     assert O.sample(l, 1.0, 2, 1.0, 0.75)[0] == 2
 
 
+def test_sampler_flat_vocabulary_inverse_cdf_is_exact():
+    """A flat distribution over the whole 128,256-entry vocabulary: every
+    survivor has mass 1/n, so the draw (j + 1/2) / n must pick token j, and a
+    top-p cut of 0.3 keeps exactly the first 38,477 ids (i/n < 0.3), over
+    which the draw (j + 1/2) / 38477 picks token j.  Running sums carried in
+    fp32 drift by far more than 1/(2n) over this many terms and fail here."""
+    n = 128256
+    l = np.full(n, 0.25, dtype=np.float32)
+    for j in (0, 1, 777, 50000, 99999, 128000, n - 1):
+        tok, margin = O.sample(l, 1.0, 0, 1.0, (j + 0.5) / n)
+        assert tok == j and margin > 0.4 / n
+    kept = 38477
+    for j in (0, 12345, 30000, kept - 1):
+        tok, _ = O.sample(l, 1.0, 0, 0.3, (j + 0.5) / kept)
+        assert tok == j
+    assert O.sample(l, 1.0, 0, 0.3, 0.999999)[0] == kept - 1
+    # top-k over ties keeps the lowest ids: the 1000 survivors are ids 0..999
+    assert O.sample(l, 1.0, 1000, 1.0, 0.9995)[0] == 999
+
+
+@pytest.mark.parametrize("T,k,p", [(1.0, 0, 0.9), (0.7, 400, 0.95)])
+def test_sampler_frequencies_over_a_wide_vocabulary(T, k, p):
+    """The warper's probabilities over 1,000 logits, top-k off or wide: the
+    draw grid's token frequencies match them to within one grid step."""
+    rng = np.random.default_rng(21)
+    logits = rng.standard_normal(1000).astype(np.float32)
+    kept, pr = _hf_warper_probs(logits, T, k, p)
+    n = 8000
+    counts = {}
+    for j in range(n):
+        tok, _ = O.sample(logits, T, k, p, (j + 0.5) / n)
+        counts[tok] = counts.get(tok, 0) + 1
+    assert set(counts) <= set(kept)
+    cum_want = np.cumsum(pr)
+    cum_got = np.cumsum([counts.get(t, 0) for t in kept]) / n
+    assert np.max(np.abs(cum_want - cum_got)) <= 1.0 / n + 1e-9
+
+
 def test_sampler_fixed_draw_gives_fixed_token():
     rng = np.random.default_rng(20)
     l = rng.standard_normal(128256).astype(np.float32)
