@@ -42,7 +42,6 @@ DS_MAX_DIM = 1 << 24
 DS_F32, DS_BF16 = 0, 1
 DS_ROPE_HALF_SPLIT, DS_ROPE_INTERLEAVED = 0, 1
 DS_ERR_TOKEN_RANGE, DS_ERR_POSITION, DS_ERR_WAIT_TIMEOUT, DS_ERR_SAMPLING = 1, 2, 4, 8
-DS_SAMPLE_MAX_TOP_K = 1024
 DS_STEP_ADVANCE = 1
 DS_STEP_PHASE_TIMES = 2
 DS_STEP_TRACE = 4

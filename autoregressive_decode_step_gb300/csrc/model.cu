@@ -449,10 +449,7 @@ int check_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos
     int st = check_kv(m, kv);
     if (st != DS_OK) return st;
     if (sampling && sampling->temperature > 0.0f) {
-        const int64_t V = m->cfg.vocab;
-        const int64_t k_eff = (sampling->top_k <= 0 || sampling->top_k >= V) ? V : sampling->top_k;
-        if (k_eff > DS_SAMPLE_MAX_TOP_K || !(sampling->top_p > 0.0f) || sampling->top_p > 1.0f)
-            return DS_BAD_SAMPLING_PARAM;
+        if (!(sampling->top_p > 0.0f) || sampling->top_p > 1.0f) return DS_BAD_SAMPLING_PARAM;
         if (!u) return DS_BAD_ARGUMENT;
     } else if (sampling && sampling->temperature != sampling->temperature) {
         return DS_BAD_SAMPLING_PARAM;

@@ -293,24 +293,28 @@ DS_API int ds_greedy_argmax(const float *logits, int64_t logits_len, int n_rows,
                             int32_t *ids, float *max_logit, void *workspace,
                             size_t workspace_bytes, ds_stream_t stream);
 
-/* Largest top_k the sampler accepts (top_k <= 0 or >= n disables top-k). */
-#define DS_SAMPLE_MAX_TOP_K 1024
-
 DS_API size_t ds_sample_workspace_bytes(int n_rows, int64_t n);
 
 /* Per row r of logits [n_rows][n], with the explicit uniform draw u[r] in
  * [0,1): temperature -> top-k -> softmax over the survivors -> top-p ->
  * renormalise -> inverse CDF at u ("decode-ops", "API — Method", the
- * HuggingFace warper order).  In fp32 and in this order: l' = l / T;
- * survivors = the top_k largest l', ties to the lower index, in descending
- * order; e_i = exp(l'_i - l'_max); S = sum e_i in survivor order; p_i = e_i/S;
- * keep the prefix whose exclusive running sum of p is < top_p (at least one;
- * top_p >= 1 keeps all); token = first kept survivor whose inclusive running
- * sum exceeds u * (sum of kept p), else the last kept.
+ * HuggingFace warper order).  In this order: l' = l / T (fp32); survivors =
+ * the top_k largest l', ties to the lower index, in descending order;
+ * e_i = exp(l'_i - l'_max) (fp32); p_i = e_i / (sum of e over the
+ * survivors); keep the prefix whose exclusive running sum of p is < top_p (at
+ * least one; top_p >= 1 keeps all); token = first kept survivor whose
+ * inclusive running sum exceeds u * (sum of kept p), else the last kept.
+ * The running sums are exact sums of the e_i, each rounded to a multiple of
+ * 2^-F of the largest (F = min(46, 63 - ceil(log2 n)): 2^-46 at a 128,256
+ * vocabulary), so the token does not depend on summation order.
  *   temperature <= 0: greedy (first index of the maximum).
- *   top_k: 1..DS_SAMPLE_MAX_TOP_K, or <= 0 / >= n for no top-k cut.
+ *   top_k: any value; <= 0 or >= n means no top-k cut.
  *   top_p in (0, 1].  575 for a parameter outside its domain.
- *   u: device fp32 [n_rows]; ids: device int32 [n_rows]. */
+ *   u: device fp32 [n_rows]; ids: device int32 [n_rows].
+ * A row whose largest scaled logit is NaN or infinite gets the first index of
+ * that value and sets DS_ERR_SAMPLING in the workspace's error word.
+ * Each row runs as one cluster of up to 8 thread blocks; no allocation, no
+ * workspace beyond the error word. */
 DS_API int ds_sample(const float *logits, int64_t logits_len, int n_rows, int64_t n,
                      float temperature, int top_k, float top_p, const float *u, int32_t *ids,
                      void *workspace, size_t workspace_bytes, ds_stream_t stream);

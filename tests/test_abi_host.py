@@ -105,7 +105,7 @@ def test_pick_refusals(abi):
     assert L.ds_greedy_argmax(FAKE, 10, 1, 11, FAKE, None, FAKE, 1 << 20, None) == abi.DS_LOGITS_LENGTH_MISMATCH
     assert L.ds_greedy_argmax(FAKE, 0, 0, 11, FAKE, None, FAKE, 1 << 20, None) == abi.DS_EMPTY_DIMENSION
     n = 128256
-    assert L.ds_sample(FAKE, n, 1, n, 0.8, 2000, 0.95, FAKE, FAKE, FAKE, 1 << 20, None) == \
+    assert L.ds_sample(FAKE, n, 1, n, 0.8, 2000, float("nan"), FAKE, FAKE, FAKE, 1 << 20, None) == \
         abi.DS_BAD_SAMPLING_PARAM
     assert L.ds_sample(FAKE, n, 1, n, 0.8, 50, 0.0, FAKE, FAKE, FAKE, 1 << 20, None) == abi.DS_BAD_SAMPLING_PARAM
     assert L.ds_sample(FAKE, n, 1, n, 0.8, 50, 1.5, FAKE, FAKE, FAKE, 1 << 20, None) == abi.DS_BAD_SAMPLING_PARAM

@@ -227,6 +227,27 @@ def test_sampled_decode_matches_oracle_sampler(M):
     assert compared >= 3
 
 
+def test_sampled_decode_over_the_whole_vocabulary(M):
+    """Top-p sampling with no top-k cut over the tied 151,936-entry Qwen
+    vocabulary, through the model's step: the step's pick equals the
+    standalone sampler's on the step's own logits and the same draw (the
+    sampler's parity with the oracle is checked op by op)."""
+    from autoregressive_decode_step_gb300 import abi
+    cfg = small_bf16(C.QWEN3_0_6B, 1)
+    W = synth.model_weights(cfg, seed=7, device="cuda")
+    g = M.DecodeModel(cfg, W, capacity=32, block_tokens=16)
+    u = synth.uniform_draws(5, seed=8)
+    ids = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = abi.workspace(abi.ds_sample_workspace_bytes(1, cfg["vocab"]))
+    for pos, t in enumerate(synth.prompt_ids(cfg, 5, seed=9)):
+        g.set_state([t], [pos])
+        g.u[0] = u[pos]
+        g.step(sampling=(0.9, 0, 0.9))
+        abi.ds_sample(g.logits[0], 1, cfg["vocab"], 0.9, 0, 0.9, g.u[:1], ids, ws)
+        assert int(g.next_ids[0]) == int(ids[0])
+    assert g.error_word() == 0
+
+
 def test_multi_step_launch_equals_single_steps(M):
     """ds_decode_steps (n greedy steps in one launch, the pick handed to the
     next step on the device) against n separate single steps: same ids, same
