@@ -43,6 +43,9 @@ def parse():
                    help="time only the batched (64-sequence) decode (a profiling case; the line's batch-1 keys are "
                         "then absent)")
     p.add_argument("--no-ops", action="store_true", help="skip the op-level timings")
+    p.add_argument("--no-legs", action="store_true",
+                   help="skip the extra batch-1 legs (8B at contexts 4096 and 8192, the Qwen3-0.6B shape, the tiny "
+                        "decoder)")
     p.add_argument("--prompt-only", action="store_true",
                    help="time only the chunked prompt (stepSeq) leg (a profiling case)")
     p.add_argument("--batched-steps", type=int, default=None,
@@ -168,85 +171,60 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_token_time(cfg, ctx, reps, seed=0):
-    """Seconds per decoded token of the CPU oracle for the full model,
-    estimated from a bounded sample: the oracle's decode step on the same
-    shape with 0 layers (embedding, final norm, output head) and with 1 layer,
-    at position `ctx` over a synthetic context; per token = head part + n_layer
-    x layer part.  Returns (seconds per token, threads, description)."""
-    import torch
+class OracleDecoder:
+    """The CPU oracle's full-depth decode step on the given weights over a
+    synthetic prefilled context of `ctx` positions (seeded N(0,1) K/V rows,
+    the same recipe the GPU legs use): greedy, one token at a time from
+    position ctx."""
 
-    import oracle as O
-    from autoregressive_decode_step_gb300 import synth
+    def __init__(self, cfg, W, ctx, capacity, seed):
+        import oracle as O
+        from autoregressive_decode_step_gb300 import synth
 
-    one = dict(cfg, n_layer=1)
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    W = synth.model_weights(one, seed=seed, device=dev)
-    st = synth.weights_to_numpy(W)
-    del W
-    ks, vs = synth.synthetic_kv(one, ctx, seed=seed + 1, device="cpu")
-    ocfg = dict(one, block_tokens=1, max_blocks=ctx + 1)
-    m1 = O.Model(ocfg, st)
-    m0 = O.Model(dict(ocfg, n_layer=0), st)
-    from autoregressive_decode_step_gb300.synth import to_numpy_storage
-    m1.k[0][:ks[0].numel()] = to_numpy_storage(ks[0])
-    m1.v[0][:vs[0].numel()] = to_numpy_storage(vs[0])
-    t_head, t_one = [], []
-    for _ in range(reps):
+        self.O = O
+        st = synth.weights_to_numpy(W)
+        self.m = O.Model(dict(cfg, block_tokens=1, max_blocks=capacity), st)
+        dev = W["emb"].device
+        ks, vs = synth.synthetic_kv(cfg, ctx, seed=seed, device=dev)
+        for l in range(cfg["n_layer"]):
+            self.m.k[l][:ks[l].numel()] = synth.to_numpy_storage(ks[l])
+            self.m.v[l][:vs[l].numel()] = synth.to_numpy_storage(vs[l])
+        del ks, vs
+        self.tok, self.pos = 7, ctx
+
+    def step(self):
+        """One decode step; returns its wall time in seconds."""
         t = time.perf_counter()
-        m0.step(7, ctx)
-        t_head.append(time.perf_counter() - t)
-        t = time.perf_counter()
-        m1.step(7, ctx)
-        t_one.append(time.perf_counter() - t)
-    th, t1 = min(t_head), min(t_one)
-    per_token = th + cfg["n_layer"] * max(t1 - th, 0.0)
-    desc = ("oracle decode step at position %d over a synthetic %d-position context, timed with 0 and 1 "
-            "layers of the %s shape (best of %d); per token = head part + %d x layer part"
-            % (ctx, ctx, cfg["name"], reps, cfg["n_layer"]))
-    return per_token, O.threads(), desc, (th, t1)
+        logits = self.m.step(self.tok, self.pos)
+        dt = time.perf_counter() - t
+        self.tok, self.pos = self.O.argmax(logits.astype("float32"))[0], self.pos + 1
+        return dt
 
 
 def run_reference(args, rank, world):
-    from autoregressive_decode_step_gb300 import configs as C
+    """The oracle as it stands, timed on the host cores: every step is one
+    whole 32-layer decode step of the 8B shape (weights once, K/V of every
+    attended position), the same workload as the GPU arm."""
     import oracle as O
     import torch
+    from autoregressive_decode_step_gb300 import configs as C
     from autoregressive_decode_step_gb300 import synth
 
     if rank != 0:
         return 0
     cfg = C.LLAMA3_8B
-    one = dict(cfg, n_layer=1)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    W = synth.model_weights(one, seed=0, device=dev)
-    st = synth.weights_to_numpy(W)
+    W = synth.model_weights(cfg, seed=0, device=dev)
+    od = OracleDecoder(cfg, W, args.ctx, args.ctx + args.warmup + args.steps + 1, seed=1)
     del W
-    cap = args.ctx + args.warmup + args.steps + 1
-    ks, vs = synth.synthetic_kv(one, args.ctx, seed=1, device="cpu")
-    ocfg = dict(one, block_tokens=1, max_blocks=cap)
-    m1 = O.Model(ocfg, st)
-    m0 = O.Model(dict(ocfg, n_layer=0), st)
-    m1.k[0][:ks[0].numel()] = synth.to_numpy_storage(ks[0])
-    m1.v[0][:vs[0].numel()] = synth.to_numpy_storage(vs[0])
-    t = time.perf_counter()
-    m0.step(7, args.ctx)
-    t_head = time.perf_counter() - t
-    tok = 7
-    pos = args.ctx
     for _ in range(args.warmup):
-        logits = m1.step(tok, pos)
-        tok, pos = O.argmax(logits.astype("float32"))[0], pos + 1
-    total = 0.0
-    for _ in range(args.steps):
-        t = time.perf_counter()
-        logits = m1.step(tok, pos)
-        dt = time.perf_counter() - t
-        tok, pos = O.argmax(logits.astype("float32"))[0], pos + 1
-        total += dt + (cfg["n_layer"] - 1) * max(dt - t_head, 0.0)
+        od.step()
+    times = [od.step() for _ in range(args.steps)]
+    total = sum(times)
     value = args.steps / total
-    sample = ("each step: the oracle's decode step with 1 of the 32 layers plus the full output head, greedy, "
-              "context growing from %d; per token = step time + 31 x (step time - head-only time %.3f s)"
-              % (args.ctx, t_head))
+    sample = ("every step a whole decode step of the oracle (32 layers + the 128,256-row head, greedy) at positions "
+              "%d..%d after %d untimed steps, over a synthetic %d-position context; %d threads"
+              % (args.ctx + args.warmup, args.ctx + args.warmup + args.steps - 1, args.warmup, args.ctx, O.threads()))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -259,12 +237,12 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ GPU arm
-STEP_PROFILE = os.path.join(ROOT, "profiles", "step_kernel_llama3_8b.md")
+STEP_TRAFFIC = os.path.join(ROOT, "profiles", "step_kernel_llama3_8b.json")
 
 
 def kernel_source_sha():
     """sha256 over the sources of the persistent step kernel (the dominant
-    kernel); the committed ncu summary records the value it was taken on."""
+    kernel); the committed traffic record names the value it was taken on."""
     import hashlib
     h = hashlib.sha256()
     for name in ("step.cu", "common.cuh", "internal.h"):
@@ -273,25 +251,144 @@ def kernel_source_sha():
     return h.hexdigest()
 
 
-def profile_summary_traffic_ratio(kernel_src_sha):
-    """DRAM bytes over algorithmic bytes of the step kernel, from the
-    committed ncu summary if it was taken on the current kernel source (else
-    None).  Traffic is proportional to the bytes streamed, so a launch's
-    traffic is this ratio times its algorithmic bytes."""
+def traffic_ratio(kernel_src_sha):
+    """DRAM bytes over algorithmic bytes of the step kernel from the committed
+    ncu record, when it was taken on the current kernel source (else None).
+    Traffic is proportional to the bytes streamed, so a launch's traffic is
+    this ratio times its algorithmic bytes."""
     try:
-        text = open(STEP_PROFILE).read()
-    except OSError:
+        with open(STEP_TRAFFIC) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    sha = ratio = None
-    for line in text.splitlines():
-        if line.startswith("- kernel source sha256:"):
-            sha = line.split(":", 1)[1].strip()
-        if line.startswith("- dram bytes / algorithmic bytes:"):
-            try:
-                ratio = float(line.split(":", 1)[1].strip().split()[0])
-            except ValueError:
-                ratio = None
-    return ratio if sha == kernel_src_sha else None
+    if rec.get("kernel_source_sha256") != kernel_src_sha:
+        return None
+    return float(rec["dram_bytes"]) / float(rec["algorithmic_bytes"])
+
+
+def time_batch1(model, cfg, K, chunk, first, ctx, stream):
+    """K greedy decode steps of one sequence from position ctx, in launches of
+    up to `chunk` steps each (the picks handed over on the device), between
+    CUDA events on `stream`; returns (ms, launches)."""
+    import torch
+
+    chunks = []
+    left = K
+    while left > 0:
+        chunks.append(min(chunk, left))
+        left -= chunks[-1]
+    model.set_state([first], [ctx])
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for n in chunks:
+        model.steps(n, stream=stream)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1), len(chunks)
+
+
+def run_batch1_leg(cfg, W, dev, ctx, K, warmup, chunk, kv_seed, prompt=None):
+    """Batch-1 greedy decode of `cfg` from a context of ctx positions (a
+    random prompt prefilled through the decode step when `prompt` is given,
+    else seeded N(0,1) K/V rows), K steps timed as in the main leg; the
+    roofline is every weight byte once plus the K/V of every attended
+    position, over the measured HBM bandwidth."""
+    import torch
+
+    from autoregressive_decode_step_gb300 import configs as C
+    from autoregressive_decode_step_gb300 import synth
+    from autoregressive_decode_step_gb300.model import DecodeModel
+
+    model = DecodeModel(cfg, W, capacity=ctx + max(K, warmup) + 8, device=dev, block_tokens=16)
+    if prompt is not None:
+        model.prefill(prompt)
+        first = int(model.next_ids[0])
+    else:
+        ks, vs = synth.synthetic_kv(cfg, ctx, seed=kv_seed, device=dev)
+        for l in range(cfg["n_layer"]):
+            model.k_cache[l][:ctx].copy_(ks[l])
+            model.v_cache[l][:ctx].copy_(vs[l])
+        del ks, vs
+        first = synth.prompt_ids(cfg, 1, seed=kv_seed)[0]
+    stream = torch.cuda.Stream(device=dev)
+    time_batch1(model, cfg, warmup, chunk, first, ctx, stream)
+    ms, launches = time_batch1(model, cfg, K, chunk, first, ctx, stream)
+    err = model.error_word()
+    if err:
+        raise RuntimeError("device error word %d" % err)
+    alg = sum(C.step_bytes(cfg, ctx + i + 1) for i in range(K)) / K
+    peak, kind = peaks()
+    achieved = alg / (ms / K / 1e3) / 1e9
+    del model
+    torch.cuda.empty_cache()
+    return {"value": K / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms / K, "steps": K, "warmup": warmup,
+            "launches": launches, "context": ctx,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_source": kind, "algorithmic_bytes_per_step": alg}}
+
+
+def run_toy_leg(dev, reps=50):
+    """The pages' tiny decoder (vocab 40, d 16, 2 layers; P4's seed-0
+    weights and prompt): microseconds per greedy step, one captured-graph
+    replay per step and 16 steps per launch, and the oracle's microseconds
+    per step on one host core."""
+    import torch
+
+    import oracle as O
+    from autoregressive_decode_step_gb300 import configs as C
+    from autoregressive_decode_step_gb300 import synth
+    from autoregressive_decode_step_gb300.model import DecodeModel
+
+    cfg = C.TOY
+    st = synth.p4_to_storage(synth.p4_toy_weights(cfg, 0), cfg)
+    W = {k: ([torch.from_numpy(a).to(dev) for a in v] if isinstance(v, list) else torch.from_numpy(v).to(dev))
+         for k, v in st.items()}
+    g = DecodeModel(cfg, W, capacity=cfg["max_seq"], device=dev, block_tokens=4)
+    prompt = list(synth.P4_PROMPT)
+    g.prefill(prompt)
+    first = int(g.next_ids[0])
+    p0 = len(prompt)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        replay = g.graph(advance=True, write_logits=False, stream=stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(3):
+            g.set_state([first], [p0])
+            torch.cuda.synchronize()
+            ev[0].record(stream)
+            fn()
+            ev[1].record(stream)
+            ev[1].synchronize()
+            best = min(best, ev[0].elapsed_time(ev[1]) * 1e3)
+        return best
+
+    def replays():
+        for _ in range(16):
+            replay(stream)
+
+    us_graph = timed(replays) / 16
+    us_multi = timed(lambda: g.steps(16, stream=stream)) / 16
+    ids = torch.zeros(16, dtype=torch.int32, device=dev)
+    g.set_state([first], [p0])
+    g.steps(16, ids_out=ids)
+    gpu_ids = [first] + ids.cpu().tolist()[:15]
+    o = O.Model(dict(cfg, block_tokens=1, max_blocks=cfg["max_seq"]), st)
+    before = O.threads()
+    O.set_threads(1)
+    t0 = time.perf_counter()
+    want, _ = O.greedy_generate(o, prompt, 16)
+    t_oracle = time.perf_counter() - t0
+    O.set_threads(before)
+    return {"workload": "tiny Llama-style decoder of \"The forward pass end to end\" (vocab 40, d 16, 2 layers, "
+                        "4q/2kv x 4, ff 24, fp32, P4's seed-0 weights and prompt [3,14,15,9,2,6]), 16 greedy steps",
+            "us_per_step_graph_replay": us_graph, "us_per_step_16_per_launch": us_multi,
+            "oracle_us_per_step_one_core": t_oracle * 1e6 / (len(prompt) + 16),
+            "ids_equal_oracle": gpu_ids == want, "first_ids": gpu_ids[:4]}
 
 
 def run_batched(cfg, W, dev, rank, clocks_cls, bus, warmup=3, steps=None):
@@ -751,16 +848,20 @@ def run_ours(args, rank, world, local):
     alg_bytes = sum(step_bytes) / n_launch
     launch_us = ms * 1000.0 / n_launch
     achieved = alg_bytes / (launch_us / 1e6) / 1e9
-    ratio = profile_summary_traffic_ratio(kernel_source_sha()) if args.layers is None else None
+    ratio = traffic_ratio(kernel_source_sha()) if args.layers is None else None
     traffic = ratio * alg_bytes if ratio is not None else None
+    per_launch_steps = sorted(set(chunks)) if chunks else [1]
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic,
-                "kernel": "step_kernel: persistent cooperative decode step (all layers + head + argmax); "
-                          + ("%d greedy steps per launch, picks handed over on the device" % args.chunk
-                             if chunks else "one launch per token"),
+                "kernel": "step_kernel: persistent cooperative decode step (all layers + head + argmax); %s greedy "
+                          "step(s) per launch, %d launch(es), picks handed over on the device"
+                          % ("/".join(str(c) for c in per_launch_steps), n_launch),
                 "peak_source": peak_kind + " (MEASURED_PEAKS hbm_gbs copy)" if peak_kind == "measured" else peak_kind,
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "algorithmic_bytes": "every weight byte once + K/V of every attended position",
+                "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum over algorithmic bytes from "
+                                  "profiles/step_kernel_llama3_8b.json, times this launch's algorithmic bytes"
+                                  if traffic is not None else "no ncu record on the current kernel source",
                 "mean_launch_us": launch_us}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
@@ -783,20 +884,55 @@ def run_ours(args, rank, world, local):
             line["prompt_chunks"] = run_step_seq(cfg, W, dev, rank, clocks_cls=ClockSampler, bus=bus)
         except Exception as e:  # reported in the line, never fatal to the step's numbers
             line["prompt_chunks"] = {"error": "%s: %s" % (type(e).__name__, e)}
+    if args.layers is None and not args.no_legs:
+        legs = {}
+        for c in (4096, 8192):
+            try:
+                legs[str(c)] = run_batch1_leg(cfg, W, dev, c, K, Wm, args.chunk, kv_seed=rank + 11 + c)
+                legs[str(c)]["workload"] = ("llama3-8b shape, batch-1 greedy decode, synthetic %d-position context "
+                                            "(seeded N(0,1) K/V), %d decoded" % (c, K))
+            except Exception as e:
+                legs[str(c)] = {"error": "%s: %s" % (type(e).__name__, e)}
+        line["context_legs"] = legs
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.layers is None:
+        # the oracle as it stands, whole decode steps of the same model
+        od = OracleDecoder(cfg, W, args.ctx, args.ctx + 8, seed=1)
+        import oracle as O
+        times = [od.step() for _ in range(3)]
+        del od
+        line["cpu_baseline"] = {"value": len(times) / sum(times), "unit": "tokens/s", "cores": O.threads(),
+                                "kind": "oracle", "step_s": times,
+                                "sample": "3 whole decode steps of the oracle (32 layers + head, greedy) at positions "
+                                          "%d..%d over a synthetic %d-position context, on the same weights"
+                                          % (args.ctx, args.ctx + 2, args.ctx)}
     del W
     torch.cuda.empty_cache()
+    if args.layers is None and not args.no_legs:
+        try:
+            Q = C.QWEN3_0_6B
+            Wq = synth.model_weights(Q, seed=0, device=dev)
+            leg = run_batch1_leg(Q, Wq, dev, 512, 256, 32, 32, kv_seed=rank + 21,
+                                 prompt=synth.prompt_ids(Q, 512, seed=rank + 22))
+            leg["workload"] = ("qwen3-0.6b shape (28 layers, d 1024, 16q/8kv x 128, ff 3072, tied 151,936 head, bf16 "
+                               "weights, fp32 K/V), batch-1 greedy decode, 512-token random prompt prefilled through "
+                               "the decode step, 256 decoded")
+            line["qwen3_0_6b"] = leg
+            del Wq
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["qwen3_0_6b"] = {"error": "%s: %s" % (type(e).__name__, e)}
+        try:
+            line["toy"] = run_toy_leg(dev)
+        except Exception as e:
+            line["toy"] = {"error": "%s: %s" % (type(e).__name__, e)}
     if args.layers is None and not args.no_ops:
         try:
             line["ops"] = run_ops(dev)
         except Exception as e:  # reported in the line, never fatal to the step's numbers
             line["ops"] = {"error": "%s: %s" % (type(e).__name__, e)}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        per_tok, threads, desc, parts = oracle_token_time(C.LLAMA3_8B, args.ctx, reps=3)
-        line["cpu_baseline"] = {"value": 1.0 / per_tok, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                "sample": desc, "head_s": parts[0], "one_layer_step_s": parts[1]}
-        if "ops" in line and "ops" in line["ops"]:
+        if rank == 0 and world == 1 and not args.no_cpu_baseline and "ops" in line["ops"]:
             per_op = oracle_op_times()
-            line["cpu_baseline"]["per_op_us"] = per_op
+            line.setdefault("cpu_baseline", {})["per_op_us"] = per_op
             line["cpu_baseline"]["per_op_us_one_core"] = oracle_op_times(threads=1)
             for k, v in line["ops"]["ops"].items():
                 v["oracle_us"] = per_op[k]
