@@ -65,7 +65,7 @@ class ModelConfig(ctypes.Structure):
 
 class ModelWeights(ctypes.Structure):
     _fields_ = [("emb", P), ("out", P), ("final_norm", P), ("n1", P), ("wqkv", P), ("wo", P), ("n2", P),
-                ("wgu", P), ("wd", P)]
+                ("wgu", P), ("wd", P), ("q_norm", P), ("k_norm", P)]
 
 
 class KVCache(ctypes.Structure):

@@ -53,9 +53,18 @@ __global__ void silu_mul_kernel(const float *gate, const float *up, float *out, 
     }
 }
 
-// One thread per rotation pair of q (then k): theta = pos * base^(-2p/hd),
-// angles formed in fp64 ("decode-ops", "API — Method"), rotation in fp32.
-__global__ void rope_kernel(float *q, int n_qh, float *k, int n_kh, long long pos, int hd, double base, int layout) {
+// The (cos, sin) of every rotation pair of one ds_rope call: the angles
+// pos * base^(-2p/hd) are formed in fp64 on the host once per call
+// ("decode-ops", "API — Method": the angle pairs are built once and reused
+// for every head), rounded to fp32, and passed by value.
+template <int P>
+struct RopeAngles {
+    float c[P], s[P];
+};
+
+// One thread per rotation pair of q (then k), the rotation in fp32.
+template <int P>
+__global__ void rope_kernel(float *q, int n_qh, float *k, int n_kh, int hd, int layout, const RopeAngles<P> ang) {
     grid_dependency_wait();
     const int half = hd >> 1;
     const int pair_id = blockIdx.x * blockDim.x + threadIdx.x;
@@ -63,13 +72,31 @@ __global__ void rope_kernel(float *q, int n_qh, float *k, int n_kh, long long po
     if (pair_id >= total) return;
     const int head = pair_id / half, pr = pair_id % half;
     float *v = head < n_qh ? q + (long long)head * hd : k + (long long)(head - n_qh) * hd;
-    const double theta = (double)pos * pow(base, -(double)(2 * pr) / (double)hd);
-    const float c = (float)cos(theta), s = (float)sin(theta);
+    const float c = ang.c[pr], s = ang.s[pr];
     const int ia = layout == DS_ROPE_INTERLEAVED ? 2 * pr : pr;
     const int ib = layout == DS_ROPE_INTERLEAVED ? 2 * pr + 1 : pr + half;
     const float a = v[ia], b = v[ib];
     v[ia] = a * c - b * s;
     v[ib] = a * s + b * c;
+}
+
+template <int P>
+static cudaError_t launch_rope(float *q, int n_qh, float *k, int n_kh, int64_t pos, int hd, double base, int layout,
+                               cudaStream_t stream) {
+    RopeAngles<P> ang;
+    const int half = hd / 2;
+    for (int p = 0; p < P; ++p) {
+        ang.c[p] = 1.0f;
+        ang.s[p] = 0.0f;
+        if (p < half) {
+            const double theta = (double)pos * std::pow(base, -(double)(2 * p) / (double)hd);
+            ang.c[p] = (float)std::cos(theta);
+            ang.s[p] = (float)std::sin(theta);
+        }
+    }
+    const int pairs = (n_qh + n_kh) * half;
+    return launch_ex(rope_kernel<P>, dim3((pairs + 255) / 256), dim3(256), 0, stream, false, q, n_qh, k, n_kh, hd,
+                     layout, ang);
 }
 
 // cos/sin of pos * base^(-2p/hd) for every position row and pair, fp64
@@ -273,10 +300,11 @@ extern "C" DS_API int ds_rope(float *q, int64_t q_len, float *k, int64_t k_len, 
     if (layout != DS_ROPE_HALF_SPLIT && layout != DS_ROPE_INTERLEAVED) return DS_BAD_DTYPE;
     if (head_dim % 2 || head_dim > 1024 || !q || (n_kh > 0 && !k) || !(base > 0.0)) return DS_BAD_ARGUMENT;
     if (pos < 0 || pos > DS_MAX_DIM) return DS_CACHE_LENGTH_MISMATCH;
-    const int pairs = (n_qh + n_kh) * (head_dim / 2);
-    cudaError_t e = launch_ex(rope_kernel, dim3((pairs + 255) / 256), dim3(256), 0,
-                              reinterpret_cast<cudaStream_t>(stream), false, q, n_qh, k, n_kh, (long long)pos,
-                              head_dim, base, layout);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the angle table rides in the launch's parameters: 512 bytes up to
+    // head_dim 128, 4 KB up to head_dim 1024
+    const cudaError_t e = head_dim <= 128 ? launch_rope<64>(q, n_qh, k, n_kh, pos, head_dim, base, layout, s)
+                                          : launch_rope<512>(q, n_qh, k, n_kh, pos, head_dim, base, layout, s);
     return e == cudaSuccess ? DS_OK : DS_CUDA_ERROR;
 }
 

@@ -180,6 +180,61 @@ __device__ __forceinline__ void tc_load_residual(const TcArgs &p, int tile, int 
 // One chunk (32 sequences) of the fused epilogue for the tile's feature of
 // this thread (row r of the accumulator); `old` is the chunk's residual as
 // tc_load_residual left it (TC_ADD only).
+// QK-norm of one 32-vector chunk of a q|k|v tile (Qwen3's per-head RMSNorm
+// before RoPE): xch[f * kTcXchStride + i] holds feature f of vector i; every q
+// head and every k head (hd consecutive features, aligned to the tile) is
+// scaled per vector by 1/sqrt(mean of its squares + eps) and by q_norm or
+// k_norm; v features are left alone.  The four epilogue warps call it.
+__device__ void tc_qk_norm(const TcArgs &p, int m, int r, float *xch) {
+    const int lane = r & 31, hd = p.head_dim;
+    const bool normed = m < p.nq_cols + p.nkv_cols;
+    float *hs = xch + kTcBM * kTcXchStride;  // [4 warps][32 vectors] head square sums
+    float sq[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float x = xch[r * kTcXchStride + i];
+        sq[i] = x * x;
+    }
+    float tot[32];
+    if (hd >= 32) {
+        // halving exchanges: lane L ends with the warp's 32 features summed for vector L
+#pragma unroll
+        for (int c = 32, b = 16; c > 1; c >>= 1, b >>= 1) {
+            const bool up = (lane & b) != 0;
+#pragma unroll
+            for (int k = 0; k < c / 2; ++k) {
+                const float send = up ? sq[k] : sq[k + c / 2];
+                const float keep = up ? sq[k + c / 2] : sq[k];
+                sq[k] = keep + __shfl_xor_sync(0xffffffffu, send, b);
+            }
+        }
+        hs[(r >> 5) * 32 + lane] = sq[0];
+        named_sync(1, kTcEpiThreads);
+        const int w0 = (r / hd) * (hd >> 5);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float a = 0.0f;
+            for (int w = w0; w < w0 + (hd >> 5); ++w) a += hs[w * 32 + i];
+            tot[i] = a;
+        }
+    } else {  // a head is an aligned group of hd lanes
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float a = sq[i];
+            for (int o = hd >> 1; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            tot[i] = a;
+        }
+    }
+    if (normed) {
+        const bool is_q = m < p.nq_cols;
+        const float w = __ldg((is_q ? p.q_norm : p.k_norm) + (is_q ? m : m - p.nq_cols) % hd);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            xch[r * kTcXchStride + i] *= (1.0f / sqrtf(tot[i] / (float)hd + p.qk_eps)) * w;
+    }
+    named_sync(1, kTcEpiThreads);  // the rescaled rows, before RoPE reads partner features
+}
+
 template <int EPI>
 __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const float (&v)[32], const float (&old)[32],
                                   float *xch, int *s_row, const float *s_scale, int r) {
@@ -263,6 +318,7 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
     } else {
         const int m = tile * kTcBM + r;
         const int total = p.nq_cols + 2 * p.nkv_cols;
+        if (p.q_norm) tc_qk_norm(p, m, r, xch);
         if (m < total) {
             const bool rot = m < p.nq_cols + p.nkv_cols;
             const int hd = p.head_dim, half = hd >> 1;
@@ -343,7 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     int *s_ok = s_flags + 2;                              // [2][4]
     int *s_row = s_ok + 8;                                // [2][kTcMaxN] cache row, position (q|k|v)
     float *s_scale = reinterpret_cast<float *>(s_row + 2 * kTcMaxN);  // [kTcMaxN] folded RMSNorm scales
-    float *xch = s_scale + kTcMaxN;                                   // [128][33]
+    float *xch = s_scale + kTcMaxN;                                   // [128][33], then [4][32]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = (p.K + kTcBK - 1) / kTcBK;
@@ -640,14 +696,14 @@ int tc_n_pad(int n) { return std::max(32, (n + 31) / 32 * 32); }
 
 int tc_stages(int n_pad, int split, int msub) {
     const size_t stage = (size_t)msub * kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
-    const size_t fixed = 1024 + 256 + kTcSmemInts * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
+    const size_t fixed = 1024 + 256 + kTcSmemInts * 4 + (size_t)kTcBM * (kTcXchStride + 1) * 4 + 64;
     int s = (int)((kTcSmemLimit - fixed) / stage);
     return std::min(s, kTcMaxStages);
 }
 
 size_t tc_smem_bytes(int n_pad, int split, int msub, int stages) {
     const size_t stage = (size_t)msub * kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
-    return 1024 + (size_t)stages * stage + 256 + kTcSmemInts * 4 + (size_t)kTcBM * kTcXchStride * 4 + 64;
+    return 1024 + (size_t)stages * stage + 256 + kTcSmemInts * 4 + (size_t)kTcBM * (kTcXchStride + 1) * 4 + 64;
 }
 
 int tc_m_tiles(int M, int epi) { return epi == TC_SILU ? (M + kTcBM / 2 - 1) / (kTcBM / 2) : (M + kTcBM - 1) / kTcBM; }

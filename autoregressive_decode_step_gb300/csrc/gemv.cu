@@ -265,6 +265,30 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemv_t_kernel(const __grid_cons
         } else {  // EPI_QKV
             vals[t] = v;
             named_sync(1, kGtConsumers);
+            if (p.q_norm) {  // QK-norm: each q / k head of the band RMS-normalised before RoPE
+                const int col = band * BAND_COLS + t;
+                const bool normed = t < BAND_COLS && col < p.nq_cols + p.nkv_cols;
+                const int hd = p.head_dim;
+                const float x = normed ? v : 0.0f;
+                float s2 = x * x;
+                if (hd >= 32) {  // a head spans hd / 32 whole warps; red is free here
+                    s2 = warp_sum(s2);
+                    if (lane == 0) red[warp] = s2;
+                    named_sync(1, kGtConsumers);
+                    const int w0 = (t / hd) * (hd >> 5);
+                    s2 = 0.0f;
+                    for (int w = w0; w < w0 + (hd >> 5); ++w) s2 += red[w];
+                } else {
+                    for (int o = hd >> 1; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+                }
+                if (normed) {
+                    const bool is_q = col < p.nq_cols;
+                    const int i = (is_q ? col : col - p.nq_cols) % hd;
+                    v = x * (1.0f / sqrtf(s2 / (float)hd + p.eps)) * __ldg((is_q ? p.q_norm : p.k_norm) + i);
+                    vals[t] = v;
+                }
+                named_sync(1, kGtConsumers);
+            }
             const int col = band * BAND_COLS + t;
             const int total = p.nq_cols + 2 * p.nkv_cols;
             const int pos = *p.pos;

@@ -90,6 +90,9 @@ struct GemvTArgs {
     int rope_rows;
     const int *block_table;
     int block_tokens, max_blocks;
+    // QK-norm before RoPE (null: none): every q / k head scaled by
+    // 1/sqrt(mean of its squares + eps) and by these [head_dim] weights
+    const float *q_norm, *k_norm;
 };
 
 // Columns of one band (partial sums per band) for an element size.
@@ -249,6 +252,7 @@ constexpr int kStMaxSplits = 64;
 struct StepLayer {  // aligned as CUtensorMap requires
     CUtensorMap maps[5];  // q|k|v, o, gate, up, down
     const float *n1, *n2;
+    const float *qn, *kn;  // QK-norm weights [head_dim] or null
 };
 
 struct StepParams {
@@ -296,15 +300,18 @@ struct StepParams {
     int kv_align;           // attention split boundaries are multiples of this (whole blocks)
     int kv_stage_pos;       // positions per K/V stage
     int scratch_floats;     // shared scratch after the ring
+    int max_inflight;       // weight stages requested and not yet landed at most (0: no cap)
     void *kc[kStMaxLayers];
     void *vc[kStMaxLayers];
 };
 
 size_t step_layer_bytes();
-void step_layer_fill(void *dst, const CUtensorMap *maps5, const float *n1, const float *n2);
+void step_layer_fill(void *dst, const CUtensorMap *maps5, const float *n1, const float *n2, const float *qn,
+                     const float *kn);
 int step_scratch_floats(const ds_model_config *c, int grid, int nb_qkv, int nb_o, int nb_gu, int nb_d);
 bool step_supported(const ds_model_config *c);
 int step_stages(int scratch_floats);
+int step_inflight_setting();
 size_t step_smem_bytes(int stages, int scratch_floats);
 cudaError_t launch_step(const void *params, int w_dtype, int kv_dtype, int gq, int grid, cudaStream_t stream);
 

@@ -31,6 +31,7 @@ struct ds_model {
     const void *emb, *out;
     const float *final_norm;
     std::vector<const float *> n1, n2;
+    std::vector<const float *> qn, kn;  // QK-norm weights per layer (empty: none)
     std::vector<const void *> wqkv, wo, wgu, wd;
     char *ws;
     size_t ws_bytes;
@@ -52,6 +53,7 @@ struct ds_model {
     // the persistent step kernel
     bool step_ok;
     int step_grid, step_splits, step_stages, step_scratch;
+    int step_inflight;  // weight stages in flight at most (0: no cap)
     ds::StepLayer *step_layers;
     unsigned *step_bar;
     int *step_abort;
@@ -335,6 +337,8 @@ int run_step(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t *pos, 
         a.block_table = kv->block_table;
         a.block_tokens = kv->block_tokens;
         a.max_blocks = kv->max_blocks;
+        a.q_norm = m->qn.empty() ? nullptr : m->qn[l];
+        a.k_norm = m->kn.empty() ? nullptr : m->kn[l];
         a.tm0 = m->maps[5 * l + 0];
         DS_TRY(launch_gemv_t(a, c.w_dtype, PRO_RMSNORM, EPI_QKV, m->grid_qkv, s, pdl), DS_KIND_QKV);
 
@@ -482,6 +486,14 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
         if (!aligned(w->wqkv[l]) || !aligned(w->wo[l]) || !aligned(w->wgu[l]) || !aligned(w->wd[l]) ||
             !aligned(w->n1[l]) || !aligned(w->n2[l]))
             return DS_BAD_ARGUMENT;
+    // QK-norm: both weight sets or neither
+    const bool qk_norm = w->q_norm || w->k_norm;
+    if (qk_norm) {
+        if (!w->q_norm || !w->k_norm) return DS_BAD_ARGUMENT;
+        for (int l = 0; l < cfg->n_layer; ++l)
+            if (!w->q_norm[l] || !w->k_norm[l] || ((uintptr_t)w->q_norm[l] & 3) || ((uintptr_t)w->k_norm[l] & 3))
+                return DS_BAD_ARGUMENT;
+    }
 
     ds_model *m = new (std::nothrow) ds_model();
     if (!m) return DS_BAD_ARGUMENT;
@@ -497,6 +509,10 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
         m->wo.push_back(w->wo[l]);
         m->wgu.push_back(w->wgu[l]);
         m->wd.push_back(w->wd[l]);
+        if (qk_norm) {
+            m->qn.push_back(w->q_norm[l]);
+            m->kn.push_back(w->k_norm[l]);
+        }
     }
     char *ws = static_cast<char *>(workspace);
     m->ws = ws;
@@ -574,6 +590,7 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
     m->step_splits = L.step_splits;
     m->step_stages = L.step_stages;
     m->step_scratch = L.step_scratch;
+    m->step_inflight = step_inflight_setting();
     m->step_layers = reinterpret_cast<StepLayer *>(ws + L.step_layers);
     m->kv_maps_dev = reinterpret_cast<CUtensorMap *>(ws + L.kv_maps);
     m->step_bar = reinterpret_cast<unsigned *>(ws + L.step_bar);
@@ -644,6 +661,9 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
             q.head_dim = cfg->head_dim;
             q.rope_layout = cfg->rope_layout;
             q.kv_dtype = cfg->kv_dtype;
+            q.q_norm = qk_norm ? w->q_norm[l] : nullptr;
+            q.k_norm = qk_norm ? w->k_norm[l] : nullptr;
+            q.qk_eps = cfg->eps;
             TcArgs &o = m->tc[4 * l + 1];
             ok = ok && mk(TC_ADD, 1, m->wo[l], nullptr, (long long)cfg->d * es, cfg->d, nq, m->att_bf, o, 1);
             o.y = m->x;
@@ -692,7 +712,8 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
 
     std::vector<unsigned char> layer_img((size_t)std::max(cfg->n_layer, 1) * step_layer_bytes(), 0);
     for (int l = 0; l < cfg->n_layer; ++l)
-        step_layer_fill(layer_img.data() + (size_t)l * step_layer_bytes(), &m->maps[5 * l], w->n1[l], w->n2[l]);
+        step_layer_fill(layer_img.data() + (size_t)l * step_layer_bytes(), &m->maps[5 * l], w->n1[l], w->n2[l],
+                        qk_norm ? w->q_norm[l] : nullptr, qk_norm ? w->k_norm[l] : nullptr);
     if (prepare_kernels() != cudaSuccess || cudaMemset(workspace, 0, L.total) != cudaSuccess ||
         cudaMemcpy(m->step_layers, layer_img.data(), layer_img.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
         launch_rope_table(m->rope_cos, m->rope_sin, cfg->max_ctx, cfg->head_dim, cfg->rope_base,
@@ -828,6 +849,7 @@ int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t 
     p.kv_stage_pos = p.kv_tma ? kv_stage_positions(c, kv->block_tokens) : 0;
     p.kv_align = p.kv_tma ? std::max(8, kv->block_tokens) : 1;
     p.scratch_floats = m->step_scratch;
+    p.max_inflight = m->step_inflight;
     for (int l = 0; l < c.n_layer; ++l) {
         p.kc[l] = kv->k[l];
         p.vc[l] = kv->v[l];

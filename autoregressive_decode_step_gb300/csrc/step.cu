@@ -23,6 +23,8 @@
 // an abort flag, after which the remaining phases run without waiting.
 #include <algorithm>
 #include <climits>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -52,6 +54,10 @@ constexpr int kStAttnMinPer = DS_ST_ATTN_MIN_PER;  // fewest positions per atten
 constexpr int kStMergeBatch = 20;
 constexpr int kStBoxesPerStage = kStStageBytes / (kStBoxRows * kStBandBytes);  // 8 boxes of 16 rows at 64 KB
 constexpr size_t kStSmemLimit = 227 * 1024;
+#ifndef DS_ST_MAX_INFLIGHT
+#define DS_ST_MAX_INFLIGHT 2
+#endif
+constexpr int kStMaxInflight = DS_ST_MAX_INFLIGHT;  // weight stages requested and not landed (0: no cap)
 
 __device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
 
@@ -326,6 +332,10 @@ __device__ __forceinline__ void issue_stage(const StageDesc &d, unsigned char *d
 }
 
 // The producer: every weight stage of the step, in order, through the ring.
+// At most p.max_inflight stages are requested and not yet landed at any time
+// (0: every free slot is requested at once): the ring still buffers
+// p.stages landed stages for consumers that are busy elsewhere, but fewer
+// bytes queue in the memory system ahead of the phase hand-offs' polls.
 template <int ES>
 __device__ void produce_all(const Ring &r, const StepParams &p) {
     const uint64_t pol = policy_evict_first();
@@ -333,6 +343,7 @@ __device__ void produce_all(const Ring &r, const StepParams &p) {
     bool ok = true;
     const int pos0 = __ldcg(p.pos);
     const int cap = p.max_blocks * p.block_tokens;
+    const uint32_t inflight = p.max_inflight > 0 && p.max_inflight < r.stages ? (uint32_t)p.max_inflight : 0u;
     for (int step = 0; step < p.n_steps && ok; ++step) {  // weights do not depend on the token
         StageCursor fc;
         fc.n_ctx = min(max(pos0 + step + 1, 1), cap);
@@ -344,6 +355,13 @@ __device__ void produce_all(const Ring &r, const StepParams &p) {
             if (use > 0 && !st_wait(&r.empty[s], (use - 1) & 1, p)) {
                 ok = false;
                 break;
+            }
+            if (inflight && fill >= inflight) {  // stage fill - inflight has landed (its slot is not yet reused)
+                const uint32_t f = fill - inflight;
+                if (!st_wait(&r.full[f % r.stages], (f / r.stages) & 1, p)) {
+                    ok = false;
+                    break;
+                }
             }
             mbar_arrive_expect_tx(&r.full[s], d.bytes);
             issue_stage(d, r.base + (size_t)s * kStStageBytes, &r.full[s], pol, p);
@@ -503,6 +521,36 @@ __device__ float block_sumsq(float v, float *red) {
     return tot;
 }
 
+// QK-norm of one band of the q|k|v output (Qwen3's per-head RMSNorm before
+// RoPE): v[t] holds column col0 + t (t < band_cols, heads of hd columns
+// aligned to the band); every q head is scaled by 1/sqrt(mean of its squares
+// + eps) and by qn, every k head by its own scale and kn, v columns are left
+// alone.  hsum: 8 floats of shared scratch.  All consumer threads call it.
+__device__ void qk_norm_band(float *v, float *hsum, int col0, int band_cols, const float *qn, const float *kn,
+                             int nq_cols, int nkv_cols, int hd, float eps) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int col = col0 + t;
+    const bool normed = t < band_cols && col < nq_cols + nkv_cols;
+    const float x = normed ? v[t] : 0.0f;
+    float s2 = x * x;
+    if (hd >= 32) {  // a head spans hd / 32 whole warps
+        s2 = warp_sum(s2);
+        if (lane == 0) hsum[warp] = s2;
+        named_sync(1, kStConsumers);
+        const int w0 = (t / hd) * (hd >> 5);
+        s2 = 0.0f;
+        for (int w = w0; w < w0 + (hd >> 5); ++w) s2 += hsum[w];
+    } else {  // a head is an aligned group of hd lanes
+        for (int o = hd >> 1; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    if (normed) {
+        const bool is_q = col < nq_cols;
+        const int i = (is_q ? col : col - nq_cols) % hd;
+        v[t] = x * (1.0f / sqrtf(s2 / (float)hd + eps)) * __ldg((is_q ? qn : kn) + i);
+    }
+    named_sync(1, kStConsumers);
+}
+
 enum { ST_STORE = 0, ST_ADD = 1, ST_SILU = 2, ST_QKV = 3 };
 enum { SRC_PLAIN = 0, SRC_NORM = 1, SRC_ATTN = 2 };
 
@@ -659,6 +707,9 @@ __device__ void consume_gt(const Ring &r, uint32_t &fill, int K, int sub_cols, i
         } else {  // ST_QKV: RoPE on q and k; K/V written at pos and handed to attention
             vals[t] = v * scale;
             named_sync(1, kStConsumers);
+            const StepLayer &QL = p.layers[layer];
+            if (QL.qn) qk_norm_band(vals, vals + 256, band * BAND_COLS, BAND_COLS, QL.qn, QL.kn, p.nq_cols,
+                                    p.nkv_cols, p.hd, p.eps);
             const int col = band * BAND_COLS + t;
             const int total = p.nq_cols + 2 * p.nkv_cols;
             if (t < BAND_COLS && col < total) {
@@ -1549,12 +1600,15 @@ __global__ void __launch_bounds__(kStThreads, 1) step_kernel(const __grid_consta
 size_t step_layer_bytes() { return sizeof(StepLayer); }
 
 // Host image of one layer's step descriptor: its five tensor maps and norms.
-void step_layer_fill(void *dst, const CUtensorMap *maps5, const float *n1, const float *n2) {
+void step_layer_fill(void *dst, const CUtensorMap *maps5, const float *n1, const float *n2, const float *qn,
+                     const float *kn) {
     StepLayer L;
     std::memset(&L, 0, sizeof L);
     for (int i = 0; i < 5; ++i) L.maps[i] = maps5[i];
     L.n1 = n1;
     L.n2 = n2;
+    L.qn = qn;
+    L.kn = kn;
     std::memcpy(dst, &L, sizeof L);
 }
 
@@ -1603,6 +1657,15 @@ int step_stages(int scratch_floats) {
     for (int s = kStMaxStages; s >= 2; --s)
         if (step_smem_bytes(s, scratch_floats) <= kStSmemLimit) return s;
     return 0;
+}
+
+// Stages in flight at most (see produce_all); DS_STEP_INFLIGHT overrides the
+// default, 0 meaning every free ring slot.
+int step_inflight_setting() {
+    int v = kStMaxInflight;
+    const char *e = std::getenv("DS_STEP_INFLIGHT");
+    if (e && *e) v = std::max(0, std::atoi(e));
+    return v;
 }
 
 template <typename T, typename KT, int GQ>

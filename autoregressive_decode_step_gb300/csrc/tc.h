@@ -46,6 +46,10 @@ struct TcArgs {
     int nq_cols, nkv_cols, head_dim, rope_layout;
     void *k_cache, *v_cache;
     int kv_dtype;
+    // TC_QKV: QK-norm before RoPE (null: none), every q / k head scaled by
+    // 1/sqrt(mean of its squares + qk_eps) and by these [head_dim] weights
+    const float *q_norm, *k_norm;
+    float qk_eps;
     // the sequence whose blocks row s addresses: row_seq[s], or s when null
     // (a prompt chunk of one sequence gives every row the same sequence)
     const int *row_seq;

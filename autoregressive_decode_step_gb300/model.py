@@ -48,7 +48,8 @@ class DecodeModel:
             mc.rope_high_freq_factor, mc.rope_orig_max_pos = sc["high_freq_factor"], sc["original_max_position"]
         self._mc = mc
         W = weights
-        self._arrays = {k: _ptr_array(W[k]) for k in ("n1", "wqkv", "wo", "n2", "wgu", "wd")}
+        names = ("n1", "wqkv", "wo", "n2", "wgu", "wd") + (("q_norm", "k_norm") if "q_norm" in W else ())
+        self._arrays = {k: _ptr_array(W[k]) for k in names}
         mw = abi.ModelWeights()
         mw.emb = W["emb"].data_ptr()
         mw.out = W["out"].data_ptr()

@@ -101,6 +101,16 @@ def model_weights(cfg, seed=0, device="cpu"):
     return W
 
 
+def qk_norm_weights(cfg, seed=0, device="cpu", std=0.3):
+    """Per-layer QK-norm weights (fp32 [head_dim], N(1, std)) as the
+    ``q_norm`` and ``k_norm`` lists of a weight dict."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    hd = cfg["head_dim"]
+    mk = lambda: torch.randn(hd, generator=g, device=device, dtype=torch.float32).mul_(std).add_(1.0)
+    return {"q_norm": [mk() for _ in range(cfg["n_layer"])], "k_norm": [mk() for _ in range(cfg["n_layer"])]}
+
+
 def to_numpy_storage(t):
     """A torch tensor as the oracle's numpy storage: float32, or uint16 bits
     for bf16."""

@@ -224,8 +224,9 @@ DS_API int ds_add_rmsnorm(float *residual, int64_t residual_len, const float *x,
 
 /* Rotate q (n_qh heads) and k (n_kh heads, may be NULL with n_kh = 0) of
  * head_dim values each, in place, to position `pos`: pair p turns by
- * pos * base^(-2p/head_dim), angles formed in fp64 for this call ("decode-ops",
- * "API — Method"), the rotation applied in fp32.  layout: DS_ROPE_*.
+ * pos * base^(-2p/head_dim), the head_dim/2 angles formed once per call in fp64
+ * on the host and rounded to fp32 ("decode-ops", "API — Method"), the rotation
+ * applied in fp32 on the device.  layout: DS_ROPE_*.
  * q_len must be n_qh*head_dim (562), k_len n_kh*head_dim (563); head_dim
  * even and <= 1024 (577); pos >= 0 (566). */
 DS_API int ds_rope(float *q, int64_t q_len, float *k, int64_t k_len, int64_t pos, int n_qh,
@@ -372,6 +373,14 @@ typedef struct {
     const float *const *n2;
     const void *const *wgu;
     const void *const *wd;
+    /* Optional QK-norm, as Qwen3 checkpoints define it (not on the pages):
+     * host arrays of n_layer device pointers to fp32 [head_dim] weights, or
+     * both NULL (no QK-norm; a zeroed struct has none).  Every q head is
+     * scaled by 1 / sqrt(mean of its head_dim squares + eps) and by q_norm,
+     * every k head likewise with k_norm, after the projection and before
+     * RoPE; v is untouched.  One set without the other: 577. */
+    const float *const *q_norm;
+    const float *const *k_norm;
 } ds_model_weights;
 
 /* The KV cache: per layer one K and one V buffer of rows of n_kvh*head_dim
