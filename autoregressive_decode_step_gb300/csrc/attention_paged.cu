@@ -5,8 +5,9 @@
 // end", "The code": forward_token's attention).
 //
 // The work is the list of every sequence's cache blocks (block_tokens = 16
-// positions), cut into equal contiguous ranges, one per CTA, so every CTA
-// streams the same number of K/V bytes whatever the mix of context lengths.
+// positions), cut into equal contiguous ranges, one per CTA (at most 32 CTAs
+// per sequence), so every CTA streams the same number of K/V bytes whatever
+// the mix of context lengths.
 // A block's K rows (16 positions x n_kvh heads x 128 dims) are contiguous in
 // the layer's K buffer, as are its V rows; a producer warp moves each with
 // one bulk asynchronous copy into a ring of shared-memory stages (K stage,
@@ -39,6 +40,10 @@ constexpr int kPaMaxKvh = 8;
 constexpr int kPaMaxSeqs = 256;
 constexpr size_t kPaSmemLimit = 227 * 1024 - 4096;  // dynamic part: the kernel has 3 KB of static shared memory
 constexpr int kPaRingBytes = 192 * 1024;
+// CTAs a launch spreads one sequence's blocks over at most: few sequences
+// with long contexts then take part of the grid, each CTA streaming more
+// blocks through its ring, and the merge of a sequence stays short
+constexpr int kPaMaxCtasPerSeq = 32;
 
 struct PaSeqs {
     int n_ctx[kPaMaxSeqs];
@@ -81,17 +86,40 @@ __device__ void pa_finish_sequence(const PagedAttnArgs &p, int s, int g, long lo
     __threadfence();
     for (int j = 0; j < GQ; ++j) {
         const int h = g * GQ + j;
+        auto rec_of = [&](int c) { return p.partials + ((size_t)c + s) * p.n_qh * rec + (size_t)h * rec; };
+        // the largest record max: lanes read contributors 32 apart, then a
+        // warp max (exact whatever the order)
         float M = -INFINITY;
-        for (int c = c_first; c <= c_last; ++c)
-            M = fmaxf(M, __ldcg(p.partials + ((size_t)c + s) * p.n_qh * rec + (size_t)h * rec));
+        for (int c = c_first + lane; c <= c_last; c += 32) M = fmaxf(M, __ldcg(rec_of(c)));
+        M = warp_max(M);
+        // sum and accumulator in CTA order, eight contributors' loads in flight
         float L = 0.0f, A[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int c = c_first; c <= c_last; ++c) {
-            const float *rr = p.partials + ((size_t)c + s) * p.n_qh * rec + (size_t)h * rec;
-            const float mc = __ldcg(rr);
-            const float w = mc == -INFINITY ? 0.0f : expf(mc - M);
-            L = fmaf(__ldcg(rr + 1), w, L);
+        for (int c0 = c_first; c0 <= c_last; c0 += 8) {
+            float mc[8], lc[8];
+            float4 ac[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) A[e] = fmaf(__ldcg(rr + 2 + lane * 4 + e), w, A[e]);
+            for (int k = 0; k < 8; ++k) {
+                mc[k] = -INFINITY;
+                lc[k] = 0.0f;
+                ac[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (c0 + k <= c_last) {
+                    const float *rr = rec_of(c0 + k);
+                    mc[k] = __ldcg(rr);
+                    lc[k] = __ldcg(rr + 1);
+                    ac[k] = make_float4(__ldcg(rr + 2 + lane * 4), __ldcg(rr + 3 + lane * 4), __ldcg(rr + 4 + lane * 4),
+                                        __ldcg(rr + 5 + lane * 4));
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (c0 + k > c_last) break;
+                const float w = mc[k] == -INFINITY ? 0.0f : expf(mc[k] - M);
+                L = fmaf(lc[k], w, L);
+                A[0] = fmaf(ac[k].x, w, A[0]);
+                A[1] = fmaf(ac[k].y, w, A[1]);
+                A[2] = fmaf(ac[k].z, w, A[2]);
+                A[3] = fmaf(ac[k].w, w, A[3]);
+            }
         }
         const long long o = ((long long)s * p.n_qh + h) * kPaHd + lane * 4;
 #pragma unroll
@@ -178,7 +206,7 @@ __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_kernel
     const long long T = sq.first[p.n_seqs];
     // only min(grid, blocks) CTAs take part, so that every one has a non-empty
     // range and the contributors to a sequence are consecutive CTAs
-    const int Ge = (int)min((long long)G, T);
+    const int Ge = (int)min(min((long long)G, T), (long long)p.n_seqs * kPaMaxCtasPerSeq);
     const bool in = (int)blockIdx.x < Ge;
     const long long u0 = in ? T * blockIdx.x / Ge : 0, u1 = in ? T * (blockIdx.x + 1) / Ge : 0;
     // the sequence holding unit u (sequences are in unit order)
@@ -488,7 +516,7 @@ __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_tc_ker
     }
     __syncthreads();
     const long long T = sq.first[p.n_seqs];
-    const int Ge = (int)min((long long)G, T);
+    const int Ge = (int)min(min((long long)G, T), (long long)p.n_seqs * kPaMaxCtasPerSeq);
     const bool in = (int)blockIdx.x < Ge;
     const long long u0 = in ? T * blockIdx.x / Ge : 0, u1 = in ? T * (blockIdx.x + 1) / Ge : 0;
     auto seq_of = [&](long long u) {

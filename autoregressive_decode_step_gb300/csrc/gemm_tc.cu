@@ -442,8 +442,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             // previous kernel's output is awaited
             long long u = u0;
             int pre = (int)std::min<long long>(stages, u1 - u0);
-            auto issue_a = [&](int s, long long unit) {
-                const int tile = (int)(unit / KB), kb = (int)(unit - (long long)tile * KB);
+            // the unit (tile, k-block) of every stage walked incrementally: no
+            // division per stage (the issuing thread's instruction count is on
+            // the critical path of the weight stream)
+            auto issue_a = [&](int s, int tile, int kb) {
                 for (int h = 0; h < MS; ++h) {
                     const int st = tile * MS + h;  // 128-feature sub-tile
                     unsigned char *sa = smem + (size_t)s * stage_bytes + h * kTcABytes;
@@ -460,31 +462,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                     }
                 }
             };
-            auto issue_b = [&](int s, long long unit) {
-                const int tile = (int)(unit / KB), kb = (int)(unit - (long long)tile * KB);
-                (void)tile;
+            auto issue_b = [&](int s, int kb) {
                 unsigned char *sb = smem + (size_t)s * stage_bytes + a_bytes;
                 tma_box_g2s_nohint(sb, &p.tb, kb * kTcBK, 0, &full[s]);
                 if (p.split) tma_box_g2s_nohint(sb + b_bytes, &p.tb, kb * kTcBK, p.b_lo_row, &full[s]);
             };
-            for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
-                issue_a(i, u0 + i);
+            const int tile0 = (int)(u0 / KB), kb0 = (int)(u0 - (long long)tile0 * KB);
+            {
+                int tile = tile0, kb = kb0;
+                for (int i = 0; i < pre; ++i) {
+                    mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
+                    issue_a(i, tile, kb);
+                    if (++kb == KB) {
+                        kb = 0;
+                        ++tile;
+                    }
+                }
             }
             grid_dependency_wait();
-            for (int i = 0; i < pre; ++i) issue_b(i, u0 + i);
+            {
+                int kb = kb0;
+                for (int i = 0; i < pre; ++i) {
+                    issue_b(i, kb);
+                    if (++kb == KB) kb = 0;
+                }
+            }
             uint32_t fill = (uint32_t)pre;
+            int tile = tile0, kb = kb0 + pre;
+            while (kb >= KB) {
+                kb -= KB;
+                ++tile;
+            }
+            int s = pre % stages;
+            uint32_t use = (uint32_t)(pre / stages);
             bool ok = true;
             for (u = u0 + pre; u < u1; ++u, ++fill) {
-                const int s = fill % stages;
-                const uint32_t use = fill / stages;
                 if (!tc_wait(&empty[s], (use - 1) & 1, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
-                issue_a(s, u);
-                issue_b(s, u);
+                issue_a(s, tile, kb);
+                issue_b(s, kb);
+                if (++kb == KB) {
+                    kb = 0;
+                    ++tile;
+                }
+                if (++s == stages) {
+                    s = 0;
+                    ++use;
+                }
             }
             // every copy issued has landed before the CTA may exit
             const uint32_t first = fill > (uint32_t)stages ? fill - stages : 0;
@@ -498,6 +525,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         if (lane == 0) {
             grid_dependency_wait();
             const uint32_t idesc = tc_idesc(A_MN, p.n_pad);
+            const bool split = p.split != 0;
+            const uint64_t b_lo_step = (uint64_t)(b_bytes >> 4);  // the lo activation tile, b_bytes further
             uint32_t fill = 0;
             int seg_i = 0;
             long long u = u0;
@@ -519,18 +548,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                         break;
                     }
                     tc_fence_after();
+                    // descriptors of this stage formed once; every 16-row step and
+                    // sub-tile only adds a constant to the 16-byte address field
+                    // (the issuing thread's instruction count bounds the MMA rate)
                     const uint32_t sa0 = smem_u32(smem + (size_t)s * stage_bytes);
-                    const uint32_t sb = sa0 + a_bytes;
+                    const uint64_t a0 = A_MN ? smem_desc(sa0, kTcABytes / 2, 1024) : smem_desc(sa0, 16, 1024);
+                    const uint64_t b0 = smem_desc(sa0 + a_bytes, 16, 1024);
+                    const uint32_t first = kb > sg.kb0 ? 1u : 0u;
 #pragma unroll
                     for (int k = 0; k < kTcBK / 16; ++k) {
-                        const uint64_t bd = smem_desc(sb + k * 32, 16, 1024);
-                        for (int h = 0; h < MS; ++h) {  // sub-tile h accumulates n_pad columns further
-                            const uint32_t sa = sa0 + h * kTcABytes;
-                            const uint64_t ad = A_MN ? smem_desc(sa + k * 2048, kTcABytes / 2, 1024)
-                                                     : smem_desc(sa + k * 32, 16, 1024);
-                            const uint32_t d = d_tmem + (uint32_t)(h * p.n_pad);
-                            tc_mma(d, ad, bd, idesc, (kb > sg.kb0 || k > 0) ? 1u : 0u);
-                            if (p.split) tc_mma(d, ad, smem_desc(sb + b_bytes + k * 32, 16, 1024), idesc, 1u);
+                        const uint64_t bd = b0 + (uint64_t)(k * 2);  // 32 bytes further per step
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (h < MS) {
+                                const uint64_t ad = a0 + (uint64_t)(h * (kTcABytes >> 4) + k * (A_MN ? 128 : 2));
+                                const uint32_t d = d_tmem + (uint32_t)(h * p.n_pad);
+                                tc_mma(d, ad, bd, idesc, (first | (uint32_t)k) ? 1u : 0u);
+                                if (split) tc_mma(d, ad, bd + b_lo_step, idesc, 1u);
+                            }
                         }
                     }
                     tc_commit(&empty[s]);
@@ -694,6 +729,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 // accumulator (the epilogue reads 32 columns at a time).
 int tc_n_pad(int n) { return std::max(32, (n + 31) / 32 * 32); }
 
+int tc_tmem_cols(int acc_bufs, int msub, int n_pad) {
+    int cols = 32;
+    while (cols < acc_bufs * msub * n_pad) cols *= 2;
+    return cols;
+}
+
 int tc_stages(int n_pad, int split, int msub) {
     const size_t stage = (size_t)msub * kTcABytes + (size_t)n_pad * kTcBK * 2 * (split ? 2 : 1);
     const size_t fixed = 1024 + 256 + kTcSmemInts * 4 + (size_t)kTcBM * (kTcXchStride + 1) * 4 + 64;
@@ -818,8 +859,7 @@ int tc_run(const void *A, const void *X, int64_t n, int64_t M, int64_t K, int a_
     a.acc_bufs = 2;
     a.m_tiles = tc_m_tiles(a.M, a.epi);
     a.stages = tc_stages(a.n_pad, 0, 1);
-    a.tmem_cols = 32;
-    while (a.tmem_cols < 2 * a.n_pad) a.tmem_cols *= 2;
+    a.tmem_cols = tc_tmem_cols(a.acc_bufs, a.msub, a.n_pad);
     a.y = Y;
     a.ldy = (int)M;
     if (!ws || ws_bytes < tc_ws_bytes(n, M, K, a.epi)) return DS_WORKSPACE_TOO_SMALL;

@@ -312,6 +312,7 @@ int step_scratch_floats(const ds_model_config *c, int grid, int nb_qkv, int nb_o
 bool step_supported(const ds_model_config *c);
 int step_stages(int scratch_floats);
 int step_inflight_setting();
+int step_stage_bytes();  // bytes of one ring stage of the step kernel
 size_t step_smem_bytes(int stages, int scratch_floats);
 cudaError_t launch_step(const void *params, int w_dtype, int kv_dtype, int gq, int grid, cudaStream_t stream);
 

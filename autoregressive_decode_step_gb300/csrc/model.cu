@@ -639,8 +639,7 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
             a.acc_bufs = 2 * a.msub * a.n_pad <= 512 ? 2 : 1;
             a.m_tiles = (tc_m_tiles(M, epi) + a.msub - 1) / a.msub;
             a.stages = tc_stages(a.n_pad, 1, a.msub);
-            a.tmem_cols = 32;
-            while (a.tmem_cols < a.acc_bufs * a.msub * a.n_pad) a.tmem_cols *= 2;
+            a.tmem_cols = tc_tmem_cols(a.acc_bufs, a.msub, a.n_pad);
             a.partials = reinterpret_cast<float *>(ws + L.tc_partials);
             a.counters = reinterpret_cast<int *>(ws + L.tc_counters);
             a.err = m->err;
@@ -740,7 +739,7 @@ int kv_stage_positions(const ds_model_config &c, int block_tokens) {
     const int es = c.kv_dtype == DS_BF16 ? 2 : 4;
     const int row = c.head_dim * es;
     if (row % 16 || c.head_dim > 128 || ((long long)c.n_kvh * row) % 16) return 0;
-    int P = std::min(256, 65536 / (2 * row)) / 64 * 64;
+    int P = std::min(256, step_stage_bytes() / (2 * row)) / 64 * 64;
     if (P < 64 || block_tokens < 1 || block_tokens > 256 || P % block_tokens) return 0;
     // every box of a block lands block_tokens * row bytes after the previous
     // one: tensor copies need 128-byte-aligned shared-memory destinations

@@ -6,21 +6,24 @@
 //   embed | per layer: q|k|v (RMSNorm prologue, RoPE + K/V write epilogue) |
 //   attention | o (+ residual) | gate|up (RMSNorm prologue, SiLU epilogue) |
 //   down (+ residual) | final RMSNorm + output head + greedy argmax.
-// Consumers meet at a grid barrier between phases (every phase needs the
-// whole output of the one before).  The producer warp never waits at those
-// barriers: weights do not depend on activations, so it streams the next
-// phase's weight boxes into the shared-memory ring while consumers finish a
-// phase, wait at a barrier or run attention.  The weight stream therefore
-// runs across phase boundaries without the drain and refill a kernel launch
-// per phase would cost.
+// Activations pass between phases as tagged 64-bit words (value + the phase
+// sequence number) that readers poll, so a CTA starts a phase as soon as the
+// slice of the previous phase's output it needs has arrived; there is no grid
+// barrier.  The producer warp never waits for activations: weights do not
+// depend on them, so it streams the next phase's weight boxes into the
+// shared-memory ring while consumers finish a phase, wait for their inputs
+// or run attention.  The weight stream therefore runs across phase
+// boundaries without the drain and refill a kernel launch per phase would
+// cost.
 //
 // Arithmetic per phase is the same as the standalone kernels': stream-K
-// ranges of 8-row x 512-byte tensor-map boxes for the transposed projections,
-// fixed-order cross-CTA reductions by the last CTA of each band, whole-row
-// bulk copies for the head.  Activations written by other CTAs are read
-// through L2 (ld.global.cg) so no stale L1 line is ever used.  Every wait is
-// bounded: a grid barrier or mbarrier that times out sets the error word and
-// an abort flag, after which the remaining phases run without waiting.
+// ranges of 16-row x 512-byte tensor-map boxes for the transposed projections,
+// fixed-order cross-CTA reductions by the CTA holding each band's last box,
+// whole-row bulk copies for the head.  Activations written by other CTAs are
+// read through L2 (ld.global.cg) so no stale L1 line is ever used.  Every wait is
+// bounded: a tagged-word poll or mbarrier wait that times out sets the error
+// word and an abort flag, after which the remaining phases run without
+// waiting.
 #include <algorithm>
 #include <climits>
 #include <cstdio>
@@ -1613,6 +1616,7 @@ void step_layer_fill(void *dst, const CUtensorMap *maps5, const float *n1, const
 }
 
 int step_max_layers() { return kStMaxLayers; }
+int step_stage_bytes() { return kStStageBytes; }
 int step_max_splits() { return kStMaxSplits; }
 
 // Shared-memory floats the consumers need after the ring, for a config.

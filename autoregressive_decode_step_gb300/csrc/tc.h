@@ -74,6 +74,9 @@ struct TcArgs {
 };
 
 int tc_n_pad(int n);
+// TMEM columns to allocate for acc_bufs accumulators of msub sub-tiles of
+// n_pad columns (a power of two, at least 32).
+int tc_tmem_cols(int acc_bufs, int msub, int n_pad);
 int tc_stages(int n_pad, int split, int msub);
 int tc_m_tiles(int M, int epi);
 int tc_grid(int m_tiles, int K);

@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--no-legs", action="store_true",
                    help="skip the extra batch-1 legs (8B at contexts 4096 and 8192, the Qwen3-0.6B shape, the tiny "
                         "decoder)")
+    p.add_argument("--ops-only", action="store_true",
+                   help="time only the op-level decode glue (a profiling case: no step, no CPU baseline)")
+    p.add_argument("--ops-reps", type=int, default=200, help="timed launches per op in the op-level leg")
     p.add_argument("--prompt-only", action="store_true",
                    help="time only the chunked prompt (stepSeq) leg (a profiling case)")
     p.add_argument("--batched-steps", type=int, default=None,
@@ -243,12 +246,8 @@ STEP_TRAFFIC = os.path.join(ROOT, "profiles", "step_kernel_llama3_8b.json")
 def kernel_source_sha():
     """sha256 over the sources of the persistent step kernel (the dominant
     kernel); the committed traffic record names the value it was taken on."""
-    import hashlib
-    h = hashlib.sha256()
-    for name in ("step.cu", "common.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "autoregressive_decode_step_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()
+    from autoregressive_decode_step_gb300.ncu_record import kernel_source_sha as sha
+    return sha()
 
 
 def traffic_ratio(kernel_src_sha):
@@ -585,6 +584,15 @@ def op_inputs():
                  synth.normal((n,), seed=3, mean=1.0, std=0.1))
     d["rope"] = (int(torch.randint(0, 8192, (1,), generator=torch.Generator().manual_seed(0))),
                  synth.normal((32 * 128,), seed=10), synth.normal((8 * 128,), seed=20))
+    # the output head of the 8B shape (bf16 [128,256][4096], 1.05 GB: larger
+    # than L2) and its normalised input
+    d["head"] = (synth.normal((128256, 4096), seed=50, std=0.02, dtype=torch.bfloat16), synth.normal((4096,), seed=51))
+    # one decode step's attention at 8192 cached positions: 32 q heads over
+    # 8 KV heads of 128, bf16 K/V (four caches of 33.6 MB rotated: larger
+    # than L2 together)
+    d["attn"] = ([(synth.normal((8192, 8 * 128), seed=60 + 2 * i, dtype=torch.bfloat16),
+                   synth.normal((8192, 8 * 128), seed=61 + 2 * i, dtype=torch.bfloat16)) for i in range(4)],
+                 synth.normal((32 * 128,), seed=70))
     V = 128256
     L = synth.normal((V,), seed=40)
     L[torch.randperm(V, generator=torch.Generator().manual_seed(41))[:3]] = float(L.max()) + 1.0
@@ -593,14 +601,17 @@ def op_inputs():
     return d
 
 
-OP_NAMES = ("gemv_transposed_4096x4096", "gemv_transposed_4096x14336", "add_rmsnorm_4096",
-            "rope_half_split_32q_8k_x128", "greedy_argmax_128256", "sample_t0.8_k50_p0.95_128256")
+OP_NAMES = ("gemv_transposed_4096x4096", "gemv_transposed_4096x14336", "gemv_head_128256x4096_bf16",
+            "add_rmsnorm_4096", "rope_half_split_32q_8k_x128", "gqa_decode_attn_32q_8kv_x128_ctx8192_bf16",
+            "greedy_argmax_128256", "sample_t0.8_k50_p0.95_128256")
 
 
 def op_bytes():
     V = 128256
     return {"gemv_transposed_4096x4096": 4096 * 4096 * 4 + 4096 * 4 * 2,
             "gemv_transposed_4096x14336": 4096 * 14336 * 4 + (4096 + 14336) * 4,
+            "gemv_head_128256x4096_bf16": 128256 * 4096 * 2 + 4096 * 4 + 128256 * 4,
+            "gqa_decode_attn_32q_8kv_x128_ctx8192_bf16": 2 * 8192 * 8 * 128 * 2 + 2 * 32 * 128 * 4,
             "add_rmsnorm_4096": 5 * 4096 * 4,
             "rope_half_split_32q_8k_x128": 2 * 40 * 128 * 4,
             "greedy_argmax_128256": V * 4, "sample_t0.8_k50_p0.95_128256": V * 4}
@@ -608,28 +619,35 @@ def op_bytes():
 
 def run_ops(dev, reps=200, warmup=5):
     """The decode glue one op at a time at the pages' op-level sizes, through
-    the C ABI: each op's device time per launch over `reps` launches between
-    CUDA events on the launching stream after `warmup` launches, and its
-    algorithmic bytes over that time."""
+    the C ABI: each op's device time per launch, `reps` launches captured in
+    a CUDA graph (after `warmup` eager launches) and the replay timed between
+    CUDA events on the replaying stream (so the host's per-call cost is not
+    in the number), and its algorithmic bytes over that time."""
     import torch
 
     from autoregressive_decode_step_gb300 import abi as A
 
-    stream = torch.cuda.current_stream(dev)
     d = op_inputs()
     us = {}
 
     def gpu_us(fn):
         for i in range(warmup):
             fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                fn(i)
+        stream = torch.cuda.current_stream(dev)
+        g.replay()
         stream.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(reps):
-            fn(i)
+        g.replay()
         e1.record(stream)
         e1.synchronize()
+        del g
         return e0.elapsed_time(e1) * 1e3 / reps
 
     for rows, cols in ((4096, 4096), (4096, 14336)):
@@ -642,6 +660,22 @@ def run_ops(dev, reps=200, warmup=5):
             lambda i: A.ds_gemv_transposed(mats_d[i % 3], xd, rows, cols, y, ws))
         del mats_d
         torch.cuda.empty_cache()
+    W, x = (t.to(dev) for t in d["head"])
+    y = torch.empty(128256, device=dev)
+    us["gemv_head_128256x4096_bf16"] = gpu_us(lambda i: A.ds_gemv(W, x, 128256, 4096, y))
+    del W
+    torch.cuda.empty_cache()
+    caches, q = d["attn"]
+    caches = [(k.to(dev), v.to(dev)) for k, v in caches]
+    q = q.to(dev)
+    att = torch.empty(32 * 128, device=dev)
+    lens = torch.tensor([8192], dtype=torch.int32, device=dev)
+    ws = A.workspace(A.ds_attention_workspace_bytes(1, 32, 8, 128, 8192), dev)
+    us["gqa_decode_attn_32q_8kv_x128_ctx8192_bf16"] = gpu_us(
+        lambda i: A.ds_gqa_decode_attn(q, caches[i % 4][0], caches[i % 4][1], 8192, None, 512, 16, lens, 1, 32, 8,
+                                       128, 1.0 / 128 ** 0.5, att, ws))
+    del caches
+    torch.cuda.empty_cache()
     r, x, w = (t.to(dev) for t in d["norm"])
     h = torch.empty(4096, device=dev)
     us["add_rmsnorm_4096"] = gpu_us(lambda i: A.ds_add_rmsnorm(r, x, w, 1e-5, h, 4096))
@@ -663,7 +697,8 @@ def run_ops(dev, reps=200, warmup=5):
                     for k, v in us.items()},
             "reps": reps, "warmup": warmup,
             "workload": "op-level decode glue, fp32, seeded N(0,1) inputs at the pages' measured sizes; the "
-                        "GEMVs rotate three weight copies (larger than L2 together)"}
+                        "GEMVs rotate three weight copies and the attention four caches (larger than L2 together); "
+                        "device time per launch from a replayed CUDA graph of the launches"}
 
 
 def oracle_op_times(threads=None):
@@ -672,6 +707,9 @@ def oracle_op_times(threads=None):
     in microseconds."""
     import oracle as O
 
+    from autoregressive_decode_step_gb300 import synth
+
+    synth_np = synth.to_numpy_storage
     d = op_inputs()
     out = {}
     before = O.threads()
@@ -692,6 +730,13 @@ def oracle_op_times(threads=None):
         a_np, x_np = mats[0].numpy(), x.double().numpy()
         out["gemv_transposed_%dx%d" % (rows, cols)] = best_us(
             lambda: O.gemv_transposed(a_np, x_np, rows, cols, O.DT_F32))
+    W, x = d["head"]
+    w_np, xh = synth_np(W), x.double().numpy()
+    out["gemv_head_128256x4096_bf16"] = best_us(lambda: O.gemv(w_np, xh, 128256, 4096, O.DT_BF16), min_calls=1)
+    caches, q = d["attn"]
+    k_np, v_np, q_np = synth_np(caches[0][0]), synth_np(caches[0][1]), q.double().numpy()
+    out["gqa_decode_attn_32q_8kv_x128_ctx8192_bf16"] = best_us(
+        lambda: O.gqa_attention(q_np, k_np, v_np, O.DT_BF16, 8192, 32, 8, 128, 1.0 / 128 ** 0.5), min_calls=1)
     r, x, w = (t.numpy() for t in d["norm"])
     out["add_rmsnorm_4096"] = best_us(lambda: O.add_rmsnorm(r, x, w, 1e-5, O.DT_F32))
     pos, q, k = d["rope"]
@@ -718,6 +763,10 @@ def run_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.ops_only:
+        if rank == 0:
+            print(json.dumps({"ops": run_ops(dev, reps=args.ops_reps, warmup=min(5, args.ops_reps))}), flush=True)
+        return 0
     cfg = dict(C.LLAMA3_8B)
     if args.layers is not None:
         cfg["n_layer"] = args.layers
@@ -927,7 +976,7 @@ def run_ours(args, rank, world, local):
             line["toy"] = {"error": "%s: %s" % (type(e).__name__, e)}
     if args.layers is None and not args.no_ops:
         try:
-            line["ops"] = run_ops(dev)
+            line["ops"] = run_ops(dev, reps=args.ops_reps)
         except Exception as e:  # reported in the line, never fatal to the step's numbers
             line["ops"] = {"error": "%s: %s" % (type(e).__name__, e)}
         if rank == 0 and world == 1 and not args.no_cpu_baseline and "ops" in line["ops"]:

@@ -4,9 +4,10 @@ through the C ABI.
 The no-allocation variant is for callers that cannot allocate device memory
 (their device memory belongs to another allocator, or they receive only an
 operation's inputs and outputs); its split-reduction scratch lives in a fixed
-area inside the library.  This file is collected last so that a run stopping
-at the first failure has already run every other test, and it must pass both
-on its own in a fresh process and after the rest of the suite.
+area inside the library.  Its tests are marked run_last (the suite's conftest
+moves them to the end of the run) so that a run stopping at the first failure
+has already run every other test; they must pass both on their own in a fresh
+process and after the rest of the suite.
 """
 import numpy as np
 import pytest
@@ -16,7 +17,7 @@ import oracle as O
 from autoregressive_decode_step_gb300 import synth
 from tests.gpu_util import FP32_TOL, host, rel_err
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.run_last]
 
 
 @pytest.fixture(scope="module")
