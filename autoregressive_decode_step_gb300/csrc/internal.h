@@ -301,6 +301,8 @@ struct StepParams {
     int kv_stage_pos;       // positions per K/V stage
     int scratch_floats;     // shared scratch after the ring
     int max_inflight;       // weight stages requested and not yet landed at most (0: no cap)
+    int chain_inflight;     // the same while the attention chain runs (o and K/V stages; 0: max_inflight)
+    int chain_gu_stages;    // first gate|up stages issued under chain_inflight
     void *kc[kStMaxLayers];
     void *vc[kStMaxLayers];
 };
@@ -312,6 +314,7 @@ int step_scratch_floats(const ds_model_config *c, int grid, int nb_qkv, int nb_o
 bool step_supported(const ds_model_config *c);
 int step_stages(int scratch_floats);
 int step_inflight_setting();
+void step_chain_setting(int *cap, int *gu_stages);
 int step_stage_bytes();  // bytes of one ring stage of the step kernel
 size_t step_smem_bytes(int stages, int scratch_floats);
 cudaError_t launch_step(const void *params, int w_dtype, int kv_dtype, int gq, int grid, cudaStream_t stream);

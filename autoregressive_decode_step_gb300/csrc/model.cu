@@ -54,6 +54,7 @@ struct ds_model {
     bool step_ok;
     int step_grid, step_splits, step_stages, step_scratch;
     int step_inflight;  // weight stages in flight at most (0: no cap)
+    int step_chain_inflight, step_chain_gu;  // the cap during the attention chain
     ds::StepLayer *step_layers;
     unsigned *step_bar;
     int *step_abort;
@@ -591,6 +592,7 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
     m->step_stages = L.step_stages;
     m->step_scratch = L.step_scratch;
     m->step_inflight = step_inflight_setting();
+    step_chain_setting(&m->step_chain_inflight, &m->step_chain_gu);
     m->step_layers = reinterpret_cast<StepLayer *>(ws + L.step_layers);
     m->kv_maps_dev = reinterpret_cast<CUtensorMap *>(ws + L.kv_maps);
     m->step_bar = reinterpret_cast<unsigned *>(ws + L.step_bar);
@@ -849,6 +851,8 @@ int run_step_fused(ds_model *m, const ds_kv_cache *kv, int32_t *tokens, int32_t 
     p.kv_align = p.kv_tma ? std::max(8, kv->block_tokens) : 1;
     p.scratch_floats = m->step_scratch;
     p.max_inflight = m->step_inflight;
+    p.chain_inflight = m->step_chain_inflight;
+    p.chain_gu_stages = m->step_chain_gu;
     for (int l = 0; l < c.n_layer; ++l) {
         p.kc[l] = kv->k[l];
         p.vc[l] = kv->v[l];

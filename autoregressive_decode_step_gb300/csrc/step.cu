@@ -61,6 +61,14 @@ constexpr size_t kStSmemLimit = 227 * 1024;
 #define DS_ST_MAX_INFLIGHT 2
 #endif
 constexpr int kStMaxInflight = DS_ST_MAX_INFLIGHT;  // weight stages requested and not landed (0: no cap)
+#ifndef DS_ST_CHAIN_INFLIGHT
+#define DS_ST_CHAIN_INFLIGHT 1
+#endif
+#ifndef DS_ST_CHAIN_GU_STAGES
+#define DS_ST_CHAIN_GU_STAGES 3
+#endif
+constexpr int kStChainInflight = DS_ST_CHAIN_INFLIGHT;  // the cap during the attention chain (0: the plain cap)
+constexpr int kStChainGuStages = DS_ST_CHAIN_GU_STAGES;  // first gate|up stages counted as chain stages
 
 __device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
 
@@ -347,11 +355,18 @@ __device__ void produce_all(const Ring &r, const StepParams &p) {
     const int pos0 = __ldcg(p.pos);
     const int cap = p.max_blocks * p.block_tokens;
     const uint32_t inflight = p.max_inflight > 0 && p.max_inflight < r.stages ? (uint32_t)p.max_inflight : 0u;
+    // stages requested while the consumers run the attention chain (the o
+    // projection's and cached K/V stages, and the first p.chain_gu_stages of
+    // gate|up): fewer bytes in flight there keep the hand-off polls fast, and
+    // the ring fills before the chain ends either way
+    const uint32_t inflight_chain =
+        p.chain_inflight > 0 && p.chain_inflight < r.stages ? (uint32_t)p.chain_inflight : inflight;
     for (int step = 0; step < p.n_steps && ok; ++step) {  // weights do not depend on the token
         StageCursor fc;
         fc.n_ctx = min(max(pos0 + step + 1, 1), cap);
         cursor_begin<ES>(fc, p);
         StageDesc d;
+        int cur_ph = -1, ph_stage = 0;
         while (cursor_desc<ES>(fc, p, d)) {
             const int s = fill % r.stages;
             const uint32_t use = fill / r.stages;
@@ -359,8 +374,13 @@ __device__ void produce_all(const Ring &r, const StepParams &p) {
                 ok = false;
                 break;
             }
-            if (inflight && fill >= inflight) {  // stage fill - inflight has landed (its slot is not yet reused)
-                const uint32_t f = fill - inflight;
+            const int ph_now = d.head ? 5 : fc.ph;
+            ph_stage = ph_now == cur_ph ? ph_stage + 1 : 0;
+            cur_ph = ph_now;
+            const bool chain = ph_now == 1 || ph_now == 4 || (ph_now == 2 && ph_stage < p.chain_gu_stages);
+            const uint32_t cap_now = chain ? inflight_chain : inflight;
+            if (cap_now && fill >= cap_now) {  // stage fill - cap has landed (its slot is not yet reused)
+                const uint32_t f = fill - cap_now;
                 if (!st_wait(&r.full[f % r.stages], (f / r.stages) & 1, p)) {
                     ok = false;
                     break;
@@ -1670,6 +1690,20 @@ int step_inflight_setting() {
     const char *e = std::getenv("DS_STEP_INFLIGHT");
     if (e && *e) v = std::max(0, std::atoi(e));
     return v;
+}
+
+// The cap while the attention chain runs, and the gate|up stages it covers;
+// DS_STEP_CHAIN_INFLIGHT="cap,gate_up_stages" overrides (cap 0: the plain cap).
+void step_chain_setting(int *cap, int *gu_stages) {
+    *cap = kStChainInflight;
+    *gu_stages = kStChainGuStages;
+    const char *e = std::getenv("DS_STEP_CHAIN_INFLIGHT");
+    if (e && *e) {
+        int c = 0, g = kStChainGuStages;
+        const int n = std::sscanf(e, "%d,%d", &c, &g);
+        if (n >= 1) *cap = std::max(0, c);
+        if (n >= 2) *gu_stages = std::max(0, g);
+    }
 }
 
 template <typename T, typename KT, int GQ>
