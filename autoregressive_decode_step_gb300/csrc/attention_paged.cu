@@ -43,7 +43,10 @@ constexpr int kPaRingBytes = 192 * 1024;
 // CTAs a launch spreads one sequence's blocks over at most: few sequences
 // with long contexts then take part of the grid, each CTA streaming more
 // blocks through its ring, and the merge of a sequence stays short
-constexpr int kPaMaxCtasPerSeq = 32;
+#ifndef DS_PA_MAX_CTAS_PER_SEQ
+#define DS_PA_MAX_CTAS_PER_SEQ 32
+#endif
+constexpr int kPaMaxCtasPerSeq = DS_PA_MAX_CTAS_PER_SEQ;
 
 struct PaSeqs {
     int n_ctx[kPaMaxSeqs];

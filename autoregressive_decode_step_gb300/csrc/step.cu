@@ -58,7 +58,7 @@ constexpr int kStMergeBatch = 20;
 constexpr int kStBoxesPerStage = kStStageBytes / (kStBoxRows * kStBandBytes);  // 8 boxes of 16 rows at 64 KB
 constexpr size_t kStSmemLimit = 227 * 1024;
 #ifndef DS_ST_MAX_INFLIGHT
-#define DS_ST_MAX_INFLIGHT 2
+#define DS_ST_MAX_INFLIGHT 0
 #endif
 constexpr int kStMaxInflight = DS_ST_MAX_INFLIGHT;  // weight stages requested and not landed (0: no cap)
 #ifndef DS_ST_CHAIN_INFLIGHT
