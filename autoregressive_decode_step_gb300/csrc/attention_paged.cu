@@ -5,9 +5,9 @@
 // end", "The code": forward_token's attention).
 //
 // The work is the list of every sequence's cache blocks (block_tokens = 16
-// positions), cut into equal contiguous ranges, one per CTA (at most 32 CTAs
-// per sequence), so every CTA streams the same number of K/V bytes whatever
-// the mix of context lengths.
+// positions), cut into equal contiguous ranges, one per CTA (about 16 blocks
+// a CTA, 8 to 64 CTAs per sequence), so every CTA streams the same number of
+// K/V bytes whatever the mix of context lengths.
 // A block's K rows (16 positions x n_kvh heads x 128 dims) are contiguous in
 // the layer's K buffer, as are its V rows; a producer warp moves each with
 // one bulk asynchronous copy into a ring of shared-memory stages (K stage,
@@ -40,13 +40,22 @@ constexpr int kPaMaxKvh = 8;
 constexpr int kPaMaxSeqs = 256;
 constexpr size_t kPaSmemLimit = 227 * 1024 - 4096;  // dynamic part: the kernel has 3 KB of static shared memory
 constexpr int kPaRingBytes = 192 * 1024;
-// CTAs a launch spreads one sequence's blocks over at most: few sequences
-// with long contexts then take part of the grid, each CTA streaming more
-// blocks through its ring, and the merge of a sequence stays short
-#ifndef DS_PA_MAX_CTAS_PER_SEQ
-#define DS_PA_MAX_CTAS_PER_SEQ 32
-#endif
-constexpr int kPaMaxCtasPerSeq = DS_PA_MAX_CTAS_PER_SEQ;
+// Bounds on the CTAs a launch spreads its blocks over (pa_ctas)
+constexpr int kPaMinCtasPerSeq = 8;
+constexpr int kPaMaxCtasPerSeq = 64;
+constexpr int kPaBlocksPerCta = 16;
+
+// CTAs a launch over n_seqs sequences of T blocks in all takes part with:
+// about kPaBlocksPerCta blocks per CTA, at least kPaMinCtasPerSeq and at most
+// kPaMaxCtasPerSeq per sequence, at most the grid (few sequences then keep
+// the merge of their per-CTA records short; many fill the grid).
+__device__ __forceinline__ int pa_ctas(int G, long long T, int n_seqs) {
+    long long g = T / kPaBlocksPerCta;
+    g = max(g, (long long)n_seqs * kPaMinCtasPerSeq);
+    g = min(g, (long long)n_seqs * kPaMaxCtasPerSeq);
+    g = min(g, T);
+    return (int)max(1ll, min(g, (long long)G));
+}
 
 struct PaSeqs {
     int n_ctx[kPaMaxSeqs];
@@ -209,7 +218,7 @@ __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_kernel
     const long long T = sq.first[p.n_seqs];
     // only min(grid, blocks) CTAs take part, so that every one has a non-empty
     // range and the contributors to a sequence are consecutive CTAs
-    const int Ge = (int)min(min((long long)G, T), (long long)p.n_seqs * kPaMaxCtasPerSeq);
+    const int Ge = pa_ctas(G, T, p.n_seqs);
     const bool in = (int)blockIdx.x < Ge;
     const long long u0 = in ? T * blockIdx.x / Ge : 0, u1 = in ? T * (blockIdx.x + 1) / Ge : 0;
     // the sequence holding unit u (sequences are in unit order)
@@ -519,7 +528,7 @@ __global__ void __launch_bounds__(kPaMaxKvh * 32 + 32, 1) paged_attention_tc_ker
     }
     __syncthreads();
     const long long T = sq.first[p.n_seqs];
-    const int Ge = (int)min(min((long long)G, T), (long long)p.n_seqs * kPaMaxCtasPerSeq);
+    const int Ge = pa_ctas(G, T, p.n_seqs);
     const bool in = (int)blockIdx.x < Ge;
     const long long u0 = in ? T * blockIdx.x / Ge : 0, u1 = in ? T * (blockIdx.x + 1) / Ge : 0;
     auto seq_of = [&](long long u) {
