@@ -165,7 +165,10 @@ __device__ __forceinline__ bool tc_next_seg(long long &u, long long u1, int KB, 
     return true;
 }
 
-__device__ __forceinline__ float silu_tc(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z / (1 + e^-z); the quotient as an approximate reciprocal times
+// z (two ulps at most: no per-item branch to a division slow path in the
+// epilogue's unrolled loops).  1 + e^-z >= 1, and an infinite e^-z gives -0.
+__device__ __forceinline__ float silu_tc(float z) { return __fdividef(z, 1.0f + expf(-z)); }
 
 // The residual values (TC_ADD) of one chunk for the tile's feature of this
 // thread, requested before the chunk's sums are waited for.
@@ -289,86 +292,187 @@ __device__ void tc_epilogue_chunk(const TcArgs &p, int tile, int chunk, const fl
         }
         return;
     } else {
-    // SILU and QKV exchange values between partner features through shared
-    // memory, scaled by the folded RMSNorm (1 where there is none)
+    // SILU and QKV exchange values between features through shared memory,
+    // scaled by the folded RMSNorm (1 where there is none); then thread
+    // (warp q, lane i) of the four takes vector j0 + i and a run of
+    // consecutive features, so its items are independent of one another and
+    // its outputs leave as a few 16-byte stores
 #pragma unroll
     for (int i = 0; i < 32; ++i) xch[r * kTcXchStride + i] = v[i] * s_scale[j0 + i];
     named_sync(1, kTcEpiThreads);
+    const int lane = r & 31, q = r >> 5;
+    const int j = j0 + lane;
     if constexpr (EPI == TC_SILU) {
-        const int g = tile * (kTcBM / 2) + r;
-        if (r < kTcBM / 2 && g < p.M) {
-#pragma unroll 8
-            for (int i = 0; i < 32; ++i) {
-                const int j = j0 + i;
-                if (j < p.n) {
-                    const float gate = xch[r * kTcXchStride + i], up = xch[(r + kTcBM / 2) * kTcXchStride + i];
-                    const float f = silu_tc(gate) * up;
-                    const long long o = (long long)j * p.ldy + g;
-                    if (p.yb_lo) {
-                        __nv_bfloat16 hi, lo;
-                        split_bf16(f, hi, lo);
-                        p.yb[o] = hi;
-                        p.yb[o + p.yb_lo] = lo;
-                    } else {
-                        p.yb[o] = __float2bfloat16_rn(f);
-                    }
+        // gate features 16 q .. 16 q + 15 of the tile's 64 (rows f of the
+        // exchange buffer; their up features are rows f + 64)
+        constexpr int kF = kTcBM / 8;
+        const int f0 = q * kF, g0 = tile * (kTcBM / 2) + f0;
+        if (j < p.n && g0 < p.M) {
+            float f[kF];
+#pragma unroll
+            for (int k = 0; k < kF; ++k) {
+                const float gate = xch[(f0 + k) * kTcXchStride + lane];
+                const float up = xch[(f0 + k + kTcBM / 2) * kTcXchStride + lane];
+                f[k] = silu_tc(gate) * up;
+            }
+            __nv_bfloat16 *dst = p.yb + (long long)j * p.ldy + g0;
+            const bool vec = g0 + kF <= p.M && (reinterpret_cast<uintptr_t>(dst) & 15) == 0 && (p.yb_lo & 7) == 0;
+            __nv_bfloat16 hi[kF], lo[kF];
+#pragma unroll
+            for (int k = 0; k < kF; ++k) {
+                if (p.yb_lo) {
+                    split_bf16(f[k], hi[k], lo[k]);
+                } else {
+                    hi[k] = __float2bfloat16_rn(f[k]);
+                    lo[k] = hi[k];
                 }
+            }
+            if (vec) {
+#pragma unroll
+                for (int k = 0; k < kF; k += 8) {
+                    *reinterpret_cast<uint4 *>(dst + k) = pack8_bf16(hi + k);
+                    if (p.yb_lo) *reinterpret_cast<uint4 *>(dst + p.yb_lo + k) = pack8_bf16(lo + k);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kF; ++k)
+                    if (g0 + k < p.M) {
+                        dst[k] = hi[k];
+                        if (p.yb_lo) dst[k + p.yb_lo] = lo[k];
+                    }
             }
         }
     } else {
-        const int m = tile * kTcBM + r;
-        const int total = p.nq_cols + 2 * p.nkv_cols;
-        if (p.q_norm) tc_qk_norm(p, m, r, xch);
-        if (m < total) {
-            const bool rot = m < p.nq_cols + p.nkv_cols;
+        if (p.q_norm) tc_qk_norm(p, tile * kTcBM + r, r, xch);
+        // features 32 q .. 32 q + 31 of the tile: q columns, then k, then v
+        constexpr int kF = kTcBM / 4;
+        const int f0 = q * kF, m0 = tile * kTcBM + f0;
+        const int nq = p.nq_cols, nkv = p.nkv_cols, total = nq + 2 * nkv;
+        if (j < p.n && m0 < total) {
+            const int pos = s_row[kTcMaxN + j], row = s_row[j];
+            const bool pos_ok = pos >= 0 && pos < p.rope_rows;
             const int hd = p.head_dim, half = hd >> 1;
-            const int ih = (m < p.nq_cols ? m : m - p.nq_cols) % hd;
-            int pair = 0, partner = r;
-            bool first = true;
-            if (rot) {
-                if (p.rope_layout == DS_ROPE_HALF_SPLIT) {
-                    first = ih < half;
-                    pair = first ? ih : ih - half;
-                    partner = first ? r + half : r - half;
-                } else {
-                    first = (ih & 1) == 0;
-                    pair = ih >> 1;
-                    partner = r ^ 1;
-                }
-            }
-            const int nj = min(32, p.n - j0);
-            // the chunk's rotation angles, loaded together before any use
-            float cs[32], sn[32];
+            const bool split_layout = p.rope_layout == DS_ROPE_HALF_SPLIT;
+            float out[kF];
+            // the run's region (q, k or v columns) and place in its head: with
+            // hd a multiple of 32 the run lies inside one head (and, half-split
+            // with hd >= 64, inside one half of it), so the rotation pairs and
+            // partner features follow from the run's first feature
+            const int base = m0 < nq ? 0 : (m0 < nq + nkv ? nq : nq + nkv);
+            const int rend = m0 < nq ? nq : (m0 < nq + nkv ? nq + nkv : total);
+            const bool whole_run = m0 + kF <= rend && hd % kF == 0 && (!split_layout || half % kF == 0);
+            if (whole_run) {
+                const int ih0 = (m0 - base) % hd;
+                if (!pos_ok || base == nq + nkv) {  // v columns (or no angle): as they are
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                cs[i] = 1.0f;
-                sn[i] = 0.0f;
-                if (rot && i < nj) {
-                    const int pos = s_row[kTcMaxN + j0 + i];
-                    if (pos >= 0 && pos < p.rope_rows) {
-                        cs[i] = __ldg(p.rope_cos + (long long)pos * half + pair);
-                        sn[i] = __ldg(p.rope_sin + (long long)pos * half + pair);
+                    for (int k = 0; k < kF; ++k) out[k] = xch[(f0 + k) * kTcXchStride + lane];
+                } else {
+                    // the run's angles: pairs pair0 .. (half-split) or pair0 .. pair0 + 15 (interleaved)
+                    const bool first_half = ih0 < half;
+                    const int pair0 = split_layout ? (first_half ? ih0 : ih0 - half) : ih0 >> 1;
+                    constexpr int kA = kF;  // angles loaded (the interleaved layout uses the first kF / 2)
+                    const int na = split_layout ? kF : kF / 2;
+                    const float *cp = p.rope_cos + (long long)pos * half + pair0;
+                    const float *sp = p.rope_sin + (long long)pos * half + pair0;
+                    float cs[kA], sn[kA];
+                    if (((reinterpret_cast<uintptr_t>(cp) | reinterpret_cast<uintptr_t>(sp)) & 15) == 0) {
+#pragma unroll
+                        for (int k = 0; k < kA; k += 4) {
+                            if (k < na) {
+                                const float4 c4 = __ldg(reinterpret_cast<const float4 *>(cp + k));
+                                const float4 s4 = __ldg(reinterpret_cast<const float4 *>(sp + k));
+                                cs[k] = c4.x; cs[k + 1] = c4.y; cs[k + 2] = c4.z; cs[k + 3] = c4.w;
+                                sn[k] = s4.x; sn[k + 1] = s4.y; sn[k + 2] = s4.z; sn[k + 3] = s4.w;
+                            } else {
+                                cs[k] = cs[k + 1] = cs[k + 2] = cs[k + 3] = 1.0f;
+                                sn[k] = sn[k + 1] = sn[k + 2] = sn[k + 3] = 0.0f;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kA; ++k) {
+                            cs[k] = k < na ? __ldg(cp + k) : 1.0f;
+                            sn[k] = k < na ? __ldg(sp + k) : 0.0f;
+                        }
+                    }
+                    if (split_layout) {
+                        const int pf0 = first_half ? f0 + half : f0 - half;  // the partner run
+#pragma unroll
+                        for (int k = 0; k < kF; ++k) {
+                            const float x = xch[(f0 + k) * kTcXchStride + lane];
+                            const float o = xch[(pf0 + k) * kTcXchStride + lane];
+                            out[k] = first_half ? x * cs[k] - o * sn[k] : o * sn[k] + x * cs[k];
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kF; ++k) {
+                            const float x = xch[(f0 + k) * kTcXchStride + lane];
+                            const float o = xch[(f0 + (k ^ 1)) * kTcXchStride + lane];
+                            out[k] = (k & 1) == 0 ? x * cs[k >> 1] - o * sn[k >> 1] : o * sn[k >> 1] + x * cs[k >> 1];
+                        }
                     }
                 }
-            }
+            } else {
+                // narrow heads or a run across regions: one item at a time,
+                // every item's inputs loaded before any output is stored
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int j = j0 + i;
-                if (i >= nj) break;
-                float out = xch[r * kTcXchStride + i];
-                const int row = s_row[j0 + i];
-                if (rot) {
-                    const float o = xch[partner * kTcXchStride + i];
-                    out = first ? out * cs[i] - o * sn[i] : o * sn[i] + out * cs[i];
+                for (int k = 0; k < kF; ++k) {
+                    const int m = m0 + k, f = f0 + k;
+                    const float x = xch[f * kTcXchStride + lane];
+                    const bool rot = pos_ok && m < nq + nkv;
+                    const int ih = (m < nq ? m : m - nq) % hd;
+                    const bool first = split_layout ? ih < half : (ih & 1) == 0;
+                    const int pair = split_layout ? (first ? ih : ih - half) : ih >> 1;
+                    const int partner = split_layout ? (first ? f + half : f - half) : f ^ 1;
+                    float cs = 1.0f, sn = 0.0f, o = 0.0f;
+                    if (rot) {
+                        cs = __ldg(p.rope_cos + (long long)pos * half + pair);
+                        sn = __ldg(p.rope_sin + (long long)pos * half + pair);
+                        o = xch[partner * kTcXchStride + lane];
+                    }
+                    out[k] = rot ? (first ? x * cs - o * sn : o * sn + x * cs) : x;
                 }
-                if (m < p.nq_cols) {
-                    p.y[(long long)j * p.ldy + m] = out;
-                } else if (row >= 0) {
-                    const int kv = m - p.nq_cols;
-                    if (kv < p.nkv_cols)
-                        store_as(p.k_cache, (long long)row * p.nkv_cols + kv, p.kv_dtype, out);
-                    else
-                        store_as(p.v_cache, (long long)row * p.nkv_cols + kv - p.nkv_cols, p.kv_dtype, out);
+            }
+            if (m0 + kF <= nq) {  // q columns only: fp32 to the q rows
+                float *dst = p.y + (long long)j * p.ldy + m0;
+                if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+                    for (int k = 0; k < kF; k += 4)
+                        *reinterpret_cast<float4 *>(dst + k) = make_float4(out[k], out[k + 1], out[k + 2], out[k + 3]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < kF; ++k) dst[k] = out[k];
+                }
+            } else if (m0 >= nq && row >= 0 && ((m0 + kF <= nq + nkv) || (m0 >= nq + nkv && m0 + kF <= total)) &&
+                       p.kv_dtype == DS_BF16) {
+                // one cache's columns only, bf16: to the position's cache row
+                const bool is_k = m0 < nq + nkv;
+                const int c0 = is_k ? m0 - nq : m0 - nq - nkv;
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(is_k ? p.k_cache : p.v_cache) +
+                                     (long long)row * nkv + c0;
+                __nv_bfloat16 b[kF];
+#pragma unroll
+                for (int k = 0; k < kF; ++k) b[k] = __float2bfloat16_rn(out[k]);
+                if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+                    for (int k = 0; k < kF; k += 8) *reinterpret_cast<uint4 *>(dst + k) = pack8_bf16(b + k);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < kF; ++k) dst[k] = b[k];
+                }
+            } else {  // a run that straddles q / k / v, or an fp32 cache: one item at a time
+#pragma unroll
+                for (int k = 0; k < kF; ++k) {
+                    const int m = m0 + k;
+                    if (m < nq) {
+                        p.y[(long long)j * p.ldy + m] = out[k];
+                    } else if (m < total && row >= 0) {
+                        const int kv = m - nq;
+                        if (kv < nkv)
+                            store_as(p.k_cache, (long long)row * nkv + kv, p.kv_dtype, out[k]);
+                        else
+                            store_as(p.v_cache, (long long)row * nkv + kv - nkv, p.kv_dtype, out[k]);
+                    }
                 }
             }
         }

@@ -90,6 +90,14 @@ __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16 &hi, __nv_bflo
     hi = __float2bfloat16_rn(v);
     lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
+// Eight bf16 values as one 16-byte word, b[0] at the lowest address.
+__device__ __forceinline__ uint4 pack8_bf16(const __nv_bfloat16 *b) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        w[k] = (uint32_t)__bfloat16_as_ushort(b[2 * k]) | ((uint32_t)__bfloat16_as_ushort(b[2 * k + 1]) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
 cudaError_t prepare_tc_kernels();
 
 }  // namespace ds

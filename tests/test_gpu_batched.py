@@ -117,6 +117,44 @@ def test_batched_llama8b_shape_two_layers_paged(M):
     assert p.g.error_word() == 0
 
 
+@pytest.mark.parametrize("head_dim,layout,kv", [(64, C.ROPE_INTERLEAVED, C.BF16), (32, C.ROPE_HALF_SPLIT, C.BF16),
+                                                (128, C.ROPE_INTERLEAVED, C.F32), (8, C.ROPE_HALF_SPLIT, C.BF16)])
+def test_batched_rope_layouts_and_head_sizes(M, head_dim, layout, kv):
+    """The q|k|v epilogue's cases: runs of 32 features inside one head
+    (interleaved pairs at head_dim 64), runs across the two halves of a head
+    (half-split at 32), an fp32 cache (item by item) and heads narrower than
+    a run (8); 24 sequences at contexts 1..200, 2 steps, and the K/V rows
+    each step wrote."""
+    n_qh = 512 // head_dim
+    cfg = dict(C.LLAMA3_8B, n_layer=2, vocab=3000, d=512, n_qh=n_qh, n_kvh=max(1, n_qh // 4), head_dim=head_dim,
+               ff=768, rope_layout=layout, kv_dtype=kv)
+    ctx = synth.context_lengths(24, 1, 200, seed=31)
+    p = Pair(M, cfg, 24, ctx, 2, block_tokens=16, seed=32)
+    toks = synth.prompt_ids(cfg, 48, seed=33)
+    for t in range(2):
+        got, ref = p.step(toks[24 * t:24 * (t + 1)])
+        _, compared = check_logits_and_ids(p, got, ref)
+        assert compared >= 18
+    row_len = cfg["n_kvh"] * cfg["head_dim"]
+    table = host(p.g.block_table)
+    for s in (0, 11, 23):
+        pos = ctx[s] + 1
+        row = int(table[s][pos // 16]) * 16 + pos % 16
+        for l in range(2):
+            if kv == C.BF16:
+                kg = O.bf16_bits_to_f64(host(p.g.k_cache[l][row]))
+                vg = O.bf16_bits_to_f64(host(p.g.v_cache[l][row]))
+            else:
+                kg = host(p.g.k_cache[l][row]).astype(np.float64)
+                vg = host(p.g.v_cache[l][row]).astype(np.float64)
+            ko = p.o.k[l][row * row_len:(row + 1) * row_len]
+            vo = p.o.v[l][row * row_len:(row + 1) * row_len]
+            if kv == C.BF16:
+                ko, vo = O.bf16_bits_to_f64(ko), O.bf16_bits_to_f64(vo)
+            assert rel_err(kg, ko) <= BF16_TOL and rel_err(vg, vo) <= BF16_TOL
+    assert p.g.error_word() == 0
+
+
 def test_batched_qwen_shape_per_row_sampling(M):
     """Tied Qwen3-0.6B widths, 1 layer, 8 sequences, per-row sampling at
     temperature 0.8 / top_k 50 / top_p 0.95 with one seeded draw per row: the
