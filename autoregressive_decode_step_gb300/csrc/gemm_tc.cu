@@ -126,6 +126,26 @@ __host__ __device__ constexpr uint32_t tc_idesc(int a_mn, int n) {
            ((uint32_t)(kTcBM >> 4) << 24);
 }
 
+// Bounded wait until the counter at ctr reaches target (acquire), giving up
+// once another role has aborted.
+__device__ bool tc_wait_count(const int *ctr, int target, volatile int *abort_flag, int *err) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if ((it & 63u) == 63u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                flag_error(err, DS_ERR_WAIT_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+        __nanosleep(32);
+    }
+}
+
 // Bounded mbarrier wait that also gives up once another role has aborted.
 __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -693,6 +713,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         int seg_i = 0;
         TcSeg sg;
         const int n_chunks = p.n_pad / 32;
+        const size_t sub_floats = (size_t)kTcBM * p.n_pad;
+        int pend[2] = {0, 0}, n_pend = 0;  // split tiles this CTA contributed to, in range order
         if (EPI == TC_QKV) {  // every vector's cache row and position, before any accumulator is awaited
             const int cap = p.max_blocks * p.block_tokens;
             for (int j = et; j < p.n_pad; j += kTcEpiThreads) {
@@ -746,7 +768,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             tc_fence_after();
             const bool whole = sg.kb0 == 0 && sg.kb1 == KB;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * MS * p.n_pad);
-            const size_t sub_floats = (size_t)kTcBM * p.n_pad;
             if (!ok) break;
             if (whole) {
                 for (int h = 0; h < MS; ++h)
@@ -774,51 +795,64 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[buf]);
-                // contributors of this tile: the CTAs holding its first and last unit
-                const long long tu0 = (long long)sg.tile * KB, tu1 = tu0 + KB - 1;
-                const int c_first = (int)(((tu0 + 1) * G - 1) / W);
-                const int c_last = (int)(((tu1 + 1) * G - 1) / W);
+                // this contribution has landed: arrive on the tile's counter
                 __threadfence();
                 named_sync(1, kTcEpiThreads);
-                if (et == 0) {
-                    const int prev = atomicAdd(p.counters + sg.tile, 1);
-                    const bool last = prev == c_last - c_first;
-                    if (last) p.counters[sg.tile] = 0;  // ready for the next launch
-                    s_flags[1] = last ? 1 : 0;
-                }
-                named_sync(1, kTcEpiThreads);
-                if (s_flags[1]) {
-                    __threadfence();
-                    for (int h = 0; h < MS; ++h)
-                        for (int c = 0; c < n_chunks; ++c) {
-                            float v[32], old[32];
-                            if (EPI == TC_ADD) tc_load_residual(p, sg.tile * MS + h, c, r, old);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-                            // up to kTcMaxContrib contributors' partials requested at once,
-                            // added in CTA order
-                            for (int c0 = c_first; c0 <= c_last; c0 += kTcMaxContrib) {
-                                float t[kTcMaxContrib][32];
-#pragma unroll
-                                for (int k = 0; k < kTcMaxContrib; ++k)
-                                    if (c0 + k <= c_last) {
-                                        const float *src =
-                                            p.partials + ((size_t)(c0 + k) + sg.tile) * MS * sub_floats + h * sub_floats;
-#pragma unroll
-                                        for (int i = 0; i < 32; ++i) t[k][i] = __ldcg(src + (size_t)(c * 32 + i) * kTcBM + r);
-                                    }
-#pragma unroll
-                                for (int k = 0; k < kTcMaxContrib; ++k)
-                                    if (c0 + k <= c_last)
-#pragma unroll
-                                        for (int i = 0; i < 32; ++i) v[i] += t[k][i];
-                            }
-                            tc_epilogue_chunk<EPI>(p, sg.tile * MS + h, c, v, old, xch, s_row, s_scale, r);
-                        }
-                }
-                named_sync(1, kTcEpiThreads);
+                if (et == 0) atomicAdd(p.counters + sg.tile, 1);
+                if (n_pend < 2) pend[n_pend++] = sg.tile;
             }
             ++seg_i;
+        }
+        // The split tiles (at most two: the range's first and last segments)
+        // are finished together by their contributors once every partial has
+        // arrived: contributor k of nc takes the tile's 32-vector chunks k,
+        // k + nc, ...  A contributor waits only here, after all of its own
+        // partials have been written, so every wait ends.  The counter then
+        // counts departures on top of the nc arrivals; the last to leave sets
+        // it back to zero for the next launch.
+        for (int pi = n_pend - 1; pi >= 0; --pi) {  // (an abort ends the waits: all threads leave together)
+            const int tile = pend[pi];
+            // contributors of this tile: the CTAs holding its first and last unit
+            const long long tu0 = (long long)tile * KB, tu1 = tu0 + KB - 1;
+            const int c_first = (int)(((tu0 + 1) * G - 1) / W);
+            const int c_last = (int)(((tu1 + 1) * G - 1) / W);
+            const int nc = c_last - c_first + 1, kc = (int)blockIdx.x - c_first;
+            if (et == 0) s_flags[1] = tc_wait_count(p.counters + tile, nc, abort_flag, p.err) ? 1 : 0;
+            named_sync(1, kTcEpiThreads);
+            const bool ready = s_flags[1] != 0;  // one answer for the four warps
+            named_sync(1, kTcEpiThreads);
+            if (!ready) break;
+            __threadfence();
+            for (int task = kc; task < MS * n_chunks; task += nc) {
+                const int h = task / n_chunks, c = task - h * n_chunks;
+                float v[32], old[32];
+                if (EPI == TC_ADD) tc_load_residual(p, tile * MS + h, c, r, old);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                // up to kTcMaxContrib contributors' partials requested at once,
+                // added in CTA order
+                for (int c0 = c_first; c0 <= c_last; c0 += kTcMaxContrib) {
+                    float t[kTcMaxContrib][32];
+#pragma unroll
+                    for (int k = 0; k < kTcMaxContrib; ++k)
+                        if (c0 + k <= c_last) {
+                            const float *src = p.partials + ((size_t)(c0 + k) + tile) * MS * sub_floats + h * sub_floats;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) t[k][i] = __ldcg(src + (size_t)(c * 32 + i) * kTcBM + r);
+                        }
+#pragma unroll
+                    for (int k = 0; k < kTcMaxContrib; ++k)
+                        if (c0 + k <= c_last)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] += t[k][i];
+                }
+                tc_epilogue_chunk<EPI>(p, tile * MS + h, c, v, old, xch, s_row, s_scale, r);
+            }
+            named_sync(1, kTcEpiThreads);
+            if (et == 0) {
+                const int prev = atomicAdd(p.counters + tile, 1);
+                if (prev == 2 * nc - 1) p.counters[tile] = 0;
+            }
         }
     }
 
