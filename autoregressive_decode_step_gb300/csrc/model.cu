@@ -621,7 +621,9 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
         const int S = cfg->max_seqs, es = 2;
         const int nq = cfg->n_qh * cfg->head_dim, nkv = cfg->n_kvh * cfg->head_dim, nqkv = nq + 2 * nkv;
         // pair = 2: two 128-feature sub-tiles per stage share one activation tile
-        // (the large gate|up and head matrices, where tiles are plentiful)
+        // (the large gate|up and head matrices always; q|k|v, o and down up to
+        // 128 vectors, where both accumulators still fit in tensor memory):
+        // an SM's intake per weight byte then carries half the activation bytes
         auto mk = [&](int epi, int a_mn, const void *A0, const void *A1, long long stride, int M, int K, void *X,
                       TcArgs &a, int pair) {
             a = TcArgs{};
@@ -651,7 +653,8 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
         bool ok = true;
         for (int l = 0; l < cfg->n_layer && ok; ++l) {
             TcArgs &q = m->tc[4 * l + 0];
-            ok = ok && mk(TC_QKV, 1, m->wqkv[l], nullptr, (long long)nqkv * es, nqkv, cfg->d, m->h_bf, q, 1);
+            const int pair_small = tc_n_pad(S) <= 128 ? 2 : 1;
+            ok = ok && mk(TC_QKV, 1, m->wqkv[l], nullptr, (long long)nqkv * es, nqkv, cfg->d, m->h_bf, q, pair_small);
             q.y = m->q;
             q.ldy = nq;
             q.rope_cos = m->rope_cos;
@@ -666,7 +669,7 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
             q.k_norm = qk_norm ? w->k_norm[l] : nullptr;
             q.qk_eps = cfg->eps;
             TcArgs &o = m->tc[4 * l + 1];
-            ok = ok && mk(TC_ADD, 1, m->wo[l], nullptr, (long long)cfg->d * es, cfg->d, nq, m->att_bf, o, 1);
+            ok = ok && mk(TC_ADD, 1, m->wo[l], nullptr, (long long)cfg->d * es, cfg->d, nq, m->att_bf, o, pair_small);
             o.y = m->x;
             o.ldy = cfg->d;
             TcArgs &gu = m->tc[4 * l + 2];
@@ -676,7 +679,7 @@ extern "C" DS_API int ds_model_create(const ds_model_config *cfg, const ds_model
             gu.yb_lo = (long long)S * cfg->ff;
             gu.ldy = cfg->ff;
             TcArgs &dn = m->tc[4 * l + 3];
-            ok = ok && mk(TC_ADD, 1, m->wd[l], nullptr, (long long)cfg->d * es, cfg->d, cfg->ff, m->f_bf, dn, 1);
+            ok = ok && mk(TC_ADD, 1, m->wd[l], nullptr, (long long)cfg->d * es, cfg->d, cfg->ff, m->f_bf, dn, pair_small);
             dn.y = m->x;
             dn.ldy = cfg->d;
             // RMSNorms folded into the projections: o and down also write the
