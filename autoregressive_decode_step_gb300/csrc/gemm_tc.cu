@@ -32,12 +32,15 @@
 //
 // Work split: the (tile, k-block) units are cut into equal contiguous ranges,
 // one per CTA (every CTA streams the same weight bytes whatever the shape).
-// A tile whose k-blocks fall to several CTAs is finished by the last of them
-// to arrive (an atomic counter, never a wait): it adds the partial
-// accumulators the contributors left in the workspace in CTA order, so results
-// are bit-stable run to run.  Every mbarrier wait is bounded; a wait that
-// times out flags DS_ERR_WAIT_TIMEOUT and the kernel winds down, draining its
-// copies and MMAs in flight and freeing its tensor memory before it exits.
+// A tile whose k-blocks fall to several CTAs is finished by all of them
+// together: each writes its partial accumulator to the workspace and arrives
+// on the tile's counter; at the end of its range each contributor waits
+// (bounded) for its split tiles to be complete and finishes its share of
+// their 32-vector chunks, adding the partials in CTA order, so results are
+// bit-stable run to run whoever finishes a chunk.  Every wait (mbarrier or
+// counter) is bounded; a wait that times out flags DS_ERR_WAIT_TIMEOUT and
+// the kernel winds down, draining its copies and MMAs in flight and freeing
+// its tensor memory before it exits.
 #include <algorithm>
 
 #include "common.cuh"
@@ -54,7 +57,7 @@ constexpr int kTcMaxStages = 8;
 constexpr int kTcXchStride = 33;  // floats per feature row of the epilogue exchange buffer
 constexpr int kTcMaxN = 256;      // vectors per launch (the MMA's largest N)
 constexpr int kTcSmemInts = 16 + 3 * kTcMaxN;  // tmem address, flags, agreement words, per-vector rows, scales
-constexpr int kTcMaxContrib = 4;  // split partials a last arriver requests at once
+constexpr int kTcMaxContrib = 4;  // split partials one chunk's reduction requests at once
 constexpr size_t kTcSmemLimit = 227 * 1024;
 
 // ---------------------------------------------------------------- tcgen05 PTX
